@@ -1,0 +1,203 @@
+"""Pins of the oracle's cache model: StreamingLLM cap, ring vs compact, keep-set, gates, bytes."""
+import numpy as np
+import pytest
+
+from oracle import accounting as acc
+from oracle import attention as att
+from oracle import quantize as qz
+from oracle.cache import CacheSpec, OracleCache, ring_slot, streaming_survivors
+
+
+def _pos_tokens(positions, D=32):
+    """fp32 K/V rows [1,1,n,D] that carry their own absolute position exactly in fp16."""
+    p = np.asarray(positions, np.float32)
+    x = np.zeros((1, 1, len(p), D), np.float32)
+    x[0, 0, :, 0] = np.floor(p / 1024)
+    x[0, 0, :, 1] = p % 1024
+    return x
+
+
+def _positions_of(cache):
+    kh, _ = cache.dequant()
+    return (kh[0, 0, :, 0] * 1024 + kh[0, 0, :, 1]).astype(np.int64)
+
+
+def _streaming_cache(layout, sink, window):
+    cap = sink + window + (1 if layout == "compact" else 0)
+    return OracleCache(CacheSpec(batch=1, n_kv_heads=1, head_dim=32, capacity=cap, layout=layout,
+                                 sink=sink, window=window))
+
+
+def _decode(cache, n_steps, start=0):
+    for p in range(start, start + n_steps):
+        t = _pos_tokens([p])
+        cache.append(t, t)
+        cache.evict_middle()
+
+
+@pytest.mark.parametrize("n", [1, 259, 260, 261, 500])
+def test_streaming_cap_page_example(golden, n):
+    g = golden("streaming_kivi_page.json")["streaming_cap"]
+    sink, window = g["sink"], g["window"]
+    for layout in ("compact", "ring"):
+        c = _streaming_cache(layout, sink, window)
+        _decode(c, n)
+        assert c.stored == min(n, g["stored"])
+        assert c.pos == n
+        got = sorted(_positions_of(c).tolist())
+        assert got == streaming_survivors(n, sink, window)
+    if n == g["tokens_generated"]:
+        assert c.stored == g["stored"]
+
+
+def test_streaming_closed_form_survivors():
+    assert streaming_survivors(3, 4, 256) == [0, 1, 2]
+    s = streaming_survivors(40000, 4, 256)
+    assert s[:4] == [0, 1, 2, 3] and s[4:] == list(range(40000 - 256, 40000)) and len(s) == 260
+
+
+def test_compact_keeps_logical_order_and_ring_keeps_slots():
+    c = _streaming_cache("compact", 4, 16)
+    r = _streaming_cache("ring", 4, 16)
+    _decode(c, 100)
+    _decode(r, 100)
+    # compact: concatenation in logical order
+    assert _positions_of(c).tolist() == streaming_survivors(100, 4, 16)
+    # ring: each survivor sits in its closed-form slot
+    got = _positions_of(r)
+    for slot, p in enumerate(got.tolist()):
+        assert ring_slot(p, 4, 16) == slot
+
+
+@pytest.mark.slow
+def test_long_run_simulation_equals_closed_form():
+    # 40 000 single-token steps with one eviction each (reduced instance).
+    r = _streaming_cache("ring", 4, 4096)
+    _decode(r, 40000)
+    assert sorted(_positions_of(r).tolist()) == streaming_survivors(40000, 4, 4096)
+    c = _streaming_cache("compact", 4, 256)
+    _decode(c, 40000)
+    assert _positions_of(c).tolist() == streaming_survivors(40000, 4, 256)
+
+
+def test_ring_bulk_append_equals_sequential():
+    a = _streaming_cache("ring", 4, 16)
+    b = _streaming_cache("ring", 4, 16)
+    t = _pos_tokens(range(0, 57))
+    a.append(t, t)
+    _decode(b, 57)
+    np.testing.assert_array_equal(a.k.rows[:, :, :a.stored], b.k.rows[:, :, :b.stored])
+    assert a.stored == b.stored == 20 and a.pos == b.pos == 57
+
+
+def test_evict_moves_per_token_metadata_not_channel_scales():
+    rng = np.random.default_rng(4)
+    spec = CacheSpec(batch=2, n_kv_heads=2, head_dim=32, capacity=4 + 8 + 1, layout="compact", sink=4, window=8,
+                     k_format="kivi_chan", k_bits=8, v_format="affine_token", v_bits=8, v_group=32)
+    c = OracleCache(spec)
+    fill_k = rng.standard_normal((2, 2, 12, 32)).astype(np.float32)
+    fill_v = rng.standard_normal((2, 2, 12, 32)).astype(np.float32)
+    c.calibrate_k(fill_k)
+    c.append(fill_k, fill_v)
+    ch_s, ch_z = c.k.ch_scale.copy(), c.k.ch_zero.copy()
+    vs_before = c.v.tok_scale[:, :, :12].copy()
+    k_new = rng.standard_normal((2, 2, 1, 32)).astype(np.float32)
+    c.append(k_new, k_new)
+    c.evict_middle()
+    assert c.stored == 12
+    np.testing.assert_array_equal(c.k.ch_scale, ch_s)
+    np.testing.assert_array_equal(c.k.ch_zero, ch_z)
+    # rows [0,4) unchanged, rows [4,11) were rows [5,12), row 11 is the new token
+    np.testing.assert_array_equal(c.v.tok_scale[:, :, :4], vs_before[:, :, :4])
+    np.testing.assert_array_equal(c.v.tok_scale[:, :, 4:11], vs_before[:, :, 5:12])
+
+
+def test_keepset_gather_and_true_offset():
+    rng = np.random.default_rng(8)
+    S = 40
+    spec = CacheSpec(batch=1, n_kv_heads=2, head_dim=32, capacity=S + 5)
+    c = OracleCache(spec)
+    k = rng.standard_normal((1, 2, S, 32)).astype(np.float16).astype(np.float32)
+    c.append(k, k)
+    idx = np.stack([np.sort(rng.choice(S, 10, replace=False)) for _ in range(2)])[None].astype(np.int32)
+    before = c.k.rows[:, :, :S].copy()
+    c.evict_keepset(idx)
+    assert c.stored == 10 and c.pos == S
+    for h in range(2):
+        np.testing.assert_array_equal(c.k.rows[0, h, :10], before[0, h, idx[0, h]])
+    # decode after the keep-set appends at the true position and never evicts
+    t = rng.standard_normal((1, 2, 1, 32)).astype(np.float32)
+    c.append(t, t)
+    assert c.stored == 11 and c.pos == S + 1
+
+
+def test_bias_gate_and_disabled_centering_is_a_no_op():
+    rng = np.random.default_rng(12)
+    with pytest.raises(ValueError):
+        OracleCache(CacheSpec(batch=1, n_kv_heads=2, head_dim=32, capacity=4, k_format="affine_token",
+                              k_bits=4, k_group=32, k_bias=np.zeros((2, 32), np.float32)))
+    k = (rng.standard_normal((1, 2, 6, 64)) * 3).astype(np.float32)
+    base = dict(batch=1, n_kv_heads=2, head_dim=64, capacity=8, k_format="q4_0", k_bits=4, k_group=32)
+    a = OracleCache(CacheSpec(**base))
+    b = OracleCache(CacheSpec(**base, k_bias=np.zeros((2, 64), np.float32)))
+    a.append(k, k)
+    b.append(k, k)
+    np.testing.assert_array_equal(a.k.rows, b.k.rows)
+    np.testing.assert_array_equal(a.k.tok_scale.view(np.uint16), b.k.tok_scale.view(np.uint16))
+    u, d = qz.q4_0_quantize(k)
+    np.testing.assert_array_equal(a.k.rows[:, :, :6], qz.pack_nibbles(u))
+
+
+def test_mean_centering_softmax_invariance(golden):
+    # "kv-cache ... mean-centering for Q4_0", "Why this is safe": subtracting
+    # the same kbar from every key adds q . kbar to every logit of a row; the
+    # softmax does not see it.  Checked on an unquantised fp32 K cache.
+    bound = golden("mean_center_page.json")["invariance"]["nmse_bound_used"]
+    rng = np.random.default_rng(13)
+    B, Hkv, G, T, D = 2, 4, 3, 300, 64
+    k = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    kbar = (rng.standard_normal((Hkv, D)) * 1.5).astype(np.float32)
+    k = k + kbar[None, :, None, :]
+    v = rng.standard_normal((B, Hkv, T, D))
+    q = rng.standard_normal((B, Hkv * G, D))
+    o_ref = att.decode_attention(q, k, v)
+    o_c = att.decode_attention(q, qz.mean_center(k, kbar), v)
+    nmse = np.sum((o_c - o_ref) ** 2) / np.sum(o_ref ** 2)
+    assert nmse <= bound
+    # negative control: a bias that varies by token is not invisible
+    o_bad = att.decode_attention(q, k - rng.standard_normal((1, 1, T, 1)) * kbar[None, :, None, :], v)
+    assert np.sum((o_bad - o_ref) ** 2) / np.sum(o_ref ** 2) > 1e-4
+
+
+def test_page_byte_accounting(golden):
+    g = golden("streaming_kivi_page.json")
+    f = g["flagship_huge_bytes"]
+    L, H, D, T = f["layers"], f["heads"], f["head_dim"], f["T"]
+    assert round(acc.dense_cache_bytes(L, H, T, D, 2) / 1e6, 1) == f["bf16_total_bytes_MB"]
+    assert acc.side_fixed_bytes("kivi_chan", D) * L * H // 2 == f["kScales_bytes_each_KB"] * 1024
+    assert L * H * T * 2 == f["vScales_bytes_each_KB"] * 1000
+    assert round(acc.kivi_cache_bytes(L, H, T, D, 8) / 1e6, 1) == f["int8_kivi_total_MB"]
+    s = g["smoke_100_tokens"]
+    assert round(acc.kivi_cache_bytes(s["layers"], s["heads"], s["T"], s["head_dim"], 8) / 1e3) == s["int8_kivi_KB"]
+    assert round(acc.dense_cache_bytes(s["layers"], s["heads"], s["T"], s["head_dim"], 4) / 1e6, 1) == s["unquantised_MB"]
+
+
+def test_bits_per_element(golden):
+    g = golden("mlx_memo_page.json")
+    assert acc.bits_per_element(4, 64) == g["bits_per_element"]["g64_4bit"]
+    assert acc.bits_per_element(4, 32) == g["bits_per_element"]["g32_4bit"]
+    extra = acc.bits_per_element(4, 32) / acc.bits_per_element(4, 64) - 1
+    assert round(extra, 2) == g["bits_per_element"]["extra_fraction_g32_vs_g64"]
+    assert round(16 / acc.bits_per_element(4, 64), 1) == g["reduction_vs_fp16"]["g64_4bit"]
+    assert round(16 / acc.bits_per_element(3, 64), 1) == g["reduction_vs_fp16"]["g64_3bit"]
+    # the per-format byte counts agree with the bits-per-element rule
+    assert acc.side_bytes_per_token("affine_token", 4, 64, 128) * 8 / 128 == acc.bits_per_element(4, 64)
+    assert acc.side_bytes_per_token("affine_token", 4, 32, 128) * 8 / 128 == acc.bits_per_element(4, 32)
+
+
+def test_decode_read_bytes_of_the_workloads():
+    # codes + metadata + Q + O of one decode-attention call, per layer
+    assert acc.decode_read_bytes(1, 8, 8, 32, 260, "kivi_chan", 8, 0, "affine_token", 8, 32, 4) == 144512
+    assert acc.decode_read_bytes(1, 8, 24, 128, 8192, "affine_token", 4, 64, "affine_token", 4, 64, 2) == 9449472
+    assert acc.decode_read_bytes(8, 8, 32, 128, 32768, "q4_0", 4, 32, "affine_token", 8, 128, 2) == 427950080
+    assert acc.decode_read_bytes(64, 8, 32, 128, 4100, "kivi_chan", 4, 0, "affine_token", 4, 32, 2) == 303595520
