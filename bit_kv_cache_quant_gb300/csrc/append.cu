@@ -1,0 +1,268 @@
+// Quantise-on-append kernels.
+//
+// "StreamingLLM + KIVI" page, "Affine quantisation formula" and "KIVI": keys
+// per channel, values per token, scale = max(eps, (max - min)/(qMax - qMin)),
+// zero = min, codes round((x - zero)/scale) clamped to the level range.
+// "Low-bit KV caches on MLX", section 1: the same affine rule per token and
+// per 64-channel group.  "kv-cache: optional per-channel K-cache
+// mean-centering for Q4_0": subtract the per-(kv head, channel) bias, then
+// quantise symmetric 32-channel blocks.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// Per-channel K calibration: min / max over the n tokens of one (b, kv head),
+// then the fp32 scale / zero that codes are computed from and their fp16
+// stored copies.  One CTA of 256 threads per (b, kv head); 256 % D == 0.
+template <typename T>
+__global__ void __launch_bounds__(256) calibrate_kivi_kernel(CacheView c, const T* __restrict__ k, int n) {
+  __shared__ float smn[256];
+  __shared__ float smx[256];
+  const int D = c.D;
+  const int bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int d = tid % D;
+  const int tg = tid / D;
+  const int ntg = blockDim.x / D;
+  float mn = __int_as_float(0x7f800000);   // +inf
+  float mx = __int_as_float(0xff800000);   // -inf
+  const T* base = k + (size_t)bh * n * D;
+  for (int t = tg; t < n; t += ntg) {
+    float x = In<T>::ld(base + (size_t)t * D + d);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  smn[tid] = mn;
+  smx[tid] = mx;
+  __syncthreads();
+  if (tg == 0) {
+    for (int i = 1; i < ntg; ++i) {
+      mn = fminf(mn, smn[i * D + d]);
+      mx = fmaxf(mx, smx[i * D + d]);
+    }
+    const float levels = (c.k.bits == 8) ? 255.0f : 15.0f;
+    const float s = affine_scale(mn, mx, levels);
+    const size_t o = (size_t)bh * D + d;
+    c.k.ch_scale32[o] = s;
+    c.k.ch_zero32[o] = mn;
+    c.k.ch_scale[o] = __float2half_rn(s);
+    c.k.ch_zero[o] = __float2half_rn(mn);
+  }
+  if (blockIdx.x == 0 && tid == 0) c.state->k_calibrated = 1;
+}
+
+// ---------------------------------------------------------------------------
+// Row quantiser: one warp codes one token row of D = 32 * E channels; lane l
+// holds channels [l*E, l*E + E).
+
+template <int E>
+__device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[E]) {
+  if constexpr (E == 1) {
+    dst[0] = b[0];
+  } else if constexpr (E == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(b[0] | (b[1] << 8));
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; i += 4) {
+      *reinterpret_cast<uint32_t*>(dst + i) = (uint32_t)b[i] | ((uint32_t)b[i + 1] << 8) |
+                                              ((uint32_t)b[i + 2] << 16) | ((uint32_t)b[i + 3] << 24);
+    }
+  }
+}
+
+// Writes the lane's E codes u (0..levels) in the side's storage encoding.
+template <int E>
+__device__ __forceinline__ void store_codes(uint8_t* row, int lane, int bits, const int (&u)[E]) {
+  if (bits == 8) {
+    uint8_t b[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) b[i] = (uint8_t)(u[i] ^ 0x80);   // signed level q = u - 128
+    store_bytes<E>(row + lane * E, b);
+  } else {  // 4-bit: channel 2j in the low nibble of byte j
+    if constexpr (E == 1) {
+      const int nb = __shfl_down_sync(0xffffffffu, u[0], 1);
+      if ((lane & 1) == 0) row[lane >> 1] = (uint8_t)(u[0] | (nb << 4));
+    } else {
+      uint8_t b[E / 2];
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) b[i] = (uint8_t)(u[2 * i] | (u[2 * i + 1] << 4));
+      store_bytes<E / 2>(row + lane * (E / 2), b);
+    }
+  }
+}
+
+// Max / min over the `width` lanes (a power of two) of the lane's group.
+__device__ __forceinline__ float group_max(float x, int width) {
+  for (int o = 1; o < width; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float group_min(float x, int width) {
+  for (int o = 1; o < width; o <<= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+template <typename T, int E>
+__device__ __forceinline__ void quantize_row(const SideView& s, const float* __restrict__ bias, const T* __restrict__ src,
+                                             size_t bh, int cap_alloc, int slot, int lane) {
+  float x[E];
+  load_row_slice<T, E>(src + lane * E, x);
+  uint8_t* row = s.codes + ((size_t)bh * cap_alloc + slot) * s.row_bytes;
+  const size_t meta_row = ((size_t)bh * cap_alloc + slot) * s.n_groups;
+
+  if (s.fmt == KVQ_FMT_FP16) {
+    __half* dst = reinterpret_cast<__half*>(row) + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(x[i]);
+    return;
+  }
+
+  const float levels = (s.bits == 8) ? 255.0f : 15.0f;
+  int u[E];
+
+  if (s.fmt == KVQ_FMT_KIVI_CHAN) {
+    const float* sc = s.ch_scale32 + bh * (32 * E) + lane * E;
+    const float* zr = s.ch_zero32 + bh * (32 * E) + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) u[i] = affine_code(x[i], sc[i], zr[i], levels);
+    store_codes<E>(row, lane, s.bits, u);
+    return;
+  }
+
+  if (s.fmt == KVQ_FMT_AFFINE_TOKEN) {
+    const int width = s.group / E;           // lanes per group
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < E; ++i) {
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
+    }
+    mn = group_min(mn, width);
+    mx = group_max(mx, width);
+    const float sc = affine_scale(mn, mx, levels);
+#pragma unroll
+    for (int i = 0; i < E; ++i) u[i] = affine_code(x[i], sc, mn, levels);
+    store_codes<E>(row, lane, s.bits, u);
+    if (lane % width == 0) {
+      const int g = lane / width;
+      s.tok_scale[meta_row + g] = __float2half_rn(sc);
+      s.tok_zero[meta_row + g] = __float2half_rn(mn);
+    }
+    return;
+  }
+
+  // KVQ_FMT_Q4_0: optional centering, then symmetric 32-channel blocks.
+  if (bias != nullptr) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = __fsub_rn(x[i], bias[lane * E + i]);
+  }
+  const int width = 32 / E;
+  float a = fabsf(x[0]);
+#pragma unroll
+  for (int i = 1; i < E; ++i) a = fmaxf(a, fabsf(x[i]));
+  a = group_max(a, width);
+  const float d = __fdiv_rn(a, 7.0f);
+#pragma unroll
+  for (int i = 0; i < E; ++i) u[i] = q40_code(x[i], d);
+  store_codes<E>(row, lane, 4, u);
+  if (lane % width == 0) s.tok_scale[meta_row + lane / width] = __float2half_rn(d);
+}
+
+// One warp per (b, kv head, token) row of the append; 4 warps per CTA.
+template <typename T, int E>
+__global__ void __launch_bounds__(128) append_kernel(CacheView c, const T* __restrict__ k, const T* __restrict__ v,
+                                                     int n, long long rows) {
+  __shared__ long long s_pos;
+  __shared__ int s_stored;
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    s_pos = c.state->pos;
+    s_stored = c.state->stored;
+    const bool ok = (c.layout == KVQ_LAYOUT_RING) || (s_stored + n <= c.cap);
+    s_ok = ok ? 1 : 0;
+    if (!ok && blockIdx.x == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + warp;
+  if (s_ok && row < rows) {
+    const int i = (int)(row % n);
+    const long long bh = row / n;
+    const int kvh = (int)(bh % c.Hkv);
+    const long long p = s_pos + i;
+    bool write = true;
+    int slot;
+    if (c.layout == KVQ_LAYOUT_RING) {
+      if (p < c.sink) {
+        slot = (int)p;
+      } else {
+        // a later token of this same append lands in the slot: skip this one
+        write = p >= s_pos + n - c.window;
+        slot = c.sink + (int)((p - c.sink) % c.window);
+      }
+    } else {
+      slot = s_stored + i;
+    }
+    if (write) {
+      const float* bias = c.k_bias ? c.k_bias + (size_t)kvh * c.D : nullptr;
+      quantize_row<T, E>(c.k, bias, k + row * c.D, bh, c.cap_alloc, slot, lane);
+      quantize_row<T, E>(c.v, nullptr, v + row * c.D, bh, c.cap_alloc, slot, lane);
+    }
+  }
+  // The last CTA to arrive advances the counters (every CTA has read them).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&c.state->append_arrive, 1u);
+    if (prev == gridDim.x - 1) {
+      if (s_ok) {
+        const long long np = s_pos + n;
+        c.state->pos = np;
+        if (c.layout == KVQ_LAYOUT_RING) {
+          const long long w = (long long)c.sink + c.window;
+          c.state->stored = (int)(np < w ? np : w);
+        } else {
+          c.state->stored = s_stored + n;
+        }
+      }
+      c.state->append_arrive = 0u;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launch --
+
+template <typename T>
+static cudaError_t launch_append_t(const CacheView& c, const void* k, const void* v, int n, bool calibrate,
+                                   cudaStream_t st) {
+  if (calibrate) {
+    calibrate_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n);
+    note_launch();
+  }
+  const long long rows = (long long)c.B * c.Hkv * n;
+  const unsigned grid = (unsigned)((rows + 3) / 4);
+  const T* kk = static_cast<const T*>(k);
+  const T* vv = static_cast<const T*>(v);
+  switch (c.D) {
+    case 32: append_kernel<T, 1><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
+    case 64: append_kernel<T, 2><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
+    case 128: append_kernel<T, 4><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, int in_dtype, bool calibrate,
+                          cudaStream_t st) {
+  switch (in_dtype) {
+    case KVQ_DTYPE_F32: return launch_append_t<float>(c, k, v, n, calibrate, st);
+    case KVQ_DTYPE_BF16: return launch_append_t<__nv_bfloat16>(c, k, v, n, calibrate, st);
+    case KVQ_DTYPE_F16: return launch_append_t<__half>(c, k, v, n, calibrate, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,148 @@
+// Internal definitions shared by the kvq kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kRowAlign = 64;      // cap_alloc granularity: whole tiles are always in bounds
+constexpr int kPlaneAlign = 256;   // byte alignment of every plane
+
+// Device-resident counters of one cache (first 256 bytes of the cache buffer).
+struct DevState {
+  long long pos;            // absolute position of the next token
+  int stored;               // rows holding live tokens
+  int status;               // first KVQ_DEV_* error, 0 if none
+  unsigned append_arrive;   // CTA arrival counter of the append in flight
+  unsigned evict_arrive;    // CTA arrival counter of the eviction in flight
+  int k_calibrated;         // per-channel K scales frozen
+  int pad[57];
+};
+static_assert(sizeof(DevState) == 256, "DevState must be 256 bytes");
+
+// Format codes used as template parameters of the decode kernels.
+enum Fmt : int {
+  F_FP16 = 0,
+  F_KIVI8 = 1,
+  F_KIVI4 = 2,
+  F_AFF8 = 3,
+  F_AFF4 = 4,
+  F_Q40 = 5,
+};
+
+struct SideView {
+  uint8_t* codes;        // [B][Hkv][cap_alloc][row_bytes]
+  __half* tok_scale;     // [B][Hkv][cap_alloc][n_groups]
+  __half* tok_zero;      // [B][Hkv][cap_alloc][n_groups]
+  __half* ch_scale;      // [B][Hkv][D]
+  __half* ch_zero;       // [B][Hkv][D]
+  float* ch_scale32;     // [B][Hkv][D]
+  float* ch_zero32;      // [B][Hkv][D]
+  int fmt;               // kvq_format
+  int bits;
+  int group;             // channels per (scale, zero) group
+  int row_bytes;
+  int n_groups;          // per-token metadata entries per row
+};
+
+struct CacheView {
+  DevState* state;
+  unsigned* split_sem;   // [B*Hkv]
+  const float* k_bias;   // [Hkv][D] or null
+  SideView k, v;
+  int B, Hkv, D, cap, cap_alloc, layout, sink, window;
+};
+
+__device__ __forceinline__ void set_status(DevState* st, int code) {
+  atomicCAS(&st->status, 0, code);
+}
+
+// ------------------------------------------------------------ input loads --
+
+template <typename T> struct In;
+template <> struct In<float> {
+  static __device__ __forceinline__ float ld(const float* p) { return *p; }
+};
+template <> struct In<__nv_bfloat16> {
+  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+};
+template <> struct In<__half> {
+  static __device__ __forceinline__ float ld(const __half* p) { return __half2float(*p); }
+};
+
+// Reads E consecutive input elements as fp32 (exact for bf16 / fp16 inputs).
+template <typename T, int E>
+__device__ __forceinline__ void load_row_slice(const T* p, float (&x)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; ++i) x[i] = In<T>::ld(p + i);
+}
+
+// Loads element i of an io-dtype tensor as fp32; stores fp32 as io dtype (RNE).
+__device__ __forceinline__ float load_io(const void* p, size_t i, int dtype) {
+  if (dtype == KVQ_DTYPE_F32) return static_cast<const float*>(p)[i];
+  if (dtype == KVQ_DTYPE_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  return __half2float(static_cast<const __half*>(p)[i]);
+}
+__device__ __forceinline__ void store_io(void* p, size_t i, int dtype, float x) {
+  if (dtype == KVQ_DTYPE_F32) static_cast<float*>(p)[i] = x;
+  else if (dtype == KVQ_DTYPE_BF16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+  else static_cast<__half*>(p)[i] = __float2half_rn(x);
+}
+
+// -------------------------------------------------------- exact arithmetic --
+// The quantiser's decisions: IEEE fp32, round to nearest even, no contraction.
+
+__device__ __forceinline__ float affine_scale(float mn, float mx, float levels) {
+  return fmaxf(1e-5f, __fdiv_rn(__fsub_rn(mx, mn), levels));
+}
+
+__device__ __forceinline__ int affine_code(float x, float scale, float zero, float levels) {
+  float t = __fdiv_rn(__fsub_rn(x, zero), scale);
+  float u = fminf(fmaxf(rintf(t), 0.0f), levels);
+  return (int)u;
+}
+
+// Symmetric Q4_0 nibble: d == 0 stores level 0 (nibble 8).
+__device__ __forceinline__ int q40_code(float x, float d) {
+  if (d == 0.0f) return 8;
+  float t = __fdiv_rn(x, d);
+  float q = fminf(fmaxf(rintf(t), -8.0f), 7.0f);
+  return (int)q + 8;
+}
+
+// Counts kernels enqueued by the current API call (host side, per thread).
+void note_launch(int n = 1);
+
+// Launchers (defined in the kernel files).
+cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, int in_dtype, bool calibrate,
+                          cudaStream_t st);
+cudaError_t launch_evict_middle(const CacheView& c, cudaStream_t st);
+cudaError_t launch_evict_keepset(const CacheView& c, const int* idx, int n_keep, cudaStream_t st);
+
+struct DecodeArgs {
+  const void* q;
+  void* out;
+  int io_dtype;
+  int Hq;
+  float qscale;      // softmax scale * log2(e)
+  float* partials;   // [B*Hkv][nsplit][G][D+2] or null when nsplit == 1
+  int nsplit;
+};
+// Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
+// an (D, G) outside the instantiated set.
+template <int KF, int VF>
+cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st);
+
+cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, int S, int D, int w, int budget,
+                          int n_sink, float* scores, int* idx, float2* stats, int nchunk, cudaStream_t st);
+cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
+                        cudaStream_t st);
+
+constexpr int kSnapChunk = 512;   // keys per CTA of the SnapKV scoring kernels
+
+}  // namespace kvq

@@ -1,0 +1,256 @@
+/*
+ * kvq.h -- C ABI of the GB300 compressed KV cache for single-token LLM decode.
+ *
+ * The library quantises keys and values into a low-bit cache as they are
+ * appended, evicts tokens (StreamingLLM sink + window, SnapKV keep-sets),
+ * and runs grouped-query decode attention that reads the packed codes
+ * directly.  It also scores and selects SnapKV keep-sets from a prompt's keys.
+ *
+ * Sources, cited by page title and section:
+ *   [SLK]  "StreamingLLM + KIVI -- long-context decode without growing the KV
+ *          cache" (tinygpt docs)
+ *   [SKV]  "SnapKV -- Prefill Observation-Window Token Eviction"
+ *          (veloxquant-mlx docs)
+ *   [KMC]  "kv-cache: optional per-channel K-cache mean-centering for Q4_0"
+ *          (llama.cpp PR #51)
+ *   [MLX]  "Low-bit KV caches on MLX: what exists and what is missing"
+ *
+ * Conventions shared by every call
+ *   - Pointers marked "device" must point to memory of the current CUDA
+ *     device; pointers marked "host" to host memory.  The caller owns and
+ *     allocates all device memory (cache buffer, workspaces); the library
+ *     allocates none.  A kvq_cache handle is a small host-side object created
+ *     by kvq_cache_init and freed by kvq_cache_release.
+ *   - Calls that take a cudaStream_t are asynchronous and stream-ordered:
+ *     they validate their host-side arguments, enqueue kernels and return.
+ *     A host-side validation failure returns an error before anything is
+ *     enqueued.  NULL means the legacy default stream.
+ *   - The cache's counters (absolute position, stored rows) live in device
+ *     memory and are advanced by the kernels, so a captured CUDA graph of
+ *     append / evict / decode replays correctly.  Conditions only the device
+ *     can see (capacity overflow, a malformed keep-set) set a device status
+ *     word instead of trapping; kvq_stats_read reports it.
+ *   - Tensors are dense and row-major with the last dimension contiguous.
+ *     B = batch, Hkv = kv heads, Hq = query heads (a multiple of Hkv),
+ *     D = head_dim, n = tokens in a call, S = prompt length.  Query head h
+ *     attends with kv head h / (Hq / Hkv).
+ *   - No call throws; errors are returned as kvq_status with a message
+ *     available from kvq_last_error() on the calling thread.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_ABI_VERSION 1
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* bad shape, pointer, size or mode                       */
+  KVQ_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement, or a
+                                K bias with non-Q4_0 keys ([KMC] "What's included":
+                                the bias is gated to Q4_0 K caches, a mismatch fails) */
+  KVQ_ERR_CAPACITY = 3,      /* buffer or workspace too small                          */
+  KVQ_ERR_DEVICE = 4,        /* the device status word reports an error                */
+  KVQ_ERR_CUDA = 5           /* a CUDA runtime call failed                             */
+} kvq_status;
+
+/* Storage format of one side (K or V) of the cache. */
+typedef enum kvq_format {
+  /* raw fp16 rows, 2 bytes per element ([SKV] "How it works": kept rows stay fp16) */
+  KVQ_FMT_FP16 = 0,
+  /* KIVI keys: asymmetric, one (scale, zero) per (b, kv head, channel) shared by all
+     tokens, computed once from the tokens of a calibrating append and then frozen
+     ([SLK] "KIVI", "Affine quantisation formula").  bits 8 or 4.  K side only.   */
+  KVQ_FMT_KIVI_CHAN = 1,
+  /* asymmetric, one (scale, zero) per (b, kv head, token, group of `group`
+     consecutive channels): KIVI values with group = D ([SLK] "KIVI"), mlx-lm's
+     QuantizedKVCache with group = 64 ([MLX] section 1).  bits 8 or 4; group a
+     multiple of 16 dividing D.                                                      */
+  KVQ_FMT_AFFINE_TOKEN = 2,
+  /* symmetric 32-channel blocks, one fp16 scale, no zero point ([KMC] "The idea").
+     bits 4, group 32.  K side only; the only format that accepts a K bias.        */
+  KVQ_FMT_Q4_0 = 3
+} kvq_format;
+
+typedef enum kvq_layout {
+  KVQ_LAYOUT_LINEAR = 0,   /* rows appended in order; no middle eviction (SnapKV, plain) */
+  KVQ_LAYOUT_COMPACT = 1,  /* sink + window, evicted rows removed by moving the window down
+                              ([SLK] "Implementation": concatenate [0, sink) and
+                              [len - window, len))                                       */
+  KVQ_LAYOUT_RING = 2      /* sink + window; position p >= sink lives in slot
+                              sink + (p - sink) mod window, nothing moves                 */
+} kvq_layout;
+
+typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1, KVQ_DTYPE_F16 = 2 } kvq_dtype;
+
+typedef enum kvq_evict_mode {
+  KVQ_EVICT_MIDDLE = 0,    /* StreamingLLM: drop logical [sink, len - window) */
+  KVQ_EVICT_KEEPSET = 1    /* SnapKV: keep an ascending index set per (b, kv head) */
+} kvq_evict_mode;
+
+/* kvq_append flags */
+#define KVQ_APPEND_CALIBRATE_K 1   /* KIVI_CHAN keys: compute and freeze the per-channel
+                                      scales from this call's tokens before coding them */
+
+/* Device status codes (kvq_stats.device_status). */
+#define KVQ_DEV_OK 0
+#define KVQ_DEV_OVERFLOW 1         /* an append would pass the capacity; nothing was written */
+#define KVQ_DEV_BAD_KEEPSET 2      /* keep-set not strictly ascending or beyond stored rows */
+
+typedef struct kvq_config {
+  int32_t batch;        /* B >= 1 */
+  int32_t n_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;     /* D in {32, 64, 128} */
+  int32_t capacity;     /* rows per (b, kv head); COMPACT needs >= sink + window + the
+                           largest append, RING uses exactly sink + window */
+  int32_t layout;       /* kvq_layout */
+  int32_t sink;         /* StreamingLLM sink tokens (COMPACT / RING) */
+  int32_t window;       /* StreamingLLM window tokens (COMPACT / RING), >= 1 */
+  int32_t k_format, k_bits, k_group;   /* kvq_format, 16/8/4, channels per group */
+  int32_t v_format, v_bits, v_group;   /* FP16 or AFFINE_TOKEN */
+  /* device fp32 [Hkv, D] per-(kv head, channel) mean subtracted from K right before it
+     is quantised ([KMC] "Summary"); NULL disables centering.  Copied into the cache
+     buffer by kvq_cache_init.  Only legal with KVQ_FMT_Q4_0 keys. */
+  const float* k_bias;
+} kvq_config;
+
+/* Byte offsets of the planes inside the caller's cache buffer (0 = absent).  Every
+   offset is a multiple of 256.  cap_alloc = capacity rounded up to 64 rows.
+     state              device counters and status (256 bytes)
+     split_sem          uint32 [B*Hkv] arrival counters of decode splits
+     {k,v}_codes        uint8  [B][Hkv][cap_alloc][row_bytes]: fp16 bytes, or the
+                        signed 8-bit level q = u - 128, or 4-bit codes with channel
+                        2j in the low nibble of byte j
+     {k,v}_tok_scale    fp16   [B][Hkv][cap_alloc][n_groups] (AFFINE_TOKEN, Q4_0)
+     {k,v}_tok_zero     fp16   [B][Hkv][cap_alloc][n_groups] (AFFINE_TOKEN)
+     k_ch_scale/zero    fp16   [B][Hkv][D]  stored per-channel metadata (KIVI_CHAN)
+     k_ch_scale32/zero32 fp32  [B][Hkv][D]  the values codes are computed from
+     k_bias             fp32   [Hkv][D]     copy of kvq_config.k_bias               */
+typedef struct kvq_cache_layout {
+  size_t total_bytes;
+  int32_t cap_alloc;
+  int32_t k_row_bytes, v_row_bytes;
+  int32_t k_n_groups, v_n_groups;
+  size_t state, split_sem;
+  size_t k_codes, k_tok_scale, k_tok_zero, k_ch_scale, k_ch_zero, k_ch_scale32, k_ch_zero32, k_bias;
+  size_t v_codes, v_tok_scale, v_tok_zero;
+} kvq_cache_layout;
+
+typedef struct kvq_stats {
+  int64_t pos;            /* absolute position of the next token (tokens ever appended;
+                             SnapKV's true offset, [SKV] "RoPE position semantics") */
+  int32_t stored;         /* rows currently held ([SLK] "Caveats": stored vs current length) */
+  int32_t capacity;
+  int32_t device_status;  /* KVQ_DEV_* */
+  int32_t k_calibrated;   /* KIVI_CHAN: per-channel scales frozen */
+  size_t cache_bytes;     /* size of the cache buffer */
+  size_t live_bytes;      /* bytes of codes + metadata of the stored rows */
+} kvq_stats;
+
+typedef struct kvq_cache_s* kvq_cache;
+
+/* Computes the plane layout for `cfg` (no device work).  Returns INVALID_ARG or
+   UNSUPPORTED for configurations the library rejects. */
+kvq_status kvq_cache_layout_query(const kvq_config* cfg, kvq_cache_layout* out);
+
+/* Creates a cache over the caller's device buffer `dev_mem` of `bytes` bytes
+   (>= layout.total_bytes, 256-byte aligned).  Zeroes the counters and copies the
+   K bias on `stream`.  `*out` receives a host handle; the buffer must outlive it. */
+kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cudaStream_t stream,
+                          kvq_cache* out);
+
+/* Frees the host handle (not the device buffer). */
+void kvq_cache_release(kvq_cache cache);
+
+/* Quantise-on-append ([SLK] "Implementation": after each per-layer append;
+   [KMC] "Why this is safe": one subtract at the point of cache write).
+   k, v: device [B, Hkv, n, D] of `in_dtype` (kvq_dtype).  Tokens take absolute
+   positions pos .. pos + n - 1.  LINEAR / COMPACT write rows stored .. stored + n - 1
+   (device overflow -> KVQ_DEV_OVERFLOW, nothing written); RING writes each
+   surviving token into its slot and leaves stored = min(pos + n, sink + window).
+   flags: KVQ_APPEND_CALIBRATE_K computes the KIVI per-channel K scales from these
+   n tokens and freezes them (required once before any other append to a
+   KIVI_CHAN cache; UNSUPPORTED otherwise).  Codes use fp32 scales
+   scale = max(1e-5, (max - min) / (qMax - qMin)), zero = min, and
+   u = clamp(rint((x - zero) / scale), 0, qMax - qMin) ([SLK] "Affine quantisation
+   formula"); Q4_0 uses d = max|x - kbar| / 7, u = clamp(rint((x - kbar) / d), -8, 7) + 8
+   (u = 8 when d == 0).  Stored scales and zeros are fp16. */
+kvq_status kvq_append(kvq_cache cache, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype,
+                      int32_t flags, cudaStream_t stream);
+
+/* KVQ_EVICT_MIDDLE ([SLK] "Implementation"): when stored > sink + window, drop
+   logical [sink, stored - window).  COMPACT moves the window rows (codes and
+   per-token metadata) down; RING needs no data movement and enqueues nothing;
+   LINEAR returns INVALID_ARG.  Per-channel K metadata is never touched.
+   KVQ_EVICT_KEEPSET ([SKV] "How it works", step 4): keep_idx device int32
+   [B, Hkv, n_keep], strictly ascending per (b, kv head), each < stored; row
+   keep_idx[b,h,j] moves to row j, stored becomes n_keep, pos is unchanged (the
+   true offset).  Done in place, in increasing row order. */
+kvq_status kvq_evict(kvq_cache cache, int32_t mode, const int32_t* keep_idx, int32_t n_keep,
+                     cudaStream_t stream);
+
+/* Workspace bytes kvq_decode_attn needs for this cache and n_q_heads (0 when
+   the call needs none).  Depends on the cache's capacity and the SM count. */
+size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
+
+/* Fused decode attention over the stored rows, reading the packed codes and
+   dequantising in registers ([MLX] section 5: decode reads the cache; [SLK]
+   "Affine quantisation formula": attention over the dequantised K, V).
+   q: device [B, Hq, D]; out: device [B, Hq, D]; both of io_dtype.
+   o[b,h] = softmax(q . k_hat^T * softmax_scale) v_hat, k_hat/v_hat from the stored
+   codes and fp16 metadata; softmax_scale <= 0 means 1/sqrt(D).  The rows are
+   split across CTAs and merged with the online-softmax rule.  workspace: device,
+   >= kvq_decode_workspace_bytes bytes (may be NULL when that is 0).  Calls on the
+   same cache must not overlap on the GPU.  Hq / Hkv in {1, 2, 3, 4}. */
+kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
+                           float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes snapkv_select needs. */
+size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int32_t head_dim,
+                              int32_t obs_window);
+
+/* SnapKV observation-window scoring and selection ([SKV] "How it works", steps 1-3;
+   "Evidence": window clamped to S, min(budget, S) indices, sorted, budget >= S
+   keeps all).  k: device fp16, row (b, h, s) at k + ((b*Hkv + h)*head_stride + s)*D
+   elements (head_stride >= S).  score[b,h,j] = mean over the last w = min(obs_window, S)
+   rows r of softmax_j(k_r . k_j / sqrt(D)), no mask.  Kept: positions [0, min(n_sink, S))
+   plus the top (budget - n_sink) of the rest by score (equal scores: lower position
+   first), ascending.  scores_out: device fp32 [B, Hkv, S] or NULL; idx_out: device
+   int32 [B, Hkv, min(budget, S)].  n_sink > budget -> INVALID_ARG.
+   obs_window in 1..64, head_dim in {32, 64, 128}, S >= 1. */
+kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int32_t n_kv_heads, int32_t S,
+                         int32_t head_dim, int32_t obs_window, int32_t budget, int32_t n_sink,
+                         float* scores_out, int32_t* idx_out, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* The selection step of snapkv_select alone, on caller-given fp32 scores
+   [B, Hkv, S] (device), with the same rule.  Needs no workspace. */
+kvq_status snapkv_topk(const float* scores, int32_t batch, int32_t n_kv_heads, int32_t S, int32_t budget,
+                       int32_t n_sink, int32_t* idx_out, cudaStream_t stream);
+
+/* Synchronises the device, copies `cache`'s counters to the host and fills `*out`. */
+kvq_status kvq_stats_read(kvq_cache cache, kvq_stats* out);
+
+/* Clears the device status word (stream-ordered). */
+kvq_status kvq_clear_status(kvq_cache cache, cudaStream_t stream);
+
+/* Number of kernels the last call on this thread enqueued (for launch accounting). */
+int32_t kvq_last_launch_count(void);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* kvq_last_error(void);
+
+int32_t kvq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */
