@@ -1,0 +1,6 @@
+// Decode attention instantiated for keys in AFF8 and values in AFF8.
+#include "decode_impl.cuh"
+
+namespace kvq {
+template cudaError_t launch_decode<F_AFF8, F_AFF8>(const CacheView&, int, const DecodeArgs&, cudaStream_t);
+}  // namespace kvq
