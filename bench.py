@@ -1,0 +1,549 @@
+"""Decode-step benchmark of the GB300 compressed KV cache.
+
+One step = the whole hot path of one decode step over every layer of the
+workload: quantise-on-append of the new token, StreamingLLM eviction (for
+streaming layouts) and fused decode attention.  Prints one JSON line.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload mlx8k|q4_0_32k|ring|tinygpt|snapkv]
+  python bench.py --impl reference ...    # the CPU oracle on a bounded sample of the same workload
+
+Inputs are seeded synthetic tensors (synth), resident in HBM before the timed
+region.  L2 is flushed (a 256 MiB write) between timed steps, outside the
+per-step events.  Timing: CUDA events on the launching stream, barrier +
+synchronize around the timed region, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# the CPU legs time the oracle single-threaded; say so by pinning BLAS threads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import synth  # noqa: E402
+
+METRIC = "decode-attn KV-cache GB/s (% of GB300 HBM peak) and decode steps/s per config"
+DEFAULT_WORKLOAD = "mlx8k"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    a = p.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ byte model --
+
+def side_token_bytes(fmt, bits, group, D):
+    if fmt == "fp16":
+        return 2 * D
+    codes = D * bits // 8
+    if fmt == "affine_token":
+        return codes + 4 * (D // group)
+    if fmt == "q4_0":
+        return codes + 2 * (D // 32)
+    return codes
+
+
+def decode_bytes(w, T):
+    """Algorithmic bytes of one decode-attention launch (one layer): codes + metadata + Q + O."""
+    io = torch.empty((), dtype=synth.torch_dtype(w.io_dtype)).element_size()
+    per_head = T * (side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
+                    + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
+    if w.k_format == "kivi_chan":
+        per_head += 4 * w.head_dim
+    return w.batch * w.n_kv_heads * per_head + 2 * w.batch * w.n_q_heads * w.head_dim * io
+
+
+def append_bytes(w, n):
+    """Bytes of one append of n tokens (one layer): inputs read, codes + metadata written."""
+    io = torch.empty((), dtype=synth.torch_dtype(w.io_dtype)).element_size()
+    rows = w.batch * w.n_kv_heads * n
+    wr = (side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
+          + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
+    return rows * (2 * w.head_dim * io + wr)
+
+
+def stored_after(w, t_seen):
+    if w.layout == "linear":
+        return t_seen
+    return min(t_seen, w.sink + w.window)
+
+
+# ------------------------------------------------------ decode workloads --
+
+class DecodeStep:
+    """All layers of one workload: caches filled to the context, per-layer step
+    inputs and outputs resident in HBM, and two captured CUDA graphs (every
+    layer's append + eviction, then every layer's decode attention)."""
+
+    def __init__(self, kvq, w, extra_rows, device):
+        self.kvq, self.w, self.device = kvq, w, device
+        dt = synth.torch_dtype(w.io_dtype)
+        if w.layout == "linear":
+            cap = w.context + extra_rows
+        else:
+            cap = w.sink + w.window + (1 if w.layout == "compact" else 0)
+        self.caches = []
+        for layer in range(w.layers):
+            bias = synth.k_bias(w, layer, device=device) if w.use_k_bias else None
+            c = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, cap, w.k_format, w.k_bits, w.k_group,
+                            w.v_format, w.v_bits, w.v_group, layout=w.layout, sink=w.sink, window=w.window,
+                            k_bias=bias, device=device)
+            k, v = synth.layer_inputs(w, layer, 0, w.context, device=device)
+            c.append(k, v, calibrate_k=(w.k_format == "kivi_chan"))
+            del k, v
+            self.caches.append(c)
+        torch.cuda.synchronize()
+        self.t_seen = w.context
+        # step inputs (Q, new K, new V per layer) packed in one buffer so that an
+        # end-to-end step is one host-to-device copy; outputs likewise
+        L, B, Hq, Hkv, D = w.layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+        per = B * Hq * D + 2 * B * Hkv * D
+        self.stage = torch.empty(L * per, dtype=dt, device=device)
+        self.outbuf = torch.empty(L * B * Hq * D, dtype=dt, device=device)
+        self.q, self.k1, self.v1, self.out = [], [], [], []
+        for layer in range(L):
+            q, k1, v1 = synth.decode_token_inputs(w, layer, 0, w.context, device=device)
+            base = layer * per
+            qv = self.stage[base: base + q.numel()].view(q.shape)
+            kv_ = self.stage[base + q.numel(): base + q.numel() + k1.numel()].view(k1.shape)
+            vv = self.stage[base + q.numel() + k1.numel(): base + per].view(v1.shape)
+            qv.copy_(q), kv_.copy_(k1), vv.copy_(v1)
+            self.q.append(qv), self.k1.append(kv_), self.v1.append(vv)
+            self.out.append(self.outbuf[layer * B * Hq * D: (layer + 1) * B * Hq * D].view(B, Hq, D))
+        for c in self.caches:                      # workspaces allocated before capture
+            c.workspace(Hq)
+        self.launches_append = 0
+        self.launches_decode = 0
+
+    def eager_append(self):
+        n = 0
+        for layer, c in enumerate(self.caches):
+            c.launches = 0
+            c.append(self.k1[layer], self.v1[layer])
+            if self.w.layout != "linear":
+                c.evict_middle()
+            n += c.launches
+        self.t_seen += 1
+        return n
+
+    def eager_decode(self):
+        n = 0
+        for layer, c in enumerate(self.caches):
+            c.launches = 0
+            c.decode_attn(self.q[layer], out=self.out[layer])
+            n += c.launches
+        return n
+
+    def capture(self):
+        # one eager pass first: every kernel is loaded before capture
+        self.eager_append()
+        self.eager_decode()
+        torch.cuda.synchronize()
+        self.g_append = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_append):
+            self.launches_append = self.eager_append()
+        self.t_seen -= 1      # capture records the launches without running them
+        self.g_decode = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_decode):
+            self.launches_decode = self.eager_decode()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.g_append.replay()
+        self.g_decode.replay()
+        self.t_seen += 1
+
+    def stored(self):
+        return stored_after(self.w, self.t_seen)
+
+    def step_bytes(self):
+        """(append + eviction + attention bytes of the next step, attention bytes per layer)."""
+        w = self.w
+        T = stored_after(w, self.t_seen + 1)
+        dec = decode_bytes(w, T)
+        app = append_bytes(w, 1)
+        ev = 0
+        if w.layout == "compact" and self.t_seen + 1 > w.sink + w.window:
+            ev = 2 * w.batch * w.n_kv_heads * w.window * (
+                side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
+                + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
+        return w.layers * (dec + app + ev), dec
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while the GPU works."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        ident = []
+        try:
+            ident = [f"--id=GPU-{torch.cuda.get_device_properties(torch.cuda.current_device()).uuid}"]
+        except Exception:
+            ident = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *ident, f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.0)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[0]) for r in rows]
+        mx = max(num(r[1]) for r in rows)
+        busy = [s for s, r in zip(sm, rows) if num(r[2]) > 0.3 * max(num(q[2]) for q in rows)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ timed runs --
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_decode(ds, steps, warmup, world):
+    """K timed steps (graph replays), L2 flushed between them outside the events."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=ds.device)
+    for _ in range(warmup):
+        flush.zero_()
+        ds.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    total_bytes = 0
+    dec_bytes = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        b, d = ds.step_bytes()
+        total_bytes += b
+        dec_bytes.append(d)
+        flush.zero_()
+        ev[i][0].record()
+        ds.g_append.replay()
+        ev[i][1].record()
+        ds.g_decode.replay()
+        ev[i][2].record()
+        ds.t_seen += 1
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    return total_bytes, step_ms, dec_ms, dec_bytes
+
+
+def e2e_decode(ds, steps, world):
+    """Through the public Python API, eager calls, inputs from pinned host memory, result read back."""
+    host_in = torch.empty(ds.stage.shape, dtype=ds.stage.dtype, pin_memory=True)
+    host_in.copy_(ds.stage)
+    host_out = torch.empty(ds.outbuf.shape, dtype=ds.outbuf.dtype, pin_memory=True)
+    for _ in range(2):
+        ds.stage.copy_(host_in, non_blocking=True)
+        ds.eager_append()
+        ds.eager_decode()
+        host_out.copy_(ds.outbuf, non_blocking=True)
+        torch.cuda.synchronize()
+    total = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        total += ds.step_bytes()[0]
+        ds.stage.copy_(host_in, non_blocking=True)
+        ds.eager_append()
+        ds.eager_decode()
+        host_out.copy_(ds.outbuf, non_blocking=True)
+        torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    dt = max_over_ranks(t1 - t0, world)
+    return total, dt, host_in.numel() * host_in.element_size(), host_out.numel() * host_out.element_size()
+
+
+# ---------------------------------------------------- the oracle on the CPU --
+
+class OracleSample:
+    """The oracle's decode step on one (batch 0, kv head 0) slice of layer 0 of the
+    workload: quantise-on-append of one token, eviction, float64 attention over
+    the dequantised cache for the kv head's query heads."""
+
+    def __init__(self, w):
+        from oracle import attention as oatt
+        from oracle.cache import CacheSpec, OracleCache
+
+        self.oatt = oatt
+        self.w = w
+        G = w.group
+        k, v = synth.layer_inputs(w, 0, 0, w.context, batch=1)
+        k, v = k[:, :1].float().numpy(), v[:, :1].float().numpy()
+        bias = synth.k_bias(w, 0)[:1].numpy() if w.use_k_bias else None
+        if w.layout == "linear":
+            cap = w.context + 8192
+        else:
+            cap = w.sink + w.window + (1 if w.layout == "compact" else 0)
+        self.oc = OracleCache(CacheSpec(batch=1, n_kv_heads=1, head_dim=w.head_dim, capacity=cap, layout=w.layout,
+                                        sink=w.sink, window=w.window, k_format=w.k_format, k_bits=w.k_bits,
+                                        k_group=w.k_group, v_format=w.v_format, v_bits=w.v_bits, v_group=w.v_group,
+                                        k_bias=bias))
+        if w.k_format == "kivi_chan":
+            self.oc.calibrate_k(k)
+        self.oc.append(k, v)
+        q, k1, v1 = synth.decode_token_inputs(w, 0, 0, w.context, batch=1)
+        self.q = q[:, :G].float().numpy()
+        self.k1 = k1[:, :1].float().numpy()
+        self.v1 = v1[:, :1].float().numpy()
+        self.slice_w = w.with_(batch=1, n_kv_heads=1, n_q_heads=G, layers=1)
+        self.cap = cap
+
+    def step(self):
+        """Runs one step; returns its algorithmic bytes."""
+        if self.w.layout == "linear" and self.oc.stored + 1 > self.cap:
+            raise RuntimeError("oracle sample cache full")
+        self.oc.append(self.k1, self.v1)
+        if self.w.layout != "linear":
+            self.oc.evict_middle()
+        kh, vh = self.oc.dequant()
+        self.oatt.decode_attention(self.q, kh, vh)
+        return decode_bytes(self.slice_w, self.oc.stored) + append_bytes(self.slice_w, 1)
+
+    def describe(self):
+        w = self.w
+        return (f"layer 0, batch row 0, kv head 0 of {w.name} ({w.group} query heads, "
+                f"{self.oc.stored} stored tokens): append + evict + float64 attention per step")
+
+
+def cpu_baseline(w, seconds):
+    s = OracleSample(w)
+    s.step()
+    nbytes, n, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        nbytes += s.step()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} steps of {s.describe()}; {dt:.1f} s single-threaded numpy"}
+
+
+def run_reference(a, rank, world):
+    if world > 1 and rank != 0:
+        return
+    w = synth.get_workload(a.workload)
+    if w.prompt_len:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times decode workloads only"}))
+        return
+    s = OracleSample(w)
+    for _ in range(a.warmup):
+        s.step()
+    nbytes, t0 = 0, time.perf_counter()
+    for _ in range(a.steps):
+        nbytes += s.step()
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3 / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": "one (batch, kv head) slice of one layer per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{a.steps} steps of {s.describe()}"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def decode_traffic(w, kvq_dir):
+    """DRAM bytes per decode launch from the committed ncu summary, if it matches this kernel source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    src = os.path.join(kvq_dir, "csrc", "decode_impl.cuh")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    entry = d.get(w.name)
+    if not entry or entry.get("kernel_source_sha256") != sha:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# -------------------------------------------------------------------- main --
+
+def bench_decode(a, kvq, w, rank, world):
+    device = torch.device("cuda", torch.cuda.current_device())
+    extra = 2 * (a.steps + a.warmup) + 64
+    ds = DecodeStep(kvq, w, extra, device)
+    ds.capture()
+    clocks = ClockSampler()
+    clocks.start()
+    total_bytes, step_ms, dec_ms, dec_bytes = timed_decode(ds, a.steps, a.warmup, world)
+    clk = clocks.stop()
+    t_step = sum(step_ms) / 1e3
+    t_max = max_over_ranks(t_step, world)
+    value = world * total_bytes / t_max / 1e9
+    avg_dec_launch_s = sum(dec_ms) / 1e3 / (a.steps * w.layers)
+    dec_bytes_launch = sum(dec_bytes) / len(dec_bytes)
+    peak, peak_kind = read_peaks()
+    achieved = dec_bytes_launch / avg_dec_launch_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": t_max * 1e3 / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u4/u8 codes, f32 math" if w.k_format != "fp16" else "f16 codes, f32 math",
+        "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
+                   "k_format": f"{w.k_format}{w.k_bits}" + (f"g{w.k_group}" if w.k_group else ""),
+                   "v_format": f"{w.v_format}{w.v_bits}" + (f"g{w.v_group}" if w.v_group else ""),
+                   "layout": w.layout, "step": "per layer: append 1 token, evict, decode attention",
+                   "l2": "flushed (256 MiB write) between timed steps, outside the events",
+                   "parallelism": f"replicas x{world}"},
+        "decode_steps_per_s": world * a.steps / t_max,
+        "tokens_appended_per_s": world * a.steps * w.batch / t_max,
+        "decode_attn_gbs": world * sum(dec_bytes) * w.layers / max_over_ranks(sum(dec_ms) / 1e3, world) / 1e9,
+        "gpu_launches": (ds.launches_append + ds.launches_decode) * a.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": decode_traffic(w, os.path.dirname(kvq.__file__)),
+                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes_launch,
+                     "avg_launch_us": avg_dec_launch_s * 1e6, "peak_kind": f"{peak_kind} copy bandwidth"},
+        "clocks": clk,
+    }
+    if not a.no_e2e:
+        e_bytes, e_dt, h2d, d2h = e2e_decode(ds, max(3, min(a.steps, 200)), world)
+        line["e2e"] = {"value": world * e_bytes / e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h,
+                       "how": "public Python API, eager calls per layer, pinned host inputs copied in and "
+                              "outputs read back every step (wall clock)"}
+    return line
+
+
+def bench_snapkv(a, kvq, w, rank, world):
+    device = torch.device("cuda", torch.cuda.current_device())
+    k, _ = synth.snapkv_prefill(w, device=device)
+    B, H, S, D = k.shape
+    ws = torch.empty(kvq.snapkv_workspace_bytes(B, H, S, D, w.obs_window), dtype=torch.uint8, device=device)
+    scores = torch.empty((B, H, S), dtype=torch.float32, device=device)
+    idx = torch.empty((B, H, w.budget), dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(a.warmup):
+        kvq.snapkv_select(k, S, B, H, S, D, w.obs_window, w.budget, w.n_sink, scores, idx, ws)
+    nbytes = k.numel() * 2 + scores.numel() * 4 + idx.numel() * 4
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        flush.zero_()
+        ev[i][0].record()
+        kvq.snapkv_select(k, S, B, H, S, D, w.obs_window, w.budget, w.n_sink, scores, idx, ws)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t = max_over_ranks(sum(s.elapsed_time(e) for s, e in ev) / 1e3, world)
+    peak, peak_kind = read_peaks()
+    achieved = nbytes * a.steps / t / 1e9
+    return {"metric": METRIC, "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": t * 1e3 / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
+            "config": {"workload": w.name, "prompt": S, "n_kv_heads": H, "head_dim": D, "obs_window": w.obs_window,
+                       "budget": w.budget, "n_sink": w.n_sink, "step": "snapkv_select (scores + top-k)",
+                       "l2": "flushed between timed steps"},
+            "gpu_launches": 3 * a.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": f"{peak_kind} copy bandwidth"}}
+
+
+def main(argv=None):
+    a = parse_args(argv)
+    rank, world, local = dist_env()
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import bit_kv_cache_quant_gb300 as kvq
+
+    w = synth.get_workload(a.workload)
+    line = bench_snapkv(a, kvq, w, rank, world) if w.prompt_len else bench_decode(a, kvq, w, rank, world)
+    if rank == 0 and not a.no_cpu_baseline and not w.prompt_len:
+        line["cpu_baseline"] = cpu_baseline(w, a.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+"""Host-side checks of the C-ABI library: it loads, exports every function the
+header declares, and its argument validation and plane layout behave as the
+header states.  No call here touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "bit_kv_cache_quant_gb300", "libkvq.so")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not os.path.exists(LIB):
+        from bit_kv_cache_quant_gb300 import build as b   # noqa: the package import needs the .so
+
+        b.build()
+    import bit_kv_cache_quant_gb300 as m
+
+    return m
+
+
+def test_exports_every_declared_function(kvq):
+    names = kvq.declared_functions()
+    assert len(names) >= 15
+    raw = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in kvq.h but not exported"
+    assert kvq.lib.kvq_abi_version() == 1
+
+
+def test_header_functions_are_extern_c():
+    with open(os.path.join(ROOT, "include", "kvq.h")) as f:
+        text = f.read()
+    assert 'extern "C"' in text
+    # every declaration is a plain C signature: no torch, no C++ references
+    assert "torch" not in text.replace("torch types", "") and "&" not in re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+
+def _cfg(kvq, **kw):
+    base = dict(batch=2, n_kv_heads=4, head_dim=128, capacity=100, k_format="affine_token", k_bits=4, k_group=64,
+                v_format="affine_token", v_bits=4, v_group=64)
+    base.update(kw)
+    bias = base.pop("k_bias", None)
+    cfg = kvq.make_config(**base)
+    if bias is not None:
+        cfg.k_bias = bias
+    return cfg
+
+
+def _status(kvq, cfg):
+    lay = kvq.kvq_cache_layout()
+    return kvq.lib.kvq_cache_layout_query(ctypes.byref(cfg), ctypes.byref(lay)), lay
+
+
+def test_layout_planes_are_aligned_and_sized(kvq):
+    st, lay = _status(kvq, _cfg(kvq))
+    assert st == 0
+    assert lay.cap_alloc == 128 and lay.k_row_bytes == 64 and lay.k_n_groups == 2
+    offs = [lay.state, lay.split_sem, lay.k_codes, lay.k_tok_scale, lay.k_tok_zero, lay.v_codes, lay.v_tok_scale,
+            lay.v_tok_zero]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.k_tok_scale - lay.k_codes >= 2 * 4 * 128 * 64
+    assert lay.total_bytes >= lay.v_tok_zero + 2 * 4 * 128 * 2 * 2
+    assert lay.k_ch_scale == 0 and lay.k_bias == 0
+
+
+def test_layout_matches_byte_accounting(kvq):
+    # codes + metadata per stored row agree with the oracle's bytes-per-token rule
+    from oracle import accounting as acc
+
+    for fmt, bits, group in (("affine_token", 4, 64), ("affine_token", 8, 128), ("q4_0", 4, 32), ("fp16", 16, 0)):
+        vfmt = "fp16" if fmt in ("fp16", "q4_0") else fmt
+        cfg = _cfg(kvq, k_format=fmt, k_bits=bits, k_group=group, v_format=vfmt, v_bits=bits if vfmt != "fp16" else 16,
+                   v_group=group if vfmt != "fp16" else 0)
+        st, lay = _status(kvq, cfg)
+        assert st == 0, kvq.lib.kvq_last_error()
+        meta = lay.k_n_groups * 2 * (2 if fmt == "affine_token" else 1)
+        assert lay.k_row_bytes + meta == acc.side_bytes_per_token(fmt, bits, group, 128)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(head_dim=96), 2),
+    (dict(batch=0), 1),
+    (dict(k_format="kivi_chan", k_bits=3), 1),
+    (dict(k_group=48), 1),
+    (dict(v_format="q4_0", v_bits=4, v_group=32), 2),
+    (dict(v_format="kivi_chan", v_bits=8, v_group=0), 2),
+    (dict(layout="compact", sink=4, window=96), 1),       # capacity < sink + window + 1
+    (dict(layout="ring", sink=4, window=200), 1),
+    (dict(layout="ring", sink=4, window=0), 1),
+])
+def test_invalid_configs_rejected(kvq, bad, code):
+    st, _ = _status(kvq, _cfg(kvq, **bad))
+    assert st == code, kvq.lib.kvq_last_error()
+    assert kvq.lib.kvq_last_error()
+
+
+def test_bias_gate(kvq):
+    # a mean-centering bias with non-Q4_0 keys is rejected before any device work
+    st, _ = _status(kvq, _cfg(kvq, k_bias=0x1000))
+    assert st == 2 and b"Q4_0" in kvq.lib.kvq_last_error()
+    st, lay = _status(kvq, _cfg(kvq, k_format="q4_0", k_bits=4, k_group=32, k_bias=0x1000))
+    assert st == 0 and lay.k_bias != 0
+
+
+def test_snapkv_argument_checks(kvq):
+    f = kvq.lib.snapkv_select
+    ws = kvq.snapkv_workspace_bytes(1, 8, 16384, 128, 32)
+    assert ws >= 8 * 16384 * 4
+    # n_sink > budget, bad head_dim, window out of range: all rejected on the host
+    assert f(0x1000, 100, 1, 1, 100, 128, 32, 4, 5, None, 0x2000, 0x3000, ws, None) == 1
+    assert f(0x1000, 100, 1, 1, 100, 96, 32, 8, 4, None, 0x2000, 0x3000, ws, None) == 2
+    assert f(0x1000, 100, 1, 1, 100, 128, 65, 8, 4, None, 0x2000, 0x3000, ws, None) == 2
+    assert kvq.lib.snapkv_topk(0x1000, 1, 1, 10, 3, 4, 0x2000, None) == 1
+
+
+def test_null_handles(kvq):
+    assert kvq.lib.kvq_append(None, None, None, 1, 1, 0, None) == 1
+    assert kvq.lib.kvq_decode_attn(None, None, None, 1, 1, 0.0, None, 0, None) == 1
+    assert kvq.lib.kvq_decode_workspace_bytes(None, 8) == 0

@@ -1,0 +1,192 @@
+"""GPU parity: quantise-on-append and eviction, bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from kvq_helpers import assert_cache_equal, gpu_planes, host, oracle_spec
+from oracle.cache import OracleCache
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [
+    # (k_format, k_bits, k_group, v_format, v_bits, v_group)
+    ("fp16", 16, 0, "fp16", 16, 0),
+    ("kivi_chan", 8, 0, "affine_token", 8, 128),
+    ("kivi_chan", 4, 0, "affine_token", 4, 32),
+    ("affine_token", 8, 64, "affine_token", 8, 64),
+    ("affine_token", 4, 64, "affine_token", 4, 64),
+    ("affine_token", 4, 16, "affine_token", 8, 32),
+    ("q4_0", 4, 32, "affine_token", 8, 128),
+    ("q4_0", 4, 32, "affine_token", 4, 32),
+]
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import bit_kv_cache_quant_gb300 as m
+
+    assert torch.cuda.is_available()
+    return m
+
+
+def _inputs(shape, seed, dtype, offset_sigma=2.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(shape, generator=g)
+    x = x + torch.randn(shape[1], shape[3], generator=g)[None, :, None, :] * offset_sigma
+    return x.to(dtype)
+
+
+def _clip(D, group):
+    return min(group, D) if group else group
+
+
+@pytest.mark.parametrize("fmt", FORMATS, ids=lambda f: f"{f[0]}{f[1]}-{f[3]}{f[4]}g{f[5]}")
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16])
+def test_append_bit_exact(kvq, fmt, D, dtype):
+    kf, kb, kg, vf, vb, vg = fmt
+    kg, vg = _clip(D, kg), _clip(D, vg)
+    B, H, cap = 2, 3, 90
+    bias = None
+    if kf == "q4_0":
+        bias = (torch.randn(H, D, generator=torch.Generator().manual_seed(D)) * 1.5).float()
+    cache = kvq.KVCache(B, H, D, cap, kf, kb, kg, vf, vb, vg, k_bias=None if bias is None else bias.cuda())
+    oc = OracleCache(oracle_spec(cache, None if bias is None else bias.numpy()))
+    k = _inputs((B, H, 67, D), 1, dtype)
+    v = _inputs((B, H, 67, D), 2, dtype, 0.0)
+    calibrate = kf == "kivi_chan"
+    cache.append(k.cuda(), v.cuda(), calibrate_k=calibrate)
+    if calibrate:
+        oc.calibrate_k(host(k))
+    oc.append(host(k), host(v))
+    assert_cache_equal(cache, oc, "bulk append")
+    for step, n in enumerate((1, 1, 5, 16)):
+        k2 = _inputs((B, H, n, D), 10 + step, dtype) * 1.5     # frozen K scales clamp some of these
+        v2 = _inputs((B, H, n, D), 20 + step, dtype, 0.0)
+        cache.append(k2.cuda(), v2.cuda())
+        oc.append(host(k2), host(v2))
+    assert_cache_equal(cache, oc, "decode appends")
+
+
+def test_zero_bias_is_byte_identical_to_no_bias(kvq):
+    # disabled centering is a no-op: no bias and an all-zero bias give the same bytes
+    B, H, D = 1, 2, 128
+    k = _inputs((B, H, 40, D), 3, torch.bfloat16)
+    a = kvq.KVCache(B, H, D, 64, "q4_0", 4, 32, "affine_token", 8, 128)
+    b = kvq.KVCache(B, H, D, 64, "q4_0", 4, 32, "affine_token", 8, 128, k_bias=torch.zeros(H, D, device="cuda"))
+    a.append(k.cuda(), k.cuda())
+    b.append(k.cuda(), k.cuda())
+    pa, pb = gpu_planes(a), gpu_planes(b)
+    np.testing.assert_array_equal(pa["k_rows"], pb["k_rows"])
+    np.testing.assert_array_equal(pa["k_tok_scale"].view(np.uint16), pb["k_tok_scale"].view(np.uint16))
+
+
+def test_constant_and_zero_rows(kvq):
+    B, H, D = 1, 1, 64
+    k = torch.zeros(B, H, 8, D)
+    k[0, 0, 3] = 0.25
+    k[0, 0, 5, :32] = 1.0
+    for kf, kb, kg in (("affine_token", 4, 64), ("q4_0", 4, 32)):
+        cache = kvq.KVCache(B, H, D, 16, kf, kb, kg, "affine_token", 8, 64)
+        oc = OracleCache(oracle_spec(cache))
+        cache.append(k.cuda(), k.cuda())
+        oc.append(k.numpy(), k.numpy())
+        assert_cache_equal(cache, oc, kf)
+
+
+def test_overflow_sets_status_and_writes_nothing(kvq):
+    cache = kvq.KVCache(1, 2, 64, 10, "affine_token", 8, 64, "affine_token", 8, 64)
+    k = _inputs((1, 2, 8, 64), 4, torch.bfloat16)
+    cache.append(k.cuda(), k.cuda())
+    before = gpu_planes(cache)
+    k2 = _inputs((1, 2, 3, 64), 5, torch.bfloat16)
+    cache.append(k2.cuda(), k2.cuda())
+    after = gpu_planes(cache)
+    assert after["status"] == kvq.DEV_OVERFLOW
+    assert after["stored"] == 8 and after["pos"] == 8
+    np.testing.assert_array_equal(before["k_rows"], after["k_rows"])
+    st = cache.stats()
+    assert st.device_status == kvq.DEV_OVERFLOW
+    kvq.kvq_clear_status(cache.handle)
+    assert cache.stats().device_status == 0
+
+
+def test_uncalibrated_kivi_append_rejected(kvq):
+    cache = kvq.KVCache(1, 1, 32, 16, "kivi_chan", 8, 0, "affine_token", 8, 32)
+    k = torch.randn(1, 1, 2, 32, device="cuda")
+    with pytest.raises(kvq.KvqError):
+        cache.append(k, k)
+
+
+@pytest.mark.parametrize("layout,n_steps", [("compact", 1), ("compact", 259), ("compact", 261), ("compact", 300),
+                                            ("ring", 261), ("ring", 700)])
+def test_streaming_decode_matches_oracle(kvq, layout, n_steps):
+    # KIVI int8, sink 4 + window 256, one append + one evict per step
+    sink, window, D, B, H = 4, 256, 32, 1, 2
+    cap = sink + window + (1 if layout == "compact" else 0)
+    cache = kvq.KVCache(B, H, D, cap, "kivi_chan", 8, 0, "affine_token", 8, 32, layout=layout, sink=sink,
+                        window=window)
+    oc = OracleCache(oracle_spec(cache))
+    fill = _inputs((B, H, 1, D), 7, torch.float32)
+    cache.append(fill.cuda(), fill.cuda(), calibrate_k=True)
+    cache.evict_middle()
+    oc.calibrate_k(host(fill))
+    oc.append(host(fill), host(fill))
+    oc.evict_middle()
+    g = torch.Generator().manual_seed(8)
+    ks = torch.randn(n_steps, B, H, 1, D, generator=g)
+    vs = torch.randn(n_steps, B, H, 1, D, generator=g)
+    ksd, vsd = ks.cuda(), vs.cuda()
+    for t in range(n_steps):
+        cache.append(ksd[t], vsd[t])
+        cache.evict_middle()
+        oc.append(ks[t].numpy(), vs[t].numpy())
+        oc.evict_middle()
+    assert_cache_equal(cache, oc, f"{layout} after {n_steps + 1} tokens")
+    assert oc.stored == min(n_steps + 1, sink + window)
+
+
+def test_ring_bulk_append_longer_than_window(kvq):
+    sink, window, D = 4, 64, 128
+    cache = kvq.KVCache(2, 2, D, sink + window, "kivi_chan", 4, 0, "affine_token", 4, 32, layout="ring", sink=sink,
+                        window=window)
+    oc = OracleCache(oracle_spec(cache))
+    k = _inputs((2, 2, 200, D), 9, torch.bfloat16)
+    v = _inputs((2, 2, 200, D), 10, torch.bfloat16, 0.0)
+    cache.append(k.cuda(), v.cuda(), calibrate_k=True)
+    oc.calibrate_k(host(k))
+    oc.append(host(k), host(v))
+    assert_cache_equal(cache, oc, "ring bulk")
+
+
+@pytest.mark.parametrize("fmt", [FORMATS[0], FORMATS[4], FORMATS[6]], ids=["fp16", "aff4", "q40"])
+def test_keepset_gather(kvq, fmt):
+    kf, kb, kg, vf, vb, vg = fmt
+    B, H, D, S, n_keep = 2, 3, 128, 700, 130
+    cache = kvq.KVCache(B, H, D, S + 8, kf, kb, kg, vf, vb, vg)
+    oc = OracleCache(oracle_spec(cache))
+    k = _inputs((B, H, S, D), 11, torch.float16)
+    v = _inputs((B, H, S, D), 12, torch.float16, 0.0)
+    cache.append(k.cuda(), v.cuda())
+    oc.append(host(k), host(v))
+    rng = np.random.default_rng(3)
+    idx = np.stack([np.stack([np.sort(rng.choice(S, n_keep, replace=False)) for _ in range(H)]) for _ in range(B)])
+    idx[0, 0, :4] = np.arange(4)
+    idx = idx.astype(np.int32)
+    cache.evict_keepset(torch.from_numpy(idx).cuda())
+    oc.evict_keepset(idx)
+    assert_cache_equal(cache, oc, "keep-set")
+    t = _inputs((B, H, 1, D), 13, torch.float16)
+    cache.append(t.cuda(), t.cuda())
+    oc.append(host(t), host(t))
+    assert_cache_equal(cache, oc, "append after keep-set")
+    assert cache.stats().pos == S + 1
+
+
+def test_bad_keepset_sets_status(kvq):
+    cache = kvq.KVCache(1, 1, 64, 40, "fp16", 16, 0, "fp16", 16, 0)
+    k = torch.randn(1, 1, 20, 64, dtype=torch.float16, device="cuda")
+    cache.append(k, k)
+    idx = torch.tensor([[[0, 5, 5, 9]]], dtype=torch.int32, device="cuda")     # not strictly ascending
+    cache.evict_keepset(idx)
+    assert gpu_planes(cache)["status"] == kvq.DEV_BAD_KEEPSET

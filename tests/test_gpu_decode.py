@@ -1,0 +1,120 @@
+"""GPU parity: fused decode attention against float64 attention on the oracle's
+dequantised cache (same stored bytes)."""
+import numpy as np
+import pytest
+import torch
+
+from kvq_helpers import assert_attention_close, host, oracle_spec
+from oracle import attention as oatt
+from oracle.cache import OracleCache
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [
+    ("fp16", 16, 0, "fp16", 16, 0),
+    ("kivi_chan", 8, 0, "affine_token", 8, 128),
+    ("kivi_chan", 4, 0, "affine_token", 4, 32),
+    ("affine_token", 8, 64, "affine_token", 8, 64),
+    ("affine_token", 4, 64, "affine_token", 4, 64),
+    ("q4_0", 4, 32, "affine_token", 8, 128),
+    ("q4_0", 4, 32, "affine_token", 4, 32),
+]
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import bit_kv_cache_quant_gb300 as m
+
+    return m
+
+
+def _rand(shape, seed, dtype, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(dtype)
+
+
+def _build(kvq, pair, B, H, D, T, dtype, seed, cap=None, bias=False):
+    kf, kb, kg, vf, vb, vg = pair
+    kg, vg = (min(kg, D) if kg else 0), (min(vg, D) if vg else 0)
+    kbias = _rand((H, D), seed + 7, torch.float32, 1.5) if bias else None
+    cache = kvq.KVCache(B, H, D, cap or T, kf, kb, kg, vf, vb, vg,
+                        k_bias=None if kbias is None else kbias.cuda())
+    oc = OracleCache(oracle_spec(cache, None if kbias is None else kbias.numpy()))
+    k = _rand((B, H, T, D), seed, dtype, 1.0)
+    if kbias is not None:
+        k = (k.float() + kbias[None, :, None, :]).to(dtype)
+    v = _rand((B, H, T, D), seed + 1, dtype)
+    cache.append(k.cuda(), v.cuda(), calibrate_k=(kf == "kivi_chan"))
+    if kf == "kivi_chan":
+        oc.calibrate_k(host(k))
+    oc.append(host(k), host(v))
+    return cache, oc
+
+
+def _check(kvq, cache, oc, G, dtype, seed, what):
+    B, H, D = cache.batch, cache.n_kv_heads, cache.head_dim
+    q = _rand((B, H * G, D), seed + 2, dtype, 1.0)
+    out = cache.decode_attn(q.cuda())
+    kh, vh = oc.dequant()
+    ref = oatt.decode_attention(host(q), kh, vh)
+    return assert_attention_close(out, ref, what)
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}{p[1]}-{p[3]}{p[4]}")
+@pytest.mark.parametrize("G", [1, 2, 3, 4])
+@pytest.mark.parametrize("D,T", [(128, 1000), (64, 333), (32, 65)])
+def test_decode_matches_oracle(kvq, pair, G, D, T):
+    cache, oc = _build(kvq, pair, 2, 2, D, T, torch.bfloat16, seed=D + T, bias=pair[0] == "q4_0")
+    _check(kvq, cache, oc, G, torch.bfloat16, seed=G, what=f"G={G} D={D} T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 31, 33, 64, 255, 257, 1023, 4099])
+def test_decode_ragged_lengths(kvq, T):
+    pair = ("affine_token", 4, 64, "affine_token", 4, 64)
+    cache, oc = _build(kvq, pair, 1, 2, 128, T, torch.bfloat16, seed=T)
+    _check(kvq, cache, oc, 3, torch.bfloat16, seed=T, what=f"T={T}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_decode_io_dtypes(kvq, dtype):
+    pair = ("kivi_chan", 8, 0, "affine_token", 8, 32)
+    cache, oc = _build(kvq, pair, 1, 8, 32, 260, dtype, seed=5)
+    _check(kvq, cache, oc, 1, dtype, seed=6, what=str(dtype))
+
+
+def test_single_token_returns_value(kvq):
+    pair = ("affine_token", 8, 64, "affine_token", 8, 64)
+    cache, oc = _build(kvq, pair, 1, 2, 64, 1, torch.float32, seed=9)
+    q = _rand((1, 4, 64), 3, torch.float32, 5.0)
+    out = cache.decode_attn(q.cuda()).cpu().numpy()
+    _, vh = oc.dequant()
+    for h in range(4):
+        np.testing.assert_allclose(out[0, h], vh[0, h // 2, 0], rtol=0, atol=1e-6)
+
+
+def test_empty_cache_gives_zeros(kvq):
+    cache = kvq.KVCache(1, 2, 128, 64, "affine_token", 4, 64, "affine_token", 4, 64)
+    out = cache.decode_attn(torch.randn(1, 6, 128, device="cuda", dtype=torch.bfloat16))
+    assert torch.all(out == 0)
+
+
+def test_peaked_attention_and_custom_scale(kvq):
+    # large logits (scale 1.0, keys with offsets) exercise the online-softmax rescaling
+    pair = ("q4_0", 4, 32, "affine_token", 8, 128)
+    cache, oc = _build(kvq, pair, 1, 2, 128, 3000, torch.bfloat16, seed=11, bias=True)
+    q = _rand((1, 8, 128), 12, torch.bfloat16, 2.0)
+    out = cache.decode_attn(q.cuda(), softmax_scale=0.5)
+    kh, vh = oc.dequant()
+    ref = oatt.decode_attention(host(q), kh, vh, scale=0.5)
+    assert_attention_close(out, ref, "scale 0.5")
+
+
+def test_repeated_calls_are_identical(kvq):
+    # split merge counters reset themselves: the same call twice gives the same bytes
+    pair = ("affine_token", 4, 64, "affine_token", 4, 64)
+    cache, _ = _build(kvq, pair, 1, 8, 128, 8192, torch.bfloat16, seed=13)
+    q = _rand((1, 24, 128), 14, torch.bfloat16).cuda()
+    a = cache.decode_attn(q).clone()
+    b = cache.decode_attn(q)
+    assert torch.equal(a, b)
+    assert kvq.kvq_decode_workspace_bytes(cache.handle, 24) > 0

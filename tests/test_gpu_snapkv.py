@@ -1,0 +1,129 @@
+"""GPU parity: SnapKV scoring (fp32 vs the float64 oracle) and selection.
+
+Selection on identical fp32 scores (snapkv_topk) must equal the oracle's
+bit-exactly.  For the fused call the indices must equal the oracle's exactly
+whenever the oracle's gap at the top-k cutoff exceeds twice the measured
+score error; otherwise the GPU set must still be a valid top-k under the
+oracle scores widened by that error.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import snapkv as osk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import bit_kv_cache_quant_gb300 as m
+
+    return m
+
+
+def _keys(B, H, S, D, seed, sink_rows=4, sink_scale=8.0):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(B, H, S, D, generator=g)
+    k[:, :, :sink_rows] *= sink_scale
+    return k.half()
+
+
+def _topk_gpu(kvq, scores: np.ndarray, budget, n_sink):
+    B, H, S = scores.shape
+    idx = torch.empty((B, H, min(budget, S)), dtype=torch.int32, device="cuda")
+    kvq.snapkv_topk(torch.from_numpy(scores).cuda(), B, H, S, budget, n_sink, idx)
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("S,budget,n_sink", [(5000, 512, 4), (100, 512, 4), (1024, 1023, 0), (3000, 4, 4),
+                                             (17, 9, 3), (70000, 2048, 16), (1, 1, 1), (600, 600, 4)])
+def test_topk_bit_exact_on_identical_scores(kvq, S, budget, n_sink):
+    rng = np.random.default_rng(S + budget)
+    scores = rng.random((2, 3, S)).astype(np.float32) * 1e-3
+    # exact ties across the cutoff, zeros and negative zeros
+    scores[:, :, rng.integers(0, S, size=min(S, 50))] = scores[0, 0, S // 2]
+    scores[0, 1, : S // 3] = 0.0
+    scores[1, 2, : S // 4] = -0.0
+    got = _topk_gpu(kvq, scores, budget, n_sink)
+    for b in range(2):
+        for h in range(3):
+            ref = osk.select_indices(scores[b, h], budget, n_sink)
+            np.testing.assert_array_equal(got[b, h], ref, err_msg=f"b{b} h{h}")
+
+
+def test_topk_negative_scores_order(kvq):
+    scores = np.array([[[-3.0, -1.0, -2.0, 5.0, -0.5, 0.0]]], np.float32)
+    got = _topk_gpu(kvq, scores, 3, 1)
+    assert got[0, 0].tolist() == osk.select_indices(scores[0, 0], 3, 1).tolist() == [0, 3, 5]
+
+
+def _check_select(kvq, k, w, budget, n_sink):
+    B, H, S, D = k.shape
+    scores, idx = kvq.snapkv(k.cuda(), w, budget, n_sink)
+    sg = scores.cpu().numpy().astype(np.float64)
+    ig = idx.cpu().numpy()
+    kn = k.float().numpy()
+    worst_gap_ratio = np.inf
+    for b in range(B):
+        for h in range(H):
+            ref = osk.obs_window_scores(kn[b, h], w)
+            eps = np.abs(sg[b, h] - ref).max()
+            assert eps <= 1e-5 * ref.max() + 1e-9, f"score error {eps:.3e}"
+            np.testing.assert_allclose(sg[b, h].sum(), 1.0, rtol=1e-4)
+            ref_idx = osk.select_indices(ref, budget, n_sink)
+            if budget >= S:
+                np.testing.assert_array_equal(ig[b, h], np.arange(S))
+                continue
+            ns = min(n_sink, S)
+            rest = np.sort(ref[ns:])[::-1]
+            kk = budget - ns
+            gap = rest[kk - 1] - rest[kk] if kk > 0 else np.inf
+            worst_gap_ratio = min(worst_gap_ratio, gap / max(eps, 1e-30))
+            if gap > 2 * eps:
+                np.testing.assert_array_equal(ig[b, h], ref_idx)
+            else:
+                sel = set(ig[b, h].tolist())
+                assert set(range(ns)) <= sel and len(sel) == budget
+                cut = rest[kk - 1]
+                for j in range(ns, S):
+                    if ref[j] > cut + 2 * eps:
+                        assert j in sel
+                    if ref[j] < cut - 2 * eps:
+                        assert j not in sel
+            assert np.all(np.diff(ig[b, h]) > 0)
+    return worst_gap_ratio
+
+
+@pytest.mark.parametrize("S,D,w", [(700, 128, 32), (513, 64, 16), (2000, 32, 64), (40, 128, 32), (9, 64, 5)])
+def test_select_small(kvq, S, D, w):
+    k = _keys(1, 2, S, D, seed=S + w)
+    _check_select(kvq, k, w, 64, 4)
+
+
+def test_select_budget_covers_everything(kvq):
+    k = _keys(1, 1, 300, 128, seed=3)
+    _check_select(kvq, k, 32, 512, 4)
+
+
+def test_select_full_size_prompt(kvq):
+    # the 16K-token prompt, 8 kv heads, w = 32, budget 512 with 4 sinks
+    w = synth.get_workload("snapkv")
+    k, _ = synth.snapkv_prefill(w)
+    ratio = _check_select(kvq, k, w.obs_window, w.budget, w.n_sink)
+    print(f"smallest cutoff gap / score error over heads: {ratio:.1f}")
+
+
+def test_select_on_cache_rows_with_head_stride(kvq):
+    # keys read in place from a cache's fp16 K plane (row stride = cap_alloc)
+    B, H, S, D = 1, 2, 600, 128
+    cache = kvq.KVCache(B, H, D, S, "fp16", 16, 0, "fp16", 16, 0)
+    k = _keys(B, H, S, D, seed=21)
+    cache.append(k.cuda(), k.cuda())
+    ws = torch.empty(kvq.snapkv_workspace_bytes(B, H, S, D, 32), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((B, H, 100), dtype=torch.int32, device="cuda")
+    kplane = cache.plane("k_codes", B * H * cache.layout.cap_alloc * 2 * D).view(torch.float16)
+    kvq.snapkv_select(kplane, cache.layout.cap_alloc, B, H, S, D, 32, 100, 4, None, idx, ws)
+    _, ref = kvq.snapkv(k.cuda(), 32, 100, 4)
+    assert torch.equal(idx, ref)
