@@ -77,8 +77,10 @@ def test_zero_bias_is_byte_identical_to_no_bias(kvq):
     a.append(k.cuda(), k.cuda())
     b.append(k.cuda(), k.cuda())
     pa, pb = gpu_planes(a), gpu_planes(b)
-    np.testing.assert_array_equal(pa["k_rows"], pb["k_rows"])
-    np.testing.assert_array_equal(pa["k_tok_scale"].view(np.uint16), pb["k_tok_scale"].view(np.uint16))
+    # rows past the 40 stored ones were never written and hold whatever the buffer held
+    np.testing.assert_array_equal(pa["k_rows"][:, :, :40], pb["k_rows"][:, :, :40])
+    np.testing.assert_array_equal(pa["k_tok_scale"][:, :, :40].view(np.uint16),
+                                  pb["k_tok_scale"][:, :, :40].view(np.uint16))
 
 
 def test_constant_and_zero_rows(kvq):
