@@ -205,6 +205,11 @@ size_t live_bytes(const kvq_cache_s* c, int stored) {
 
 void kvq::note_launch(int n) { g_launches += n; }
 
+kvq_status kvq::report_error(kvq_status s, const char* msg) {
+  begin_call();
+  return fail(s, "%s", msg);
+}
+
 extern "C" {
 
 int32_t kvq_abi_version(void) { return KVQ_ABI_VERSION; }

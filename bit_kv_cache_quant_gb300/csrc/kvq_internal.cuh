@@ -118,6 +118,9 @@ __device__ __forceinline__ int q40_code(float x, float d) {
 // Counts kernels enqueued by the current API call (host side, per thread).
 void note_launch(int n = 1);
 
+// Records `msg` as the calling thread's last error and returns `s`.
+kvq_status report_error(kvq_status s, const char* msg);
+
 // Launchers (defined in the kernel files).
 cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, int in_dtype, bool calibrate,
                           cudaStream_t st);

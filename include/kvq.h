@@ -212,6 +212,27 @@ size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
 kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                            float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* kvq_decode_attn for callers that cannot allocate device memory.  The pages
+   have no counterpart of this call; it exists for this library's users.
+   Some callers may not call cudaMalloc at all: code running inside an allocator
+   or memory-pool callback, plugin hosts that forbid device allocations after
+   start-up, loops that must never enter the driver's allocator.  This call
+   takes the same cache, q and out as kvq_decode_attn but no workspace: the
+   split-KV partials go to a fixed device array inside the library of
+   kvq_noalloc_scratch_bytes() bytes (4 MiB), which every GPU that loads the
+   library holds until the process exits.  A cache whose
+   kvq_decode_workspace_bytes exceeds that returns KVQ_ERR_CAPACITY and enqueues
+   nothing.  The first call on each device looks up the array's device address
+   (cudaGetSymbolAddress, that device current); make that first call before any
+   stream capture.  All calls on a device share the array and leave their last
+   contents in it (nothing in it needs to start at zero): calls that overlap on
+   the GPU race and give wrong results, so serialise them.  Allocates nothing. */
+kvq_status kvq_decode_attn_noalloc(kvq_cache cache, const void* q, void* out, int32_t n_q_heads,
+                                   int32_t io_dtype, float softmax_scale, cudaStream_t stream);
+
+/* Size in bytes of the built-in scratch array kvq_decode_attn_noalloc uses. */
+size_t kvq_noalloc_scratch_bytes(void);
+
 /* Workspace bytes snapkv_select needs. */
 size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int32_t head_dim,
                               int32_t obs_window);
