@@ -7,14 +7,18 @@
 // scales upcast to fp32.  mlx-qsdpa (same memo, section 5) splits long
 // contexts; here every (b, kv head) is split over `nsplit` CTAs whose
 // partial (max, sum, accumulator) triples are merged with the online-softmax
-// rule by the last CTA to finish.
+// rule by the last CTA of the (b, kv head) to finish.
+//
+// Data movement: a CTA streams its token range through shared memory in
+// 64-token tiles.  A tile is a handful of contiguous byte ranges (K codes,
+// V codes and each metadata plane for those 64 rows), copied with 16-byte
+// cp.async by all threads, NSTAGE tiles ahead of the one being computed.
 //
 // Work mapping: a token row of D channels is read by D/16 lanes, each lane
-// owning 16 consecutive channels (8, 16 or 32 bytes of codes: one 64- or
-// 128-bit load).  A warp covers 32/(D/16) tokens at a time, the CTA (4 warps)
-// processes C such token groups per step, loading all their codes before
-// using any.  The G query heads that share a kv head are computed together so
-// each code is read once.
+// owning 16 consecutive channels (8, 16 or 32 bytes of codes: one shared-
+// memory vector load).  A warp covers 32/(D/16) tokens at a time.  The G
+// query heads that share a kv head are computed together so each code is
+// read once.
 //
 // Arithmetic kept out of the per-element loop:
 //  * per-token affine keys: q . k_hat = s * sum(q_i u_i) + z * sum(q_i) over
@@ -34,27 +38,37 @@
 namespace kvq {
 
 constexpr int kDecodeWarps = 4;
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kTileTokens = 64;       // divides kRowAlign: whole tiles stay inside cap_alloc
 
 template <int F> struct FmtBits {
   static constexpr int v = (F == F_FP16) ? 16 : ((F == F_KIVI8 || F == F_AFF8) ? 8 : 4);
 };
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
 // Codes of one lane's 16 channels.
 template <int BITS> struct Codes { uint32_t w[BITS / 2]; };
 
 template <int BITS>
-__device__ __forceinline__ void load_codes(Codes<BITS>& c, const uint8_t* p) {
+__device__ __forceinline__ void load_codes_smem(Codes<BITS>& c, const uint8_t* p) {
   if constexpr (BITS == 16) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+    const uint4 b = reinterpret_cast<const uint4*>(p)[1];
     c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
     c.w[4] = b.x; c.w[5] = b.y; c.w[6] = b.z; c.w[7] = b.w;
   } else if constexpr (BITS == 8) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
     c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
   } else {
-    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
     c.w[0] = a.x; c.w[1] = a.y;
   }
 }
@@ -99,11 +113,165 @@ __device__ __forceinline__ void unpack(const Codes<BITS>& c, float (&x)[16]) {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-template <int D, int G, int KF, int VF, int C>
-__global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) {
+// Byte offsets of one pipeline stage (one 64-token tile) in shared memory.
+struct TileLayout {
+  int kc, vc, ks, kz, vs, vz, bytes;
+};
+
+template <int D, int KF, int VF>
+__host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
+  constexpr int KROW = D * FmtBits<KF>::v / 8;
+  constexpr int VROW = D * FmtBits<VF>::v / 8;
+  constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
+  constexpr bool K_Q40 = (KF == F_Q40);
+  constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  TileLayout L;
+  int off = 0;
+  L.kc = off; off += kTileTokens * KROW;
+  L.vc = off; off += kTileTokens * VROW;
+  L.ks = off; off += (K_AFF || K_Q40) ? kTileTokens * kng * 2 : 0;
+  L.kz = off; off += K_AFF ? kTileTokens * kng * 2 : 0;
+  L.vs = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
+  L.vz = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
+  L.bytes = off;   // every term is a multiple of 128 bytes
+  return L;
+}
+
+// Merges the per-warp (max, sum, accumulator) triples in shared memory and writes
+// the output (one split) or this split's partial; the last split of a (b, kv head)
+// to finish merges every partial with the online-softmax rule.
+template <int D, int G>
+__device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split,
+                                            float (*sm_m)[G], float (*sm_l)[G], float (*sm_acc)[G][D]) {
+  constexpr int PROW = D + kPartialPad;
+  __shared__ float sm_w[kMaxSplits][G];
+  __shared__ float sm_inv[G];
+  __shared__ int s_last;
+  const size_t bh = (size_t)b * c.Hkv + kvh;
+  // Merge the warps; write the output (one split) or this split's partial.
+  for (int idx = threadIdx.x; idx < G * D; idx += kDecodeThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = sm_m[0][h];
+#pragma unroll
+    for (int w = 1; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w][h]);
+    float A = 0.0f, L = 0.0f;
+    if (M != neg_inf()) {
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) {
+        const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
+        A = fmaf(sm_acc[w][h][d], e, A);
+        L = fmaf(sm_l[w][h], e, L);
+      }
+    }
+    if (a.nsplit == 1) {
+      const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;
+      store_io(a.out, oo, a.io_dtype, L > 0.0f ? A / L : 0.0f);
+    } else {
+      float* P = a.partials + ((bh * a.nsplit + split) * G + h) * PROW;
+      P[d] = A;
+      if (d == 0) {
+        P[D] = M;
+        P[D + 1] = L;
+      }
+    }
+  }
+  if (a.nsplit == 1) return;
+
+  // The last split of this (b, kv head) to finish merges all partials.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(a.nsplit - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* P0 = a.partials + bh * a.nsplit * G * PROW;
+  // every split's (max, sum) at once, then one weight per (split, head)
+  for (int i = threadIdx.x; i < a.nsplit * G; i += kDecodeThreads) sm_w[i / G][i % G] = __ldcg(P0 + i * PROW + D);
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = neg_inf();
+    for (int sp = 0; sp < a.nsplit; ++sp) M = fmaxf(M, sm_w[sp][h]);
+    float L = 0.0f;
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+      const float ms = sm_w[sp][h];
+      const float e = (ms == neg_inf()) ? 0.0f : exp2f(ms - M);
+      L = fmaf(__ldcg(P0 + (sp * G + h) * PROW + D + 1), e, L);
+      sm_w[sp][h] = e;
+    }
+    sm_inv[h] = L > 0.0f ? 1.0f / L : 0.0f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D / 4; idx += kDecodeThreads) {
+    const int h = idx / (D / 4), d4 = idx % (D / 4);
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+      const float4 p = __ldcg(reinterpret_cast<const float4*>(P0 + (sp * G + h) * PROW) + d4);
+      const float e = sm_w[sp][h];
+      A.x = fmaf(p.x, e, A.x);
+      A.y = fmaf(p.y, e, A.y);
+      A.z = fmaf(p.z, e, A.z);
+      A.w = fmaf(p.w, e, A.w);
+    }
+    const float inv = sm_inv[h];
+    const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + 4 * d4;
+    store_io(a.out, oo + 0, a.io_dtype, A.x * inv);
+    store_io(a.out, oo + 1, a.io_dtype, A.y * inv);
+    store_io(a.out, oo + 2, a.io_dtype, A.z * inv);
+    store_io(a.out, oo + 3, a.io_dtype, A.w * inv);
+  }
+  if (threadIdx.x == 0) c.split_sem[bh] = 0u;
+}
+
+template <int KF> struct Stages { static constexpr int v = (KF == F_FP16) ? 3 : 4; };
+
+// Copies rows [row0, row0 + 64) of every plane of one (b, kv head) into a stage.
+template <int D, int KF, int VF>
+__device__ __forceinline__ void issue_tile(uint8_t* st, const TileLayout& L, const CacheView& c, size_t bh,
+                                           int row0) {
+  constexpr int KROW = D * FmtBits<KF>::v / 8;
+  constexpr int VROW = D * FmtBits<VF>::v / 8;
+  constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
+  constexpr bool K_Q40 = (KF == F_Q40);
+  constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  const size_t row = bh * c.cap_alloc + row0;
+  const int tid = threadIdx.x;
+  {
+    const uint8_t* src = c.k.codes + row * KROW;
+    for (int i = tid; i < kTileTokens * KROW / 16; i += kDecodeThreads) cp_async16(st + L.kc + 16 * i, src + 16 * i);
+  }
+  {
+    const uint8_t* src = c.v.codes + row * VROW;
+    for (int i = tid; i < kTileTokens * VROW / 16; i += kDecodeThreads) cp_async16(st + L.vc + 16 * i, src + 16 * i);
+  }
+  if constexpr (K_AFF || K_Q40) {
+    const int n16 = kTileTokens * c.k.n_groups * 2 / 16;
+    const uint8_t* s1 = reinterpret_cast<const uint8_t*>(c.k.tok_scale + row * c.k.n_groups);
+    for (int i = tid; i < n16; i += kDecodeThreads) cp_async16(st + L.ks + 16 * i, s1 + 16 * i);
+    if constexpr (K_AFF) {
+      const uint8_t* s2 = reinterpret_cast<const uint8_t*>(c.k.tok_zero + row * c.k.n_groups);
+      for (int i = tid; i < n16; i += kDecodeThreads) cp_async16(st + L.kz + 16 * i, s2 + 16 * i);
+    }
+  }
+  if constexpr (V_AFF) {
+    const int n16 = kTileTokens * c.v.n_groups * 2 / 16;
+    const uint8_t* s1 = reinterpret_cast<const uint8_t*>(c.v.tok_scale + row * c.v.n_groups);
+    const uint8_t* s2 = reinterpret_cast<const uint8_t*>(c.v.tok_zero + row * c.v.n_groups);
+    for (int i = tid; i < n16; i += kDecodeThreads) {
+      cp_async16(st + L.vs + 16 * i, s1 + 16 * i);
+      cp_async16(st + L.vz + 16 * i, s2 + 16 * i);
+    }
+  }
+}
+
+template <int D, int G, int KF, int VF>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, DecodeArgs a) {
   constexpr int NL = D / 16;                  // lanes per token
   constexpr int TPW = 32 / NL;                // tokens per warp per step
   constexpr int TPC = TPW * kDecodeWarps;     // tokens per CTA per step
+  constexpr int C = kTileTokens / TPC;        // steps per tile
+  constexpr int NSTAGE = Stages<KF>::v;
   constexpr int KB = FmtBits<KF>::v;
   constexpr int VB = FmtBits<VF>::v;
   constexpr int KROW = D * KB / 8;
@@ -113,11 +281,11 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
   constexpr bool K_Q40 = (KF == F_Q40);
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
 
+  extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float sm_m[kDecodeWarps][G];
   __shared__ float sm_l[kDecodeWarps][G];
-  __shared__ float sm_acc[kDecodeWarps][G][D];
+  __shared__ __align__(16) float sm_acc[kDecodeWarps][G][D];
   __shared__ int s_T;
-  __shared__ int s_last;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -126,13 +294,25 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
   const int slot = warp * TPW + grp;
   const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
   const size_t bh = (size_t)b * c.Hkv + kvh;
+  const int kng = c.k.n_groups;
+  const int vng = c.v.n_groups;
+  const TileLayout TL = tile_layout<D, KF, VF>(kng, vng);
 
   if (threadIdx.x == 0) s_T = c.state->stored;
   __syncthreads();
   const int T = s_T;
-  const int per = (T + a.nsplit - 1) / a.nsplit;
+  int per = (T + a.nsplit - 1) / a.nsplit;
+  per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
   const int t0 = min(T, split * per);
   const int t1 = min(T, t0 + per);
+  const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
+
+  // Start streaming before anything else.
+#pragma unroll
+  for (int s = 0; s < NSTAGE - 1; ++s) {
+    if (s < ntiles) issue_tile<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens);
+    cp_async_commit();
+  }
 
   // Query slice, pre-scaled by softmax_scale * log2(e) so exp2 can be used.
   float qf[G][16];
@@ -159,17 +339,8 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
     for (int i = 0; i < 16; ++i) s += qf[h][i];
     qsum[h] = s;
   }
-
-  const int kng = c.k.n_groups;
-  const int vng = c.v.n_groups;
   const int kg = K_AFF ? (16 * j) / c.k.group : (K_Q40 ? (j >> 1) : 0);
   const int vg = V_AFF ? (16 * j) / c.v.group : 0;
-  const uint8_t* kbase = c.k.codes + bh * c.cap_alloc * KROW + j * (KROW / NL);
-  const uint8_t* vbase = c.v.codes + bh * c.cap_alloc * VROW + j * (VROW / NL);
-  const __half* ksb = (K_AFF || K_Q40) ? c.k.tok_scale + bh * c.cap_alloc * kng + kg : nullptr;
-  const __half* kzb = K_AFF ? c.k.tok_zero + bh * c.cap_alloc * kng + kg : nullptr;
-  const __half* vsb = V_AFF ? c.v.tok_scale + bh * c.cap_alloc * vng + vg : nullptr;
-  const __half* vzb = V_AFF ? c.v.tok_zero + bh * c.cap_alloc * vng + vg : nullptr;
 
   float m[G], l[G], zacc[G], acc[G][16];
 #pragma unroll
@@ -181,53 +352,51 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
     for (int i = 0; i < 16; ++i) acc[h][i] = 0.0f;
   }
 
-  for (int base = t0; base < t1; base += TPC * C) {
-    Codes<KB> kc[C];
-    Codes<VB> vc[C];
-    float ksc[C], kzr[C], vsc[C], vzr[C];
-    bool valid[C];
-#pragma unroll
-    for (int cc = 0; cc < C; ++cc) {
-      const int t = base + cc * TPC + slot;
-      valid[cc] = t < t1;
-      const size_t tt = valid[cc] ? (size_t)t : (size_t)t0;
-      load_codes<KB>(kc[cc], kbase + tt * KROW);
-      load_codes<VB>(vc[cc], vbase + tt * VROW);
-      if constexpr (K_AFF || K_Q40) ksc[cc] = __half2float(ksb[tt * kng]);
-      if constexpr (K_AFF) kzr[cc] = __half2float(kzb[tt * kng]);
-      if constexpr (V_AFF) {
-        vsc[cc] = __half2float(vsb[tt * vng]);
-        vzr[cc] = __half2float(vzb[tt * vng]);
-      }
+  for (int it = 0; it < ntiles; ++it) {
+    cp_async_wait<NSTAGE - 2>();
+    __syncthreads();
+    {
+      const int nx = it + NSTAGE - 1;
+      if (nx < ntiles) issue_tile<D, KF, VF>(smem + (nx % NSTAGE) * TL.bytes, TL, c, bh, t0 + nx * kTileTokens);
+      cp_async_commit();
     }
+    const uint8_t* st = smem + (it % NSTAGE) * TL.bytes;
+    const int tbase = t0 + it * kTileTokens;
 
-    // Scores (log2 domain) of this lane-group's C tokens.
+    // Scores (log2 domain) of this lane-group's C tokens of the tile.
     float s[C][G];
 #pragma unroll
     for (int cc = 0; cc < C; ++cc) {
+      const int r = cc * TPC + slot;
+      Codes<KB> kc;
+      load_codes_smem<KB>(kc, st + TL.kc + r * KROW + j * (KROW / NL));
       float x[16];
-      unpack<KB>(kc[cc], x);
+      unpack<KB>(kc, x);
+      float ksc = 0.0f, kzr = 0.0f;
+      if constexpr (K_AFF || K_Q40) ksc = __half2float(reinterpret_cast<const __half*>(st + TL.ks)[r * kng + kg]);
+      if constexpr (K_AFF) kzr = __half2float(reinterpret_cast<const __half*>(st + TL.kz)[r * kng + kg]);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float p = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) p = fmaf(qf[h][i], x[i], p);
-        if constexpr (K_AFF) p = fmaf(ksc[cc], p, kzr[cc] * qsum[h]);
-        if constexpr (K_Q40) p = ksc[cc] * fmaf(-8.0f, qsum[h], p);
+        if constexpr (K_AFF) p = fmaf(ksc, p, kzr * qsum[h]);
+        if constexpr (K_Q40) p = ksc * fmaf(-8.0f, qsum[h], p);
         s[cc][h] = p;
       }
     }
 #pragma unroll
     for (int cc = 0; cc < C; ++cc) {
+      const bool valid = tbase + cc * TPC + slot < t1;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
         for (int o = NL / 2; o >= 1; o >>= 1) s[cc][h] += __shfl_xor_sync(0xffffffffu, s[cc][h], o);
-        if (!valid[cc]) s[cc][h] = neg_inf();
+        if (!valid) s[cc][h] = neg_inf();
       }
     }
 
-    // Online softmax: one rescale per step.
+    // Online softmax: one rescale per tile.
     float pw[C][G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -254,15 +423,26 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
     }
 #pragma unroll
     for (int cc = 0; cc < C; ++cc) {
+      // rows past the split's end hold whatever the buffer held (possibly NaN
+      // metadata or fp16 values): skip them rather than weight them by zero
+      if (tbase + cc * TPC + slot >= t1) continue;
+      const int r = cc * TPC + slot;
+      Codes<VB> vcod;
+      load_codes_smem<VB>(vcod, st + TL.vc + r * VROW + j * (VROW / NL));
       float x[16];
-      unpack<VB>(vc[cc], x);
+      unpack<VB>(vcod, x);
+      float vsc = 0.0f, vzr = 0.0f;
+      if constexpr (V_AFF) {
+        vsc = __half2float(reinterpret_cast<const __half*>(st + TL.vs)[r * vng + vg]);
+        vzr = __half2float(reinterpret_cast<const __half*>(st + TL.vz)[r * vng + vg]);
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         if constexpr (V_AFF) {
-          const float w = pw[cc][h] * vsc[cc];
+          const float w = pw[cc][h] * vsc;
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc[h][i] = fmaf(w, x[i], acc[h][i]);
-          zacc[h] = fmaf(pw[cc][h], vzr[cc], zacc[h]);
+          zacc[h] = fmaf(pw[cc][h], vzr, zacc[h]);
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc[h][i] = fmaf(pw[cc][h], x[i], acc[h][i]);
@@ -270,6 +450,7 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
       }
     }
   }
+  cp_async_wait<0>();
 
   if constexpr (V_AFF) {
 #pragma unroll
@@ -277,7 +458,6 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc[h][i] += zacc[h];
   }
-
   // Merge the lane-groups of the warp (lanes that share a channel slice).
 #pragma unroll
   for (int o = NL; o < 32; o <<= 1) {
@@ -301,7 +481,9 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
 #pragma unroll
     for (int h = 0; h < G; ++h) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sm_acc[warp][h][16 * j + i] = acc[h][i];
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(&sm_acc[warp][h][16 * j + i]) =
+            make_float4(acc[h][i], acc[h][i + 1], acc[h][i + 2], acc[h][i + 3]);
       if (j == 0) {
         sm_m[warp][h] = m[h];
         sm_l[warp][h] = l[h];
@@ -310,68 +492,24 @@ __global__ void __launch_bounds__(128) decode_kernel(CacheView c, DecodeArgs a) 
   }
   __syncthreads();
 
-  // Merge the warps; write the output (one split) or this split's partial.
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
-    float M = sm_m[0][h];
-#pragma unroll
-    for (int w = 1; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w][h]);
-    float A = 0.0f, L = 0.0f;
-    if (M != neg_inf()) {
-#pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
-        A = fmaf(sm_acc[w][h][d], e, A);
-        L = fmaf(sm_l[w][h], e, L);
-      }
-    }
-    if (a.nsplit == 1) {
-      const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;
-      store_io(a.out, oo, a.io_dtype, L > 0.0f ? A / L : 0.0f);
-    } else {
-      float* P = a.partials + ((bh * a.nsplit + split) * G + h) * (D + 2);
-      P[d] = A;
-      if (d == 0) {
-        P[D] = M;
-        P[D + 1] = L;
-      }
-    }
-  }
-  if (a.nsplit == 1) return;
-
-  // The last split of this (b, kv head) to finish merges all partials.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(a.nsplit - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
-    const float* P0 = a.partials + (bh * a.nsplit * G + h) * (D + 2);
-    const size_t stride = (size_t)G * (D + 2);
-    float M = neg_inf();
-    for (int sp = 0; sp < a.nsplit; ++sp) M = fmaxf(M, __ldcg(P0 + sp * stride + D));
-    float A = 0.0f, L = 0.0f;
-    if (M != neg_inf()) {
-      for (int sp = 0; sp < a.nsplit; ++sp) {
-        const float ms = __ldcg(P0 + sp * stride + D);
-        const float e = (ms == neg_inf()) ? 0.0f : exp2f(ms - M);
-        A = fmaf(__ldcg(P0 + sp * stride + d), e, A);
-        L = fmaf(__ldcg(P0 + sp * stride + D + 1), e, L);
-      }
-    }
-    const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;
-    store_io(a.out, oo, a.io_dtype, L > 0.0f ? A / L : 0.0f);
-  }
-  if (threadIdx.x == 0) c.split_sem[bh] = 0u;
+  merge_store<D, G>(c, a, b, kvh, split, sm_m, sm_l, sm_acc);
 }
 
 template <int D, int G, int KF, int VF>
 cudaError_t launch_decode_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  constexpr int C = (G >= 3) ? 2 : 4;
+  constexpr int NSTAGE = Stages<KF>::v;
+  const TileLayout L = tile_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
+  const int smem = NSTAGE * L.bytes;
+  if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  static int configured_for = -1;   // dynamic shared memory above 48 KB needs an opt-in
+  if (configured_for < smem) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes);
+    if (e != cudaSuccess) return e;
+    configured_for = NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes;
+  }
   const dim3 grid(a.nsplit, c.Hkv, c.B);
-  decode_kernel<D, G, KF, VF, C><<<grid, 128, 0, st>>>(c, a);
+  decode_kernel<D, G, KF, VF><<<grid, kDecodeThreads, smem, st>>>(c, a);
   note_launch();
   return cudaGetLastError();
 }
@@ -387,8 +525,9 @@ cudaError_t launch_decode_d(const CacheView& c, int G, const DecodeArgs& a, cuda
   }
 }
 
+// CUDA-core path: exact fp32 arithmetic on the codes, up to 4 query heads per kv head.
 template <int KF, int VF>
-cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_cc(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st) {
   switch (c.D) {
     case 32: return launch_decode_d<32, KF, VF>(c, G, a, st);
     case 64: return launch_decode_d<64, KF, VF>(c, G, a, st);

@@ -1,5 +1,5 @@
 // Decode attention instantiated for keys in KIVI8 and values in AFF8.
-#include "decode_impl.cuh"
+#include "decode_tc.cuh"
 
 namespace kvq {
 template cudaError_t launch_decode<F_KIVI8, F_AFF8>(const CacheView&, int, const DecodeArgs&, cudaStream_t);

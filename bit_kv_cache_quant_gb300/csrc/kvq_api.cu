@@ -176,14 +176,15 @@ kvq::SideView side_view(uint8_t* base, int fmt, int bits, int group, int row_b, 
 }
 
 int decode_nsplit(const kvq_cache_s* c) {
+  // About eight CTAs per SM in all (even waves), at least 256 rows per split.
   const int units = c->cfg.batch * c->cfg.n_kv_heads;
   int rows = c->cfg.capacity;
   if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);
-  const int target = 4 * c->sms;
-  int ns = (target + units - 1) / units;
+  const int target = 8 * c->sms;
+  int ns = (target + units / 2) / units;
   const int max_by_len = rows / 256 > 1 ? rows / 256 : 1;
   if (ns > max_by_len) ns = max_by_len;
-  if (ns > 128) ns = 128;
+  if (ns > kvq::kMaxSplits) ns = kvq::kMaxSplits;
   if (ns < 1) ns = 1;
   return ns;
 }
@@ -325,7 +326,7 @@ size_t kvq_decode_workspace_bytes(kvq_cache c, int32_t n_q_heads) {
   const int ns = decode_nsplit(c);
   if (ns == 1) return 0;
   const size_t G = n_q_heads / c->cfg.n_kv_heads;
-  return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + 2) * sizeof(float);
+  return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + kvq::kPartialPad) * sizeof(float);
 }
 
 kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
@@ -337,7 +338,7 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   if (n_q_heads < 1 || n_q_heads % c->cfg.n_kv_heads)
     return fail(KVQ_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
   const int G = n_q_heads / c->cfg.n_kv_heads;
-  if (G > 4) return fail(KVQ_ERR_UNSUPPORTED, "query heads per kv head must be <= 4 (got %d)", G);
+  if (G > 8) return fail(KVQ_ERR_UNSUPPORTED, "query heads per kv head must be <= 8 (got %d)", G);
   if (c->cfg.k_format == KVQ_FMT_KIVI_CHAN && !c->k_calibrated)
     return fail(KVQ_ERR_UNSUPPORTED, "per-channel K scales are not calibrated yet");
   const size_t need = kvq_decode_workspace_bytes(c, n_q_heads);

@@ -133,7 +133,7 @@ struct DecodeArgs {
   int io_dtype;
   int Hq;
   float qscale;      // softmax scale * log2(e)
-  float* partials;   // [B*Hkv][nsplit][G][D+2] or null when nsplit == 1
+  float* partials;   // [B*Hkv][nsplit][G][D + kPartialPad] or null when nsplit == 1
   int nsplit;
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
@@ -147,5 +147,7 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
                         cudaStream_t st);
 
 constexpr int kSnapChunk = 512;   // keys per CTA of the SnapKV scoring kernels
+constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)
+constexpr int kPartialPad = 4;    // decode partial row: D accumulators, max, sum, 2 pad (16-byte rows)
 
 }  // namespace kvq

@@ -109,6 +109,21 @@ def test_peaked_attention_and_custom_scale(kvq):
     assert_attention_close(out, ref, "scale 0.5")
 
 
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}{p[1]}-{p[3]}{p[4]}")
+@pytest.mark.parametrize("G", [5, 6, 8])
+def test_decode_up_to_eight_heads_per_kv_head(kvq, pair, G):
+    # bf16 io and head_dim 128 take the tensor-core kernel, which carries up to 8 heads
+    cache, oc = _build(kvq, pair, 1, 2, 128, 700, torch.bfloat16, seed=G, bias=pair[0] == "q4_0")
+    _check(kvq, cache, oc, G, torch.bfloat16, seed=G + 1, what=f"G={G}")
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}{p[1]}-{p[3]}{p[4]}")
+def test_decode_fp32_io_head_dim_128(kvq, pair):
+    # fp32 io keeps the exact CUDA-core kernel (1e-5 tolerance) at head_dim 128 too
+    cache, oc = _build(kvq, pair, 2, 2, 128, 600, torch.float32, seed=77, bias=pair[0] == "q4_0")
+    _check(kvq, cache, oc, 4, torch.float32, seed=78, what="fp32 io")
+
+
 def test_repeated_calls_are_identical(kvq):
     # split merge counters reset themselves: the same call twice gives the same bytes
     pair = ("affine_token", 4, 64, "affine_token", 4, 64)
