@@ -48,6 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    p.add_argument("--layers", type=int, default=0,
+                   help="override the workload's layer count (profiling small footprints; not a bench line)")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     return a
@@ -536,6 +538,8 @@ def main(argv=None):
     import bit_kv_cache_quant_gb300 as kvq
 
     w = synth.get_workload(a.workload)
+    if a.layers > 0:
+        w = w.with_(layers=a.layers)
     line = bench_snapkv(a, kvq, w, rank, world) if w.prompt_len else bench_decode(a, kvq, w, rank, world)
     if rank == 0 and not a.no_cpu_baseline and not w.prompt_len:
         line["cpu_baseline"] = cpu_baseline(w, a.cpu_seconds)

@@ -116,6 +116,7 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // Byte offsets of one pipeline stage (one 64-token tile) in shared memory.
 struct TileLayout {
   int kc, vc, ks, kz, vs, vz, bytes;
+  int tx;   // bytes actually transferred into a stage
 };
 
 template <int D, int KF, int VF>
@@ -134,16 +135,20 @@ __host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
   L.vs = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
   L.vz = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
   L.bytes = off;   // every term is a multiple of 128 bytes
+  L.tx = off;
   return L;
 }
 
 // Merges the per-warp (max, sum, accumulator) triples in shared memory and writes
 // the output (one split) or this split's partial; the last split of a (b, kv head)
 // to finish merges every partial with the online-softmax rule.
-template <int D, int G>
+// Accumulator layout: ACCPAD == 0: acc[warp][h][d]; ACCPAD > 0 (tensor-core
+// kernel): rows of D + ACCPAD floats, channel d at (d % (D/8)) * 8 + d / (D/8).
+template <int D, int G, int ACCPAD>
 __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split,
-                                            float (*sm_m)[G], float (*sm_l)[G], float (*sm_acc)[G][D]) {
+                                            float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc) {
   constexpr int PROW = D + kPartialPad;
+  constexpr int AROW = D + ACCPAD;
   __shared__ float sm_w[kMaxSplits][G];
   __shared__ float sm_inv[G];
   __shared__ int s_last;
@@ -151,6 +156,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   // Merge the warps; write the output (one split) or this split's partial.
   for (int idx = threadIdx.x; idx < G * D; idx += kDecodeThreads) {
     const int h = idx / D, d = idx % D;
+    const int pos = h * AROW + (ACCPAD ? (d % (D / 8)) * 8 + d / (D / 8) : d);
     float M = sm_m[0][h];
 #pragma unroll
     for (int w = 1; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w][h]);
@@ -159,7 +165,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
 #pragma unroll
       for (int w = 0; w < kDecodeWarps; ++w) {
         const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
-        A = fmaf(sm_acc[w][h][d], e, A);
+        A = fmaf(sm_acc[w * G * AROW + pos], e, A);
         L = fmaf(sm_l[w][h], e, L);
       }
     }
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   }
   __syncthreads();
 
-  merge_store<D, G>(c, a, b, kvh, split, sm_m, sm_l, sm_acc);
+  merge_store<D, G, 0>(c, a, b, kvh, split, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
 template <int D, int G, int KF, int VF>

@@ -1,0 +1,203 @@
+// Fragment, tile and TMA helpers of the tensor-core decode kernel (decode_tc.cuh).
+//
+// A pipeline stage holds one 64-token tile: the K and V code planes arrive by
+// TMA tensor copies (one per plane) with the hardware 16-byte-chunk swizzle of
+// the row length (32 / 64 / 128 bytes; 256-byte rows as [row][2][128]), the
+// per-token metadata planes by bulk copies.  One thread issues them and arms
+// the stage's mbarrier with the byte count; every thread waits on the mbarrier
+// (bounded in time) before reading the stage.
+#pragma once
+
+#include "decode_impl.cuh"
+
+namespace kvq {
+
+__device__ __forceinline__ __half2 u2h(uint32_t x) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = x;
+  return h;
+}
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Eight nibbles of w (channel i in bits 4i..4i+3) as exact fp16 pairs:
+// h[0] = (c0, c4), h[1] = (c1, c5), h[2] = (c2, c6), h[3] = (c3, c7).
+// 0x6400 | n is 1024 + n; 0x6400 | (n << 4) is 1024 + 16 n.
+__device__ __forceinline__ void nibbles_to_h2(uint32_t w, __half2 (&h)[4]) {
+  const uint32_t M = 0x64006400u;
+  const __half2 k1024 = u2h(0x64006400u);
+  const __half2 k16th = u2h(0x2C002C00u);   // 1/16
+  const __half2 km64 = u2h(0xD400D400u);    // -64
+  const uint32_t w8 = w >> 8;
+  h[0] = __hsub2(u2h((w & 0x000F000Fu) | M), k1024);
+  h[1] = __hfma2(u2h((w & 0x00F000F0u) | M), k16th, km64);
+  h[2] = __hsub2(u2h((w8 & 0x000F000Fu) | M), k1024);
+  h[3] = __hfma2(u2h((w8 & 0x00F000F0u) | M), k16th, km64);
+}
+
+// Four unsigned bytes of x as exact fp16 pairs: lo = (b0, b1), hi = (b2, b3).
+__device__ __forceinline__ void bytes_to_h2(uint32_t x, __half2& lo, __half2& hi) {
+  const __half2 k1024 = u2h(0x64006400u);
+  lo = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x5140u)), k1024);
+  hi = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x7362u)), k1024);
+}
+
+// Logical k index j of a 16-token block -> physical row inside the block.
+// The value fragments of quad thread t read rows tau(2t), tau(2t + 1),
+// tau(2t + 8), tau(2t + 9); the order is chosen so those reads are free of
+// bank conflicts for the value row length: 64-byte (and shorter) rows use
+// tau(2t + e) = t + 4e, tau(8 + 2t + e) = 8 + t + 4e; 128-byte and longer rows
+// the identity.  Key loads are conflict-free under either.
+template <int VROW>
+__device__ __forceinline__ int tau(int j) {
+  if constexpr (VROW >= 128) return j;
+  else return (j & 8) + ((j & 7) >> 1) + 4 * (j & 1);
+}
+
+// Shared-memory byte offset of byte `off` of tile row r of a code plane whose
+// rows are ROWB bytes, as the TMA swizzle places it: the 16-byte chunk index
+// is XORed with address bits 7.. of the row (bits 7-9 for 128-byte spans,
+// 7-8 for 64, 7 for 32); a 256-byte row is two 128-byte rows.
+template <int ROWB>
+__device__ __forceinline__ int swz_off(int r, int off) {
+  if constexpr (ROWB == 256) {
+    const int half = off >> 7;
+    return r * 256 + half * 128 + ((((off >> 4) & 7) ^ ((2 * r + half) & 7)) << 4) + (off & 15);
+  } else if constexpr (ROWB == 128) {
+    return r * 128 + ((((off >> 4) ^ r) & 7) << 4) + (off & 15);
+  } else if constexpr (ROWB == 64) {
+    return r * 64 + ((((off >> 4) ^ (r >> 1)) & 3) << 4) + (off & 15);
+  } else {
+    static_assert(ROWB == 32, "code rows of 32, 64, 128 or 256 bytes");
+    return r * 32 + ((((off >> 4) ^ (r >> 2)) & 1) << 4) + (off & 15);
+  }
+}
+
+// --------------------------------------------------------- mbarrier / TMA --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(m)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of the mbarrier, giving up after ~200 ms (a stage
+// normally completes in microseconds); false means the wait ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity) {
+  if (mbar_try_wait(m, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(m, parity)) {
+    if (global_ns() - t0 > 200000000ull) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// 64 rows of a code plane starting at row y (TMA tensor copy, swizzled).
+template <int ROWB>
+__device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, int y, uint64_t* m) {
+  if constexpr (ROWB == 256) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(0), "r"(0), "r"(y), "r"(smem_u32(m))
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];\n" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(0), "r"(y), "r"(smem_u32(m))
+        : "memory");
+  }
+}
+
+// Contiguous bytes (16-byte aligned, a multiple of 16) into shared memory.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+
+// One thread: copies tile rows [row0, row0 + 64) of every plane into stage `st`.
+template <int D, int KF, int VF>
+__device__ __forceinline__ void issue_tile_tma(uint8_t* st, const TileLayout& L, const CacheView& c, size_t bh,
+                                               int row0, uint64_t* m) {
+  constexpr int KROW = D * FmtBits<KF>::v / 8;
+  constexpr int VROW = D * FmtBits<VF>::v / 8;
+  constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
+  constexpr bool K_Q40 = (KF == F_Q40);
+  constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  const size_t row = bh * c.cap_alloc + row0;
+  mbar_expect_tx(m, (uint32_t)L.tx);
+  tma_rows<KROW>(st + L.kc, &c.kmap, (int)row, m);
+  tma_rows<VROW>(st + L.vc, &c.vmap, (int)row, m);
+  if constexpr (K_AFF || K_Q40) {
+    const uint32_t mb = c.k.n_groups * 2;
+    bulk_copy(st + L.ks, reinterpret_cast<const uint8_t*>(c.k.tok_scale) + row * mb, kTileTokens * mb, m);
+    if constexpr (K_AFF)
+      bulk_copy(st + L.kz, reinterpret_cast<const uint8_t*>(c.k.tok_zero) + row * mb, kTileTokens * mb, m);
+  }
+  if constexpr (V_AFF) {
+    const uint32_t mb = c.v.n_groups * 2;
+    bulk_copy(st + L.vs, reinterpret_cast<const uint8_t*>(c.v.tok_scale) + row * mb, kTileTokens * mb, m);
+    bulk_copy(st + L.vz, reinterpret_cast<const uint8_t*>(c.v.tok_zero) + row * mb, kTileTokens * mb, m);
+  }
+}
+
+// Stage layout with every stage a multiple of 1024 bytes (the 128-byte swizzle
+// pattern repeats every 1024 bytes and needs its destination aligned to it).
+template <int D, int KF, int VF>
+__host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
+  TileLayout L = tile_layout<D, KF, VF>(kng, vng);
+  L.bytes = (L.bytes + 1023) / 1024 * 1024;
+  return L;
+}
+
+// Key channel order: k-step ks, mma k index 2t + jj (jj in {0, 1}) and
+// 2t + 8 + jj of quad thread t.  4-bit codes: thread t reads word t of chunk
+// ks / 2 (channels 32 (ks / 2) + 8 t + 0..7), nibble pairs (c0, c4), (c2, c6)
+// for even ks and (c1, c5), (c3, c7) for odd ks.  8-bit and fp16: thread t
+// reads channels 16 ks + 4 t + 0..3.  Either way k-steps 2p, 2p + 1 cover the
+// 32-channel block p exactly.
+template <int KB>
+__device__ __forceinline__ void key_channels(int ks, int t, int (&ch)[4]) {
+  if constexpr (KB == 4) {
+    const int base = 32 * (ks >> 1) + 8 * t + (ks & 1);
+    ch[0] = base; ch[1] = base + 4; ch[2] = base + 2; ch[3] = base + 6;
+  } else {
+    const int base = 16 * ks + 4 * t;
+    ch[0] = base; ch[1] = base + 1; ch[2] = base + 2; ch[3] = base + 3;
+  }
+}
+
+}  // namespace kvq

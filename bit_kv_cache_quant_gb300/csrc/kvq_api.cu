@@ -5,8 +5,11 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
 #include <new>
 #include <string>
+
+#include <cudaTypedefs.h>
 
 #include "kvq_internal.cuh"
 
@@ -175,6 +178,50 @@ kvq::SideView side_view(uint8_t* base, int fmt, int bits, int group, int row_b, 
   return s;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A code plane of `rows` rows of `row_bytes` bytes, copied 64 rows at a time
+// into shared memory with the 16-byte-chunk swizzle matching the row length.
+bool encode_rows_map(CUtensorMap* m, void* base, size_t rows, int row_bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r;
+  if (row_bytes <= 128) {
+    const CUtensorMapSwizzle sw = row_bytes == 32    ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                     : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (sw == CU_TENSOR_MAP_SWIZZLE_NONE) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)kvq::kTmaRows};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (row_bytes == 256) {
+    const cuuint64_t dims[3] = {128, 2, rows};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {128, 2, (cuuint32_t)kvq::kTmaRows};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    return false;
+  }
+  return r == CUDA_SUCCESS;
+}
+
 int decode_nsplit(const kvq_cache_s* c) {
   // About eight CTAs per SM in all (even waves), at least 256 rows per split.
   const int units = c->cfg.batch * c->cfg.n_kv_heads;
@@ -265,6 +312,11 @@ kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cu
   v.layout = cfg->layout;
   v.sink = cfg->sink;
   v.window = cfg->window;
+  {
+    const size_t rows = (size_t)cfg->batch * cfg->n_kv_heads * lay.cap_alloc;
+    v.has_maps = cfg->head_dim >= 64 && encode_rows_map(&v.kmap, b + lay.k_codes, rows, lay.k_row_bytes) &&
+                 encode_rows_map(&v.vmap, b + lay.v_codes, rows, lay.v_row_bytes);
+  }
   // zero the counters and the split semaphores (they are contiguous at the front)
   e = cudaMemsetAsync(b, 0, lay.k_codes, stream);
   if (e == cudaSuccess && cfg->k_bias)

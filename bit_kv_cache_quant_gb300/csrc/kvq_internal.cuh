@@ -1,6 +1,7 @@
 // Internal definitions shared by the kvq kernels and the C-ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -51,11 +52,18 @@ struct SideView {
 };
 
 struct CacheView {
+  // TMA descriptors of the K and V code planes, viewed as [B*Hkv*cap_alloc rows,
+  // row_bytes] and copied 64 rows at a time with a 32/64/128-byte swizzle (rows
+  // of 256 bytes as [rows][2][128]).  Encoded once per cache; has_maps = 0 when
+  // the driver cannot encode them (the CUDA-core decode kernel is used then).
+  CUtensorMap kmap;
+  CUtensorMap vmap;
   DevState* state;
   unsigned* split_sem;   // [B*Hkv]
   const float* k_bias;   // [Hkv][D] or null
   SideView k, v;
   int B, Hkv, D, cap, cap_alloc, layout, sink, window;
+  int has_maps;
 };
 
 __device__ __forceinline__ void set_status(DevState* st, int code) {
@@ -147,6 +155,7 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
                         cudaStream_t st);
 
 constexpr int kSnapChunk = 512;   // keys per CTA of the SnapKV scoring kernels
+constexpr int kTmaRows = 64;      // rows per TMA box of a code plane (one decode tile)
 constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)
 constexpr int kPartialPad = 4;    // decode partial row: D accumulators, max, sum, 2 pad (16-byte rows)
 

@@ -103,6 +103,8 @@ typedef enum kvq_evict_mode {
 #define KVQ_DEV_OK 0
 #define KVQ_DEV_OVERFLOW 1         /* an append would pass the capacity; nothing was written */
 #define KVQ_DEV_BAD_KEEPSET 2      /* keep-set not strictly ascending or beyond stored rows */
+#define KVQ_DEV_TIMEOUT 3          /* a bounded wait inside a kernel ran out; outputs of that call
+                                      are unspecified */
 
 typedef struct kvq_config {
   int32_t batch;        /* B >= 1 */
