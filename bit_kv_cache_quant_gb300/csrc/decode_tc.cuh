@@ -41,8 +41,8 @@ __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* 
 }
 
 template <int D, int G, int KF, int VF>
-__global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
-  constexpr int NSTAGE = Stages<KF>::v;
+__global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
+  constexpr int NSTAGE = TcStages<D, KF, VF>::v;
   constexpr int KB = FmtBits<KF>::v;
   constexpr int VB = FmtBits<VF>::v;
   constexpr int KROW = D * KB / 8;
@@ -101,12 +101,15 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_
       if (s < ntiles) issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
   }
 
-  // Query fragments in key-channel order; per-block sums of q for grouped keys.
-  uint32_t qa[KS][4];
-  float qblk[NB];
+  // Query fragments in key-channel order, built once by warp 0 into shared
+  // memory (lane-major, one 16-byte vector per k-step) and read back per use;
+  // per-block sums of q for grouped keys.
+  __shared__ __align__(16) uint4 sm_qa[KS][32];
+  __shared__ float sm_qblk[NB][8];
+  if (warp == 0) {
+    float qb[NB];
 #pragma unroll
-  for (int i = 0; i < NB; ++i) qblk[i] = 0.0f;
-  {
+    for (int i = 0; i < NB; ++i) qb[i] = 0.0f;
     const bool live = g < G;
     const size_t qo = ((size_t)b * a.Hq + (size_t)kvh * G + (live ? g : 0)) * D;
 #pragma unroll
@@ -120,26 +123,26 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_
         if constexpr (K_KIVI) x *= __half2float(c.k.ch_scale[bh * D + ch[i]]);
         qv[i] = x;
       }
-      if constexpr (KG) qblk[ks >> 1] += (qv[0] + qv[1]) + (qv[2] + qv[3]);
+      if constexpr (KG) qb[ks >> 1] += (qv[0] + qv[1]) + (qv[2] + qv[3]);
       const __half2 h01 = __floats2half2_rn(qv[0], qv[1]);
       const __half2 h23 = __floats2half2_rn(qv[2], qv[3]);
       const float2 f01 = __half22float2(h01);
       const float2 f23 = __half22float2(h23);
-      qa[ks][0] = h2u(h01);
-      qa[ks][1] = h2u(__floats2half2_rn(qv[0] - f01.x, qv[1] - f01.y));
-      qa[ks][2] = h2u(h23);
-      qa[ks][3] = h2u(__floats2half2_rn(qv[2] - f23.x, qv[3] - f23.y));
+      sm_qa[ks][lane] = make_uint4(h2u(h01), h2u(__floats2half2_rn(qv[0] - f01.x, qv[1] - f01.y)), h2u(h23),
+                                   h2u(__floats2half2_rn(qv[2] - f23.x, qv[3] - f23.y)));
+    }
+    if constexpr (KG) {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 1);
+        qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 2);
+        if (t == 0) sm_qblk[i][g] = qb[i];
+      }
     }
   }
   int kgrp[NB];
-  if constexpr (KG) {
 #pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      qblk[i] += __shfl_xor_sync(0xffffffffu, qblk[i], 1);
-      qblk[i] += __shfl_xor_sync(0xffffffffu, qblk[i], 2);
-      kgrp[i] = K_AFF ? (32 * i) / c.k.group : i;
-    }
-  }
+  for (int i = 0; i < NB; ++i) kgrp[i] = K_AFF ? (32 * i) / c.k.group : i;
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 
   float m_run = neg_inf();
@@ -170,23 +173,25 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_
                        blk + tau<VROW>(2 * t + 9)};
 
     // ---------------------------------------------------------- S = Q K^T
-    float acc[NACC][2][4];
-#pragma unroll
-    for (int i = 0; i < NACC; ++i)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) acc[i][nt][0] = acc[i][nt][1] = acc[i][nt][2] = acc[i][nt][3] = 0.0f;
+    // sc[2 nt + e]: head g, logical token 8 nt + 2t + e (tile row rr[2 nt + e]).
+    float sc[4];
     const uint8_t* kpl = st + TL.kc;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
+      float acc[NACC][4];
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
       const int r = blk + tau<VROW>(nt * 8 + g);
       if constexpr (KB == 4) {
 #pragma unroll
         for (int p = 0; p < NB; ++p) {
           __half2 h[4];
           nibbles_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
-          float(&dst)[4] = acc[KG ? p : 0][nt];
-          mma_f16(dst, qa[2 * p], h2u(h[0]), h2u(h[2]));
-          mma_f16(dst, qa[2 * p + 1], h2u(h[1]), h2u(h[3]));
+          const uint4 q0 = sm_qa[2 * p][lane], q1 = sm_qa[2 * p + 1][lane];
+          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
+          float(&dst)[4] = acc[KG ? p : 0];
+          mma_f16(dst, a0, h2u(h[0]), h2u(h[2]));
+          mma_f16(dst, a1, h2u(h[1]), h2u(h[3]));
         }
       } else if constexpr (KB == 8) {
 #pragma unroll
@@ -194,56 +199,58 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_
           __half2 lo, hi;
           bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * ks + 4 * t)) ^ 0x80808080u, lo,
                       hi);
-          mma_f16(acc[KG ? (ks >> 1) : 0][nt], qa[ks], h2u(lo), h2u(hi));
+          const uint4 q0 = sm_qa[ks][lane];
+          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
+          mma_f16(acc[KG ? (ks >> 1) : 0], a0, h2u(lo), h2u(hi));
         }
       } else {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           const uint2 v = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(r, 32 * ks + 8 * t));
-          mma_f16(acc[0][nt], qa[ks], v.x, v.y);
+          const uint4 q0 = sm_qa[ks][lane];
+          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
+          mma_f16(acc[0], a0, v.x, v.y);
         }
       }
-    }
-    float sc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int nt = i >> 1, e = i & 1;
-      if constexpr (K_Q40) {
-        // the token's NB block scales in one load: d (sum q u - 8 sum q) per block
-        const uint8_t* srow = st + TL.ks + rr[i] * (2 * NB);
-        float d[NB];
-        if constexpr (NB == 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(srow);
-          const float2 f0 = __half22float2(u2h(u.x)), f1 = __half22float2(u2h(u.y));
-          d[0] = f0.x; d[1] = f0.y; d[2] = f1.x; d[3] = f1.y;
+      for (int e = 0; e < 2; ++e) {
+        const int i = 2 * nt + e;
+        float v;
+        if constexpr (K_Q40) {
+          // the token's NB block scales in one load: d (sum q u - 8 sum q) per block
+          const uint8_t* srow = st + TL.ks + rr[i] * (2 * NB);
+          float d[NB];
+          if constexpr (NB == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(srow);
+            const float2 f0 = __half22float2(u2h(u.x)), f1 = __half22float2(u2h(u.y));
+            d[0] = f0.x; d[1] = f0.y; d[2] = f1.x; d[3] = f1.y;
+          } else {
+            const float2 f0 = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(srow)));
+            d[0] = f0.x; d[1] = f0.y;
+          }
+          float wq = 0.0f;
+          v = 0.0f;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            v = fmaf(d[nb], acc[nb][e], v);
+            v = fmaf(d[nb], acc[nb][2 + e], v);
+            wq = fmaf(d[nb], sm_qblk[nb][g], wq);
+          }
+          v = fmaf(-8.0f, wq, v);
+        } else if constexpr (KG) {
+          const __half* srow = reinterpret_cast<const __half*>(st + TL.ks) + rr[i] * kng;
+          const __half* zrow = reinterpret_cast<const __half*>(st + TL.kz) + rr[i] * kng;
+          v = 0.0f;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const float x = acc[nb][e] + acc[nb][2 + e];
+            v = fmaf(__half2float(srow[kgrp[nb]]), x, fmaf(__half2float(zrow[kgrp[nb]]), sm_qblk[nb][g], v));
+          }
         } else {
-          const float2 f0 = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(srow)));
-          d[0] = f0.x; d[1] = f0.y;
+          v = acc[0][e] + acc[0][2 + e];
         }
-        float v = 0.0f, wq = 0.0f;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          v = fmaf(d[nb], acc[nb][nt][e], v);
-          v = fmaf(d[nb], acc[nb][nt][2 + e], v);
-          wq = fmaf(d[nb], qblk[nb], wq);
-        }
-        sc[i] = fmaf(-8.0f, wq, v) * a.qscale;
-      } else if constexpr (KG) {
-        const __half* srow = reinterpret_cast<const __half*>(st + TL.ks) + rr[i] * kng;
-        const __half* zrow = reinterpret_cast<const __half*>(st + TL.kz) + rr[i] * kng;
-        float v = 0.0f;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const float x = acc[nb][nt][e] + acc[nb][nt][2 + e];
-          const float sb = __half2float(srow[kgrp[nb]]);
-          if constexpr (K_AFF) v = fmaf(sb, x, fmaf(__half2float(zrow[kgrp[nb]]), qblk[nb], v));
-          else v = fmaf(sb, fmaf(-8.0f, qblk[nb], x), v);   // d (sum q u - 8 sum q)
-        }
-        sc[i] = v * a.qscale;
-      } else {
-        sc[i] = (acc[0][nt][e] + acc[0][nt][2 + e]) * a.qscale;
+        sc[i] = (tok0 - blk + rr[i] < t1) ? v * a.qscale : neg_inf();
       }
-      if (tok0 - blk + rr[i] >= t1) sc[i] = neg_inf();
     }
 
     // ------------------------------------------------- online softmax (log2)
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_tc_kernel(const __grid_
 
 template <int D, int G, int KF, int VF>
 cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  constexpr int NSTAGE = Stages<KF>::v;
+  constexpr int NSTAGE = TcStages<D, KF, VF>::v;
   const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   const int smem = NSTAGE * L.bytes + 1024;   // + alignment slack
   if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
