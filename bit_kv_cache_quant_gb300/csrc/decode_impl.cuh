@@ -150,6 +150,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   constexpr int PROW = D + kPartialPad;
   constexpr int AROW = D + ACCPAD;
   __shared__ float sm_w[kMaxSplits][G];
+  __shared__ float sm_lsum[kMaxSplits][G];
   __shared__ float sm_inv[G];
   __shared__ int s_last;
   const size_t bh = (size_t)b * c.Hkv + kvh;
@@ -191,34 +192,52 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   if (!s_last) return;
   __threadfence();
   const float* P0 = a.partials + bh * a.nsplit * G * PROW;
-  // every split's (max, sum) at once, then one weight per (split, head)
-  for (int i = threadIdx.x; i < a.nsplit * G; i += kDecodeThreads) sm_w[i / G][i % G] = __ldcg(P0 + i * PROW + D);
+  // Every split's (max, sum) at once; then one warp per head reduces them with
+  // shuffles and leaves one weight per (split, head).
+  for (int i = threadIdx.x; i < a.nsplit * G; i += kDecodeThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(P0 + i * PROW + D));
+    sm_w[i / G][i % G] = ml.x;
+    sm_lsum[i / G][i % G] = ml.y;
+  }
   __syncthreads();
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
-    float M = neg_inf();
-    for (int sp = 0; sp < a.nsplit; ++sp) M = fmaxf(M, sm_w[sp][h]);
-    float L = 0.0f;
-    for (int sp = 0; sp < a.nsplit; ++sp) {
-      const float ms = sm_w[sp][h];
-      const float e = (ms == neg_inf()) ? 0.0f : exp2f(ms - M);
-      L = fmaf(__ldcg(P0 + (sp * G + h) * PROW + D + 1), e, L);
-      sm_w[sp][h] = e;
+  {
+    const int lane = threadIdx.x & 31;
+    for (int h = threadIdx.x >> 5; h < G; h += kDecodeWarps) {
+      float M = neg_inf();
+      for (int sp = lane; sp < a.nsplit; sp += 32) M = fmaxf(M, sm_w[sp][h]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float L = 0.0f;
+      for (int sp = lane; sp < a.nsplit; sp += 32) {
+        const float ms = sm_w[sp][h];
+        const float e = (ms == neg_inf()) ? 0.0f : exp2f(ms - M);
+        L = fmaf(sm_lsum[sp][h], e, L);
+        sm_w[sp][h] = e;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane == 0) sm_inv[h] = L > 0.0f ? 1.0f / L : 0.0f;
     }
-    sm_inv[h] = L > 0.0f ? 1.0f / L : 0.0f;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * D / 4; idx += kDecodeThreads) {
     const int h = idx / (D / 4), d4 = idx % (D / 4);
+    const float4* src = reinterpret_cast<const float4*>(P0 + h * PROW) + d4;
+    constexpr int kStrideF4 = G * PROW / 4;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int sp = 0; sp < a.nsplit; ++sp) {
-      const float4 p = __ldcg(reinterpret_cast<const float4*>(P0 + (sp * G + h) * PROW) + d4);
-      const float e = sm_w[sp][h];
-      A.x = fmaf(p.x, e, A.x);
-      A.y = fmaf(p.y, e, A.y);
-      A.z = fmaf(p.z, e, A.z);
-      A.w = fmaf(p.w, e, A.w);
+    for (int sp0 = 0; sp0 < a.nsplit; sp0 += 8) {
+      float4 p[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        p[j] = (sp0 + j < a.nsplit) ? __ldcg(src + (size_t)(sp0 + j) * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = (sp0 + j < a.nsplit) ? sm_w[sp0 + j][h] : 0.0f;
+        A.x = fmaf(p[j].x, e, A.x);
+        A.y = fmaf(p[j].y, e, A.y);
+        A.z = fmaf(p[j].z, e, A.z);
+        A.w = fmaf(p[j].w, e, A.w);
+      }
     }
     const float inv = sm_inv[h];
     const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + 4 * d4;

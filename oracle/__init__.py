@@ -24,8 +24,9 @@ Precision: quantiser decisions (scales, zeros, codes) are taken in IEEE
 fp32 with round-to-nearest-even, exactly as the kernels take them; stored
 metadata is rounded to fp16; attention and SnapKV scores are float64.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` against closed
-forms, brute force, special cases that reduce to library routines and the
+Every function is pinned by ``tests/test_oracle_quantize.py``,
+``tests/test_oracle_cache.py`` and ``tests/test_oracle_attention_snapkv.py``
+against closed forms, brute force, special cases that reduce to library routines and the
 pages' printed numbers (``tests/golden/``).  No function here is "parity
 unpinned".
 """
