@@ -144,27 +144,28 @@ __host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
 // to finish merges every partial with the online-softmax rule.
 // Accumulator layout: ACCPAD == 0: acc[warp][h][d]; ACCPAD > 0 (tensor-core
 // kernel): rows of D + ACCPAD floats, channel d at (d % (D/8)) * 8 + d / (D/8).
-template <int D, int G, int ACCPAD>
+template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps>
 __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split,
                                             float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc) {
   constexpr int PROW = D + kPartialPad;
   constexpr int AROW = D + ACCPAD;
+  constexpr int NTHR = 32 * NWARP;
   __shared__ float sm_w[kMaxSplits][G];
   __shared__ float sm_lsum[kMaxSplits][G];
   __shared__ float sm_inv[G];
   __shared__ int s_last;
   const size_t bh = (size_t)b * c.Hkv + kvh;
   // Merge the warps; write the output (one split) or this split's partial.
-  for (int idx = threadIdx.x; idx < G * D; idx += kDecodeThreads) {
+  for (int idx = threadIdx.x; idx < G * D; idx += NTHR) {
     const int h = idx / D, d = idx % D;
     const int pos = h * AROW + (ACCPAD ? (d % (D / 8)) * 8 + d / (D / 8) : d);
     float M = sm_m[0][h];
 #pragma unroll
-    for (int w = 1; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w][h]);
+    for (int w = 1; w < NWARP; ++w) M = fmaxf(M, sm_m[w][h]);
     float A = 0.0f, L = 0.0f;
     if (M != neg_inf()) {
 #pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
+      for (int w = 0; w < NWARP; ++w) {
         const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
         A = fmaf(sm_acc[w * G * AROW + pos], e, A);
         L = fmaf(sm_l[w][h], e, L);
@@ -184,17 +185,22 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   }
   if (a.nsplit == 1) return;
 
-  // The last split of this (b, kv head) to finish merges all partials.
-  __threadfence();
+  // The last split of this (b, kv head) to finish merges all partials.  The
+  // barrier orders every thread's partial stores before thread 0's device-scope
+  // fence, which orders them before its arrival.
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(a.nsplit - 1));
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const bool last = atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(a.nsplit - 1);
+    if (last) __threadfence();   // the other splits' partials are visible to the whole CTA after the barrier
+    s_last = last;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const float* P0 = a.partials + bh * a.nsplit * G * PROW;
   // Every split's (max, sum) at once; then one warp per head reduces them with
   // shuffles and leaves one weight per (split, head).
-  for (int i = threadIdx.x; i < a.nsplit * G; i += kDecodeThreads) {
+  for (int i = threadIdx.x; i < a.nsplit * G; i += NTHR) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(P0 + i * PROW + D));
     sm_w[i / G][i % G] = ml.x;
     sm_lsum[i / G][i % G] = ml.y;
@@ -202,7 +208,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   __syncthreads();
   {
     const int lane = threadIdx.x & 31;
-    for (int h = threadIdx.x >> 5; h < G; h += kDecodeWarps) {
+    for (int h = threadIdx.x >> 5; h < G; h += NWARP) {
       float M = neg_inf();
       for (int sp = lane; sp < a.nsplit; sp += 32) M = fmaxf(M, sm_w[sp][h]);
 #pragma unroll
@@ -220,7 +226,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D / 4; idx += kDecodeThreads) {
+  for (int idx = threadIdx.x; idx < G * D / 4; idx += NTHR) {
     const int h = idx / (D / 4), d4 = idx % (D / 4);
     const float4* src = reinterpret_cast<const float4*>(P0 + h * PROW) + d4;
     constexpr int kStrideF4 = G * PROW / 4;

@@ -1,9 +1,13 @@
 // Decode attention on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32
 // accumulators) for head_dim 64 / 128 and bf16 / fp16 queries and outputs.
 //
-// Same split-KV structure, 64-token cp.async tiles and online-softmax merge as
-// decode_kernel; the difference is where the two contractions run.  Per warp
-// and 16-token block:
+// Same split-KV partition and online-softmax merge as decode_kernel.  A CTA of
+// eight warps streams its split in 64-token tiles that TMA copies into a ring
+// of NSTAGE shared-memory stages; warps 0-3 take the even tiles and warps 4-7
+// the odd ones, each warp 16 tokens of a tile.  There is no CTA-wide barrier
+// in the loop: every warp waits on the stage's mbarrier itself, and the last of
+// the four warps to finish a stage copies the tile NSTAGE ahead into it.
+// Per warp and 16-token block:
 //   S[16 x 16] = Q[16 x D] . K^T : rows 0..7 of the A operand hold fp16(q) of
 //     the (up to 8) query heads of the kv head, rows 8..15 the residual
 //     q - fp16(q), so the score of head h is row h + row h + 8 and q enters
@@ -40,9 +44,35 @@ __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* 
   }
 }
 
-template <int D, int G, int KF, int VF>
-__global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
-  constexpr int NSTAGE = TcStages<D, KF, VF>::v;
+// A CTA has NGRP groups of four warps; group gp consumes tiles gp, gp + NGRP, ...
+// Four-warp CTAs (four per SM) suit grids of several waves; eight-warp CTAs
+// (two per SM) halve the time per split when the whole grid fits in one wave.
+template <int NGRP> struct TcShape {
+  static constexpr int warps = 4 * NGRP;
+  static constexpr int threads = 32 * warps;
+  static constexpr int ctas_per_sm = 4 / NGRP;
+};
+
+// Pipeline depth: as many 64-token stages (a multiple of NGRP, 2 to 8) as fit
+// next to one CTA's static shared memory at TcShape::ctas_per_sm CTAs per SM.
+template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
+  static constexpr int stage = ((64 * D * FmtBits<KF>::v / 8 + 64 * D * FmtBits<VF>::v / 8 +
+                                 ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * (D / 32) * 2 +
+                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * (D / 16) * 2) +
+                                1023) / 1024 * 1024;
+  static constexpr int warps = TcShape<NGRP>::warps;
+  static constexpr int static_smem = warps * G * (D + 8) * 4 + 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 +
+                                     (D / 16) * 512 + 1024;
+  static constexpr int budget = 227 * 1024 / TcShape<NGRP>::ctas_per_sm - 2048 - static_smem;
+  static constexpr int raw = (budget / stage) / NGRP * NGRP;
+  static constexpr int v = raw < 2 ? 2 : (raw > 8 ? 8 : raw);
+};
+
+template <int D, int G, int KF, int VF, int NGRP>
+__global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_per_sm)
+    decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
+  constexpr int NSTAGE = TcStages<D, G, KF, VF, NGRP>::v;
+  constexpr int NWARP = TcShape<NGRP>::warps;
   constexpr int KB = FmtBits<KF>::v;
   constexpr int VB = FmtBits<VF>::v;
   constexpr int KROW = D * KB / 8;
@@ -59,14 +89,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __gr
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   constexpr int NACC = KG ? NB : 1;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per kv head");
+  static_assert(NSTAGE % NGRP == 0, "each stage serves one warp group");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ float sm_m[kDecodeWarps][G];
-  __shared__ float sm_l[kDecodeWarps][G];
-  __shared__ __align__(16) float sm_acc[kDecodeWarps][G][D + 8];   // channel d at (d % VCH) * 8 + d / VCH
+  __shared__ float sm_m[NWARP][G];
+  __shared__ float sm_l[NWARP][G];
+  __shared__ __align__(16) float sm_acc[NWARP][G][D + 8];   // channel d at (d % VCH) * 8 + d / VCH
   __shared__ __align__(8) uint64_t mbar[NSTAGE];
+  __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (4 per tile)
+  __shared__ int s_last_tile[NSTAGE];     // last tile copied into a stage, -1 if none
   __shared__ int s_T;
   __shared__ volatile int s_fail;
+  // Query fragments in key-channel order (lane-major, one 16-byte vector per
+  // k-step) and per-block sums of q for grouped keys.
+  __shared__ __align__(16) uint4 sm_qa[KS][32];
+  __shared__ float sm_qblk[NB][8];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int lane = threadIdx.x & 31;
@@ -79,34 +116,35 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __gr
   const int vng = c.v.n_groups;
   const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
 
+  // Thread 0 reads the stored length, sets up the barriers and starts the
+  // first NSTAGE tile copies; warp 1 meanwhile builds the query fragments.
   if (threadIdx.x == 0) {
-    s_T = c.state->stored;
-    s_fail = 0;
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
+    const int T = c.state->stored;
 #pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&mbar[s], 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&mbar[s], 1);
+      s_done[s] = 0u;
+      s_last_tile[s] = -1;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_async_smem();   // the initialised barriers are visible to the copy engine
-  }
-  __syncthreads();
-  const int T = s_T;
-  int per = (T + a.nsplit - 1) / a.nsplit;
-  per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
-  const int t0 = min(T, split * per);
-  const int t1 = min(T, t0 + per);
-  const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
-
-  if (threadIdx.x == 0) {
+    int per = (T + a.nsplit - 1) / a.nsplit;
+    per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
+    const int t0 = min(T, split * per);
+    const int ntiles = (min(T, t0 + per) - t0 + kTileTokens - 1) / kTileTokens;
 #pragma unroll
-    for (int s = 0; s < NSTAGE - 1; ++s)
-      if (s < ntiles) issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
+    for (int s = 0; s < NSTAGE; ++s) {
+      if (s < ntiles) {
+        issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
+        s_last_tile[s] = s;
+      }
+    }
+    s_T = T;
+    s_fail = 0;
   }
-
-  // Query fragments in key-channel order, built once by warp 0 into shared
-  // memory (lane-major, one 16-byte vector per k-step) and read back per use;
-  // per-block sums of q for grouped keys.
-  __shared__ __align__(16) uint4 sm_qa[KS][32];
-  __shared__ float sm_qblk[NB][8];
-  if (warp == 0) {
+  if (warp == 1) {
     float qb[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i) qb[i] = 0.0f;
@@ -140,6 +178,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __gr
       }
     }
   }
+  __syncthreads();
+  const int T = s_T;
+  int per = (T + a.nsplit - 1) / a.nsplit;
+  per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
+  const int t0 = min(T, split * per);
+  const int t1 = min(T, t0 + per);
+  const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
+
   int kgrp[NB];
 #pragma unroll
   for (int i = 0; i < NB; ++i) kgrp[i] = K_AFF ? (32 * i) / c.k.group : i;
@@ -151,227 +197,241 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __gr
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.0f;
 
-  int it = 0;
-  for (; it < ntiles; ++it) {
-    if (!mbar_wait_bounded(&mbar[it % NSTAGE], (it / NSTAGE) & 1)) s_fail = 1;
-    __syncthreads();   // every warp is also done with the stage refilled below
-    if (s_fail) break;
-    if (threadIdx.x == 0) {
-      const int nx = it + NSTAGE - 1;
-      if (nx < ntiles) {
-        fence_async_smem();
-        issue_tile_tma<D, KF, VF>(smem + (nx % NSTAGE) * TL.bytes, TL, c, bh, t0 + nx * kTileTokens,
-                                  &mbar[nx % NSTAGE]);
-      }
-    }
-    const uint8_t* st = smem + (it % NSTAGE) * TL.bytes;
-    const int blk = warp * 16;                          // this warp's 16 rows of the tile
-    const int tok0 = t0 + it * kTileTokens + blk;
-    if (tok0 >= t1) continue;                           // warp-uniform
-    // rows of the four tokens this thread's scores / value pairs belong to
-    const int rr[4] = {blk + tau<VROW>(2 * t), blk + tau<VROW>(2 * t + 1), blk + tau<VROW>(2 * t + 8),
-                       blk + tau<VROW>(2 * t + 9)};
+  const int grp = warp >> 2;
+  const int blk = (warp & 3) * 16;                      // this warp's 16 rows of each tile
+  // rows of the four tokens this thread's scores / value pairs belong to
+  const int rr[4] = {blk + tau<VROW>(2 * t), blk + tau<VROW>(2 * t + 1), blk + tau<VROW>(2 * t + 8),
+                     blk + tau<VROW>(2 * t + 9)};
 
-    // ---------------------------------------------------------- S = Q K^T
-    // sc[2 nt + e]: head g, logical token 8 nt + 2t + e (tile row rr[2 nt + e]).
-    float sc[4];
-    const uint8_t* kpl = st + TL.kc;
+  for (int it = grp; it < ntiles; it += NGRP) {
+    if (__any_sync(0xffffffffu, s_fail)) break;
+    const int stg = it % NSTAGE;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar[stg], (it / NSTAGE) & 1))) {
+      s_fail = 1;
+      break;
+    }
+    const uint8_t* st = smem + stg * TL.bytes;
+    const int tok0 = t0 + it * kTileTokens + blk;
+    if (tok0 < t1) {   // warp-uniform
+      // ---------------------------------------------------------- S = Q K^T
+      // sc[2 nt + e]: head g, logical token 8 nt + 2t + e (tile row rr[2 nt + e]).
+      float sc[4];
+      const uint8_t* kpl = st + TL.kc;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float acc[NACC][4];
+      for (int nt = 0; nt < 2; ++nt) {
+        float acc[NACC][4];
 #pragma unroll
-      for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-      const int r = blk + tau<VROW>(nt * 8 + g);
-      if constexpr (KB == 4) {
+        for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+        const int r = blk + tau<VROW>(nt * 8 + g);
+        if constexpr (KB == 4) {
 #pragma unroll
-        for (int p = 0; p < NB; ++p) {
-          __half2 h[4];
-          nibbles_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
-          const uint4 q0 = sm_qa[2 * p][lane], q1 = sm_qa[2 * p + 1][lane];
-          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
-          float(&dst)[4] = acc[KG ? p : 0];
-          mma_f16(dst, a0, h2u(h[0]), h2u(h[2]));
-          mma_f16(dst, a1, h2u(h[1]), h2u(h[3]));
+          for (int p = 0; p < NB; ++p) {
+            __half2 h[4];
+            nibbles_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
+            const uint4 q0 = sm_qa[2 * p][lane], q1 = sm_qa[2 * p + 1][lane];
+            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
+            float(&dst)[4] = acc[KG ? p : 0];
+            mma_f16(dst, a0, h2u(h[0]), h2u(h[2]));
+            mma_f16(dst, a1, h2u(h[1]), h2u(h[3]));
+          }
+        } else if constexpr (KB == 8) {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            __half2 lo, hi;
+            bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * ks + 4 * t)) ^ 0x80808080u, lo,
+                        hi);
+            const uint4 q0 = sm_qa[ks][lane];
+            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
+            mma_f16(acc[KG ? (ks >> 1) : 0], a0, h2u(lo), h2u(hi));
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const uint2 v = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(r, 32 * ks + 8 * t));
+            const uint4 q0 = sm_qa[ks][lane];
+            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
+            mma_f16(acc[0], a0, v.x, v.y);
+          }
         }
-      } else if constexpr (KB == 8) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          __half2 lo, hi;
-          bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * ks + 4 * t)) ^ 0x80808080u, lo,
-                      hi);
-          const uint4 q0 = sm_qa[ks][lane];
-          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
-          mma_f16(acc[KG ? (ks >> 1) : 0], a0, h2u(lo), h2u(hi));
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * nt + e;
+          float v;
+          if constexpr (K_Q40) {
+            // the token's NB block scales in one load: d (sum q u - 8 sum q) per block
+            const uint8_t* srow = st + TL.ks + rr[i] * (2 * NB);
+            float d[NB];
+            if constexpr (NB == 4) {
+              const uint2 u = *reinterpret_cast<const uint2*>(srow);
+              const float2 f0 = __half22float2(u2h(u.x)), f1 = __half22float2(u2h(u.y));
+              d[0] = f0.x; d[1] = f0.y; d[2] = f1.x; d[3] = f1.y;
+            } else {
+              const float2 f0 = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(srow)));
+              d[0] = f0.x; d[1] = f0.y;
+            }
+            float wq = 0.0f;
+            v = 0.0f;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              v = fmaf(d[nb], acc[nb][e], v);
+              v = fmaf(d[nb], acc[nb][2 + e], v);
+              wq = fmaf(d[nb], sm_qblk[nb][g], wq);
+            }
+            v = fmaf(-8.0f, wq, v);
+          } else if constexpr (KG) {
+            const __half* srow = reinterpret_cast<const __half*>(st + TL.ks) + rr[i] * kng;
+            const __half* zrow = reinterpret_cast<const __half*>(st + TL.kz) + rr[i] * kng;
+            v = 0.0f;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const float x = acc[nb][e] + acc[nb][2 + e];
+              v = fmaf(__half2float(srow[kgrp[nb]]), x, fmaf(__half2float(zrow[kgrp[nb]]), sm_qblk[nb][g], v));
+            }
+          } else {
+            v = acc[0][e] + acc[0][2 + e];
+          }
+          sc[i] = (tok0 - blk + rr[i] < t1) ? v * a.qscale : neg_inf();
+        }
+      }
+
+      // ------------------------------------------------- online softmax (log2)
+      float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const float mn = fmaxf(m_run, mb);                 // finite: row tok0 is valid
+      if (mn > m_run) {
+        const float alpha = exp2f(m_run - mn);
+        l_part *= alpha;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          oacc[nt][0] *= alpha; oacc[nt][1] *= alpha; oacc[nt][2] *= alpha; oacc[nt][3] *= alpha;
+        }
+        m_run = mn;
+      }
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        p[i] = exp2f(sc[i] - mn);
+        l_part += p[i];
+      }
+      uint32_t pa[4];
+      {
+        const __half2 ph0 = __floats2half2_rn(p[0], p[1]);
+        const __half2 ph1 = __floats2half2_rn(p[2], p[3]);
+        const float2 pf0 = __half22float2(ph0);
+        const float2 pf1 = __half22float2(ph1);
+        pa[0] = h2u(ph0);
+        pa[1] = h2u(__floats2half2_rn(p[0] - pf0.x, p[1] - pf0.y));
+        pa[2] = h2u(ph1);
+        pa[3] = h2u(__floats2half2_rn(p[2] - pf1.x, p[3] - pf1.y));
+      }
+
+      // ------------------------------------------------------------ O += P V
+      // Rows past the split's end were copied as whatever the buffer holds: their
+      // weight is 0, and their value scale / zero (or fp16 values) are zeroed so
+      // that no NaN reaches the MMA.
+      bool vok[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
+      __half2 sAB, zAB, sCD, zCD;
+      if constexpr (V_AFF) {
+        const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
+        const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
+        const __half h0 = __ushort_as_half(0);
+        sAB = __halves2half2(vok[0] ? vs[rr[0] * vng + vgi] : h0, vok[1] ? vs[rr[1] * vng + vgi] : h0);
+        zAB = __halves2half2(vok[0] ? vz[rr[0] * vng + vgi] : h0, vok[1] ? vz[rr[1] * vng + vgi] : h0);
+        sCD = __halves2half2(vok[2] ? vs[rr[2] * vng + vgi] : h0, vok[3] ? vs[rr[3] * vng + vgi] : h0);
+        zCD = __halves2half2(vok[2] ? vz[rr[2] * vng + vgi] : h0, vok[3] ? vz[rr[3] * vng + vgi] : h0);
+      }
+      constexpr int NW = VTB / 4;
+      uint32_t A[NW], B[NW], C[NW], E[NW];
+      const uint8_t* vpl = st + TL.vc;
+      lds_row_words<VROW, NW>(A, vpl, rr[0], g * VTB);
+      lds_row_words<VROW, NW>(B, vpl, rr[1], g * VTB);
+      lds_row_words<VROW, NW>(C, vpl, rr[2], g * VTB);
+      lds_row_words<VROW, NW>(E, vpl, rr[3], g * VTB);
+      if constexpr (VB == 16) {
+        if (tok0 + 16 > t1) {   // warp-uniform: only the split's last block
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            A[w] = vok[0] ? A[w] : 0u;
+            B[w] = vok[1] ? B[w] : 0u;
+            C[w] = vok[2] ? C[w] : 0u;
+            E[w] = vok[3] ? E[w] : 0u;
+          }
+        }
+      }
+      if constexpr (VB == 4) {
+#pragma unroll
+        for (int wi = 0; wi < NW; ++wi) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t sel = half ? 0x7632u : 0x5410u;
+            __half2 h0[4], h1[4];
+            nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // channels 8 wi + 4 half + 0..3 of tokens A, B
+            nibbles_to_h2(__byte_perm(C[wi], E[wi], sel), h1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (V_AFF) {
+                h0[i] = __hfma2(h0[i], sAB, zAB);
+                h1[i] = __hfma2(h1[i], sCD, zCD);
+              }
+              mma_f16(oacc[8 * wi + 4 * half + i], pa, h2u(h0[i]), h2u(h1[i]));
+            }
+          }
+        }
+      } else if constexpr (VB == 8) {
+#pragma unroll
+        for (int wi = 0; wi < NW; ++wi) {
+          const uint32_t a_ = A[wi] ^ 0x80808080u, b_ = B[wi] ^ 0x80808080u;
+          const uint32_t c_ = C[wi] ^ 0x80808080u, e_ = E[wi] ^ 0x80808080u;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t sel = half ? 0x7362u : 0x5140u;
+            __half2 l0, h0, l1, h1;
+            bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
+            bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
+            if constexpr (V_AFF) {
+              l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
+              l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
+            }
+            mma_f16(oacc[4 * wi + 2 * half], pa, h2u(l0), h2u(l1));
+            mma_f16(oacc[4 * wi + 2 * half + 1], pa, h2u(h0), h2u(h1));
+          }
         }
       } else {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint2 v = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(r, 32 * ks + 8 * t));
-          const uint4 q0 = sm_qa[ks][lane];
-          const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
-          mma_f16(acc[0], a0, v.x, v.y);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = 2 * nt + e;
-        float v;
-        if constexpr (K_Q40) {
-          // the token's NB block scales in one load: d (sum q u - 8 sum q) per block
-          const uint8_t* srow = st + TL.ks + rr[i] * (2 * NB);
-          float d[NB];
-          if constexpr (NB == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(srow);
-            const float2 f0 = __half22float2(u2h(u.x)), f1 = __half22float2(u2h(u.y));
-            d[0] = f0.x; d[1] = f0.y; d[2] = f1.x; d[3] = f1.y;
-          } else {
-            const float2 f0 = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(srow)));
-            d[0] = f0.x; d[1] = f0.y;
-          }
-          float wq = 0.0f;
-          v = 0.0f;
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            v = fmaf(d[nb], acc[nb][e], v);
-            v = fmaf(d[nb], acc[nb][2 + e], v);
-            wq = fmaf(d[nb], sm_qblk[nb][g], wq);
-          }
-          v = fmaf(-8.0f, wq, v);
-        } else if constexpr (KG) {
-          const __half* srow = reinterpret_cast<const __half*>(st + TL.ks) + rr[i] * kng;
-          const __half* zrow = reinterpret_cast<const __half*>(st + TL.kz) + rr[i] * kng;
-          v = 0.0f;
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const float x = acc[nb][e] + acc[nb][2 + e];
-            v = fmaf(__half2float(srow[kgrp[nb]]), x, fmaf(__half2float(zrow[kgrp[nb]]), sm_qblk[nb][g], v));
-          }
-        } else {
-          v = acc[0][e] + acc[0][2 + e];
-        }
-        sc[i] = (tok0 - blk + rr[i] < t1) ? v * a.qscale : neg_inf();
-      }
-    }
-
-    // ------------------------------------------------- online softmax (log2)
-    float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-    const float mn = fmaxf(m_run, mb);                 // finite: row tok0 is valid
-    if (mn > m_run) {
-      const float alpha = exp2f(m_run - mn);
-      l_part *= alpha;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        oacc[nt][0] *= alpha; oacc[nt][1] *= alpha; oacc[nt][2] *= alpha; oacc[nt][3] *= alpha;
-      }
-      m_run = mn;
-    }
-    float p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      p[i] = exp2f(sc[i] - mn);
-      l_part += p[i];
-    }
-    uint32_t pa[4];
-    {
-      const __half2 ph0 = __floats2half2_rn(p[0], p[1]);
-      const __half2 ph1 = __floats2half2_rn(p[2], p[3]);
-      const float2 pf0 = __half22float2(ph0);
-      const float2 pf1 = __half22float2(ph1);
-      pa[0] = h2u(ph0);
-      pa[1] = h2u(__floats2half2_rn(p[0] - pf0.x, p[1] - pf0.y));
-      pa[2] = h2u(ph1);
-      pa[3] = h2u(__floats2half2_rn(p[2] - pf1.x, p[3] - pf1.y));
-    }
-
-    // ------------------------------------------------------------ O += P V
-    // Rows past the split's end were copied as whatever the buffer holds: their
-    // weight is 0, and their value scale / zero (or fp16 values) are zeroed so
-    // that no NaN reaches the MMA.
-    bool vok[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
-    __half2 sAB, zAB, sCD, zCD;
-    if constexpr (V_AFF) {
-      const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
-      const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
-      const __half h0 = __ushort_as_half(0);
-      sAB = __halves2half2(vok[0] ? vs[rr[0] * vng + vgi] : h0, vok[1] ? vs[rr[1] * vng + vgi] : h0);
-      zAB = __halves2half2(vok[0] ? vz[rr[0] * vng + vgi] : h0, vok[1] ? vz[rr[1] * vng + vgi] : h0);
-      sCD = __halves2half2(vok[2] ? vs[rr[2] * vng + vgi] : h0, vok[3] ? vs[rr[3] * vng + vgi] : h0);
-      zCD = __halves2half2(vok[2] ? vz[rr[2] * vng + vgi] : h0, vok[3] ? vz[rr[3] * vng + vgi] : h0);
-    }
-    constexpr int NW = VTB / 4;
-    uint32_t A[NW], B[NW], C[NW], E[NW];
-    const uint8_t* vpl = st + TL.vc;
-    lds_row_words<VROW, NW>(A, vpl, rr[0], g * VTB);
-    lds_row_words<VROW, NW>(B, vpl, rr[1], g * VTB);
-    lds_row_words<VROW, NW>(C, vpl, rr[2], g * VTB);
-    lds_row_words<VROW, NW>(E, vpl, rr[3], g * VTB);
-    if constexpr (VB == 16) {
-      if (tok0 + 16 > t1) {   // warp-uniform: only the split's last block
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          A[w] = vok[0] ? A[w] : 0u;
-          B[w] = vok[1] ? B[w] : 0u;
-          C[w] = vok[2] ? C[w] : 0u;
-          E[w] = vok[3] ? E[w] : 0u;
+        for (int wi = 0; wi < NW; ++wi) {
+          mma_f16(oacc[2 * wi], pa, __byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x5410u));
+          mma_f16(oacc[2 * wi + 1], pa, __byte_perm(A[wi], B[wi], 0x7632u), __byte_perm(C[wi], E[wi], 0x7632u));
         }
       }
     }
-    if constexpr (VB == 4) {
-#pragma unroll
-      for (int wi = 0; wi < NW; ++wi) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t sel = half ? 0x7632u : 0x5410u;
-          __half2 h0[4], h1[4];
-          nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // channels 8 wi + 4 half + 0..3 of tokens A, B
-          nibbles_to_h2(__byte_perm(C[wi], E[wi], sel), h1);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (V_AFF) {
-              h0[i] = __hfma2(h0[i], sAB, zAB);
-              h1[i] = __hfma2(h1[i], sCD, zCD);
-            }
-            mma_f16(oacc[8 * wi + 4 * half + i], pa, h2u(h0[i]), h2u(h1[i]));
-          }
+    // Release the stage.  The group's last warp to finish it copies the tile
+    // NSTAGE ahead into it (the fences order the four warps' reads of the
+    // stage before the copy engine's writes).
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if ((atomicAdd(&s_done[stg], 1u) & 3u) == 3u) {
+        __threadfence_block();
+        const int nx = it + NSTAGE;
+        if (nx < ntiles) {
+          fence_async_smem();
+          issue_tile_tma<D, KF, VF>(smem + stg * TL.bytes, TL, c, bh, t0 + nx * kTileTokens, &mbar[stg]);
+          s_last_tile[stg] = nx;
         }
-      }
-    } else if constexpr (VB == 8) {
-#pragma unroll
-      for (int wi = 0; wi < NW; ++wi) {
-        const uint32_t a_ = A[wi] ^ 0x80808080u, b_ = B[wi] ^ 0x80808080u;
-        const uint32_t c_ = C[wi] ^ 0x80808080u, e_ = E[wi] ^ 0x80808080u;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t sel = half ? 0x7362u : 0x5140u;
-          __half2 l0, h0, l1, h1;
-          bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
-          bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
-          if constexpr (V_AFF) {
-            l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
-            l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
-          }
-          mma_f16(oacc[4 * wi + 2 * half], pa, h2u(l0), h2u(l1));
-          mma_f16(oacc[4 * wi + 2 * half + 1], pa, h2u(h0), h2u(h1));
-        }
-      }
-    } else {
-#pragma unroll
-      for (int wi = 0; wi < NW; ++wi) {
-        mma_f16(oacc[2 * wi], pa, __byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x5410u));
-        mma_f16(oacc[2 * wi + 1], pa, __byte_perm(A[wi], B[wi], 0x7632u), __byte_perm(C[wi], E[wi], 0x7632u));
       }
     }
   }
+  __syncthreads();
   if (s_fail) {
     // A stage never arrived: report it, wait (bounded) for the copies still
     // in flight into this CTA's shared memory, and leave the outputs alone.
     if (threadIdx.x == 0) {
       set_status(c.state, KVQ_DEV_TIMEOUT);
-      for (int k = it; k < min(ntiles, it + NSTAGE - 1); ++k) mbar_wait_bounded(&mbar[k % NSTAGE], (k / NSTAGE) & 1);
+      for (int s = 0; s < NSTAGE; ++s)
+        if (s_last_tile[s] >= 0) mbar_wait_bounded(&mbar[s], (s_last_tile[s] / NSTAGE) & 1);
     }
     return;
   }
@@ -392,26 +452,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_tc_kernel(const __gr
     }
   }
   __syncthreads();
-  merge_store<D, G, 8>(c, a, b, kvh, split, sm_m, sm_l, &sm_acc[0][0][0]);
+  merge_store<D, G, 8, NWARP>(c, a, b, kvh, split, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
-template <int D, int G, int KF, int VF>
-cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  constexpr int NSTAGE = TcStages<D, KF, VF>::v;
+template <int D, int G, int KF, int VF, int NGRP>
+cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
+  constexpr int NSTAGE = TcStages<D, G, KF, VF, NGRP>::v;
   const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   const int smem = NSTAGE * L.bytes + 1024;   // + alignment slack
-  if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
   static int configured = 0;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, KF, VF, NGRP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          NSTAGE * tc_layout<D, KF, VF>(D / 16, D / 16).bytes + 1024);
     if (e != cudaSuccess) return e;
     configured = 1;
   }
   const dim3 grid(a.nsplit, c.Hkv, c.B);
-  decode_tc_kernel<D, G, KF, VF><<<grid, kDecodeThreads, smem, st>>>(c, a);
+  decode_tc_kernel<D, G, KF, VF, NGRP><<<grid, TcShape<NGRP>::threads, smem, st>>>(c, a);
   note_launch();
   return cudaGetLastError();
+}
+
+template <int D, int G, int KF, int VF>
+cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
+  if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  return a.wide ? launch_decode_tc_shape<D, G, KF, VF, 2>(c, a, st) : launch_decode_tc_shape<D, G, KF, VF, 1>(c, a, st);
 }
 
 template <int D, int KF, int VF>

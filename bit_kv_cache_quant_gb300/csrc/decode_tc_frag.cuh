@@ -183,17 +183,6 @@ __host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
   return L;
 }
 
-// Pipeline depth of the tensor-core kernel: as many 64-token stages (2 to 4) as
-// fit in 42 KB, so that four 128-thread CTAs share an SM's shared memory.
-template <int D, int KF, int VF> struct TcStages {
-  static constexpr int bytes = ((64 * D * FmtBits<KF>::v / 8 + 64 * D * FmtBits<VF>::v / 8 +
-                                 ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * (D / 32) * 2 +
-                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * (D / 16) * 2) +
-                                1023) / 1024 * 1024;
-  static constexpr int raw = 43008 / bytes;
-  static constexpr int v = raw < 2 ? 2 : (raw > 4 ? 4 : raw);
-};
-
 // Key channel order: k-step ks, mma k index 2t + jj (jj in {0, 1}) and
 // 2t + 8 + jj of quad thread t.  4-bit codes: thread t reads word t of chunk
 // ks / 2 (channels 32 (ks / 2) + 8 t + 0..7), nibble pairs (c0, c4), (c2, c6)

@@ -143,6 +143,8 @@ struct DecodeArgs {
   float qscale;      // softmax scale * log2(e)
   float* partials;   // [B*Hkv][nsplit][G][D + kPartialPad] or null when nsplit == 1
   int nsplit;
+  int wide;          // tensor-core kernel: eight warps per CTA (the grid fits in one wave of
+                     // two CTAs per SM) instead of four
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
 // an (D, G) outside the instantiated set.
