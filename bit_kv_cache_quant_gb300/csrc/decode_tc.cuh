@@ -11,15 +11,19 @@
 //   S[16 x 16] = Q[16 x D] . K^T : rows 0..7 of the A operand hold fp16(q) of
 //     the (up to 8) query heads of the kv head, rows 8..15 the residual
 //     q - fp16(q), so the score of head h is row h + row h + 8 and q enters
-//     exactly.  The key codes enter as exact small integers; keys with
-//     per-token groups (affine, Q4_0) get one fp32 accumulator per 32-channel
-//     block and are scaled afterwards, s * sum(q u) + z * sum(q) (Q4_0:
-//     d * (sum(q u) - 8 sum(q))), so the scores carry no fp16 rounding of the
-//     keys.  Per-channel KIVI scales are folded into q; their zero term is a
-//     per-row constant the softmax does not see and is dropped.
+//     exactly.  The key codes enter as exact small integers (Q4_0 as the
+//     signed levels u - 8); keys with per-token groups (affine, Q4_0) get one
+//     fp32 accumulator per 32-channel block and are scaled afterwards, per
+//     scale group, s * sum(q u) + z * sum(q) (Q4_0: d * sum(q (u - 8))), so
+//     the scores carry no fp16 rounding of the keys.  Per-channel KIVI scales
+//     are folded into q; their zero term is a per-row constant the softmax
+//     does not see and is dropped.
 //   O[16 x D] += P[16 x 16] . V_hat : the block's probabilities as A (value +
-//     residual rows again), the value block dequantised to fp16 in registers
-//     as B (one HFMA2 with the token's fp16 scale and zero).
+//     residual rows again), the value block as B.  Values with several scale
+//     groups per token are dequantised to fp16 in registers (one HFMA2 with
+//     the token's fp16 scale and zero); values with one group per token enter
+//     as exact integer codes, the token's scale multiplies its probability and
+//     sum(p * zero) is accumulated apart in fp32 and added to every channel.
 // Codes become fp16 through the mantissa of 1024.0 (see nibbles_to_h2).
 #pragma once
 
@@ -40,6 +44,61 @@ __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* 
     for (int i = 0; i < NW / 4; ++i) {
       const uint4 v = *reinterpret_cast<const uint4*>(plane + swz_off<ROWB>(r, off + 16 * i));
       w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+  }
+}
+
+// O += P . V for one 16-token block: A = the probabilities (pa), B = the value
+// codes of the thread's four tokens (words A, B, C, E), dequantised to fp16 in
+// registers with each token's scale and zero when DEQ, else taken as exact
+// integers (the scale then sits in pa and the zero in a separate sum).
+template <int VB, int NW, int NT, bool DEQ>
+__device__ __forceinline__ void pv_mma(float (&oacc)[NT][4], const uint32_t (&pa)[4], const uint32_t (&A)[NW],
+                                       const uint32_t (&B)[NW], const uint32_t (&C)[NW], const uint32_t (&E)[NW],
+                                       __half2 sAB, __half2 zAB, __half2 sCD, __half2 zCD) {
+  if constexpr (VB == 4) {
+#pragma unroll
+    for (int wi = 0; wi < NW; ++wi) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t sel = half ? 0x7632u : 0x5410u;
+        __half2 h0[4], h1[4];
+        nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // channels 8 wi + 4 half + 0..3 of tokens A, B
+        nibbles_to_h2(__byte_perm(C[wi], E[wi], sel), h1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (DEQ) {
+            h0[i] = __hfma2(h0[i], sAB, zAB);
+            h1[i] = __hfma2(h1[i], sCD, zCD);
+          }
+          mma_f16(oacc[8 * wi + 4 * half + i], pa, h2u(h0[i]), h2u(h1[i]));
+        }
+      }
+    }
+  } else if constexpr (VB == 8) {
+#pragma unroll
+    for (int wi = 0; wi < NW; ++wi) {
+      const uint32_t a_ = A[wi] ^ 0x80808080u, b_ = B[wi] ^ 0x80808080u;
+      const uint32_t c_ = C[wi] ^ 0x80808080u, e_ = E[wi] ^ 0x80808080u;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t sel = half ? 0x7362u : 0x5140u;
+        __half2 l0, h0, l1, h1;
+        bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
+        bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
+        if constexpr (DEQ) {
+          l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
+          l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
+        }
+        mma_f16(oacc[4 * wi + 2 * half], pa, h2u(l0), h2u(l1));
+        mma_f16(oacc[4 * wi + 2 * half + 1], pa, h2u(h0), h2u(h1));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int wi = 0; wi < NW; ++wi) {
+      mma_f16(oacc[2 * wi], pa, __byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x5410u));
+      mma_f16(oacc[2 * wi + 1], pa, __byte_perm(A[wi], B[wi], 0x7632u), __byte_perm(C[wi], E[wi], 0x7632u));
     }
   }
 }
@@ -103,7 +162,9 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   // Query fragments in key-channel order (lane-major, one 16-byte vector per
   // k-step) and per-block sums of q for grouped keys.
   __shared__ __align__(16) uint4 sm_qa[KS][32];
-  __shared__ float sm_qblk[NB][8];
+  __shared__ float sm_qblk[NB][8];       // sum of q over each 32-channel block
+  __shared__ float sm_q64[NB / 2][8];    // ... over each 64-channel group
+  __shared__ float sm_q128[8];           // ... over all channels (D = 128)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int lane = threadIdx.x & 31;
@@ -161,7 +222,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
         if constexpr (K_KIVI) x *= __half2float(c.k.ch_scale[bh * D + ch[i]]);
         qv[i] = x;
       }
-      if constexpr (KG) qb[ks >> 1] += (qv[0] + qv[1]) + (qv[2] + qv[3]);
+      if constexpr (K_AFF) qb[ks >> 1] += (qv[0] + qv[1]) + (qv[2] + qv[3]);
       const __half2 h01 = __floats2half2_rn(qv[0], qv[1]);
       const __half2 h23 = __floats2half2_rn(qv[2], qv[3]);
       const float2 f01 = __half22float2(h01);
@@ -169,12 +230,22 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
       sm_qa[ks][lane] = make_uint4(h2u(h01), h2u(__floats2half2_rn(qv[0] - f01.x, qv[1] - f01.y)), h2u(h23),
                                    h2u(__floats2half2_rn(qv[2] - f23.x, qv[3] - f23.y)));
     }
-    if constexpr (KG) {
+    if constexpr (K_AFF) {
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
         qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 1);
         qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 2);
-        if (t == 0) sm_qblk[i][g] = qb[i];
+      }
+      if (t == 0) {
+        float all = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          sm_qblk[i][g] = qb[i];
+          all += qb[i];
+        }
+#pragma unroll
+        for (int j = 0; j < NB / 2; ++j) sm_q64[j][g] = qb[2 * j] + qb[2 * j + 1];
+        sm_q128[g] = all;
       }
     }
   }
@@ -186,13 +257,14 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const int t1 = min(T, t0 + per);
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
 
-  int kgrp[NB];
-#pragma unroll
-  for (int i = 0; i < NB; ++i) kgrp[i] = K_AFF ? (32 * i) / c.k.group : i;
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 
+  // Values with one (scale, zero) per token: the scale multiplies the
+  // probability instead of every code and the zero term is summed apart.
+  const bool vfold = V_AFF && vng == 1;
   float m_run = neg_inf();
   float l_part = 0.0f;
+  float zacc = 0.0f;   // sum of p * zero over this thread's tokens (vfold)
   float oacc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.0f;
@@ -227,7 +299,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
 #pragma unroll
           for (int p = 0; p < NB; ++p) {
             __half2 h[4];
-            nibbles_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
+            nibbles_to_h2<K_Q40 ? 8 : 0>(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
             const uint4 q0 = sm_qa[2 * p][lane], q1 = sm_qa[2 * p + 1][lane];
             const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
             float(&dst)[4] = acc[KG ? p : 0];
@@ -258,34 +330,40 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
           const int i = 2 * nt + e;
           float v;
           if constexpr (K_Q40) {
-            // the token's NB block scales in one load: d (sum q u - 8 sum q) per block
-            const uint8_t* srow = st + TL.ks + rr[i] * (2 * NB);
+            // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
             float d[NB];
-            if constexpr (NB == 4) {
-              const uint2 u = *reinterpret_cast<const uint2*>(srow);
-              const float2 f0 = __half22float2(u2h(u.x)), f1 = __half22float2(u2h(u.y));
-              d[0] = f0.x; d[1] = f0.y; d[2] = f1.x; d[3] = f1.y;
-            } else {
-              const float2 f0 = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(srow)));
-              d[0] = f0.x; d[1] = f0.y;
-            }
-            float wq = 0.0f;
+            load_halves<NB>(st + TL.ks + rr[i] * (2 * NB), d);
             v = 0.0f;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               v = fmaf(d[nb], acc[nb][e], v);
               v = fmaf(d[nb], acc[nb][2 + e], v);
-              wq = fmaf(d[nb], sm_qblk[nb][g], wq);
             }
-            v = fmaf(-8.0f, wq, v);
-          } else if constexpr (KG) {
-            const __half* srow = reinterpret_cast<const __half*>(st + TL.ks) + rr[i] * kng;
-            const __half* zrow = reinterpret_cast<const __half*>(st + TL.kz) + rr[i] * kng;
-            v = 0.0f;
+          } else if constexpr (K_AFF) {
+            // s * sum(q u) + z * sum(q) per scale group of 32, 64 or 128 channels
+            float x[NB];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const float x = acc[nb][e] + acc[nb][2 + e];
-              v = fmaf(__half2float(srow[kgrp[nb]]), x, fmaf(__half2float(zrow[kgrp[nb]]), sm_qblk[nb][g], v));
+            for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][e] + acc[nb][2 + e];
+            const uint8_t* srow = st + TL.ks + rr[i] * (2 * kng);
+            const uint8_t* zrow = st + TL.kz + rr[i] * (2 * kng);
+            v = 0.0f;
+            if (kng == NB) {
+              float sg[NB], zg[NB];
+              load_halves<NB>(srow, sg);
+              load_halves<NB>(zrow, zg);
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) v = fmaf(sg[nb], x[nb], fmaf(zg[nb], sm_qblk[nb][g], v));
+            } else if (2 * kng == NB) {
+              float sg[NB / 2], zg[NB / 2];
+              load_halves<NB / 2>(srow, sg);
+              load_halves<NB / 2>(zrow, zg);
+#pragma unroll
+              for (int j = 0; j < NB / 2; ++j) v = fmaf(sg[j], x[2 * j] + x[2 * j + 1], fmaf(zg[j], sm_q64[j][g], v));
+            } else if constexpr (NB == 4) {
+              float sg[1], zg[1];
+              load_halves<1>(srow, sg);
+              load_halves<1>(zrow, zg);
+              v = fmaf(sg[0], (x[0] + x[1]) + (x[2] + x[3]), zg[0] * sm_q128[g]);
             }
           } else {
             v = acc[0][e] + acc[0][2 + e];
@@ -302,18 +380,46 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
       if (mn > m_run) {
         const float alpha = exp2f(m_run - mn);
         l_part *= alpha;
+        zacc *= alpha;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           oacc[nt][0] *= alpha; oacc[nt][1] *= alpha; oacc[nt][2] *= alpha; oacc[nt][3] *= alpha;
         }
         m_run = mn;
       }
+      // Rows past the split's end were copied as whatever the buffer holds:
+      // their weight is 0, and their value scale / zero (or fp16 values) are
+      // zeroed so that no NaN reaches the MMA.
+      bool vok[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
       float p[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         p[i] = exp2f(sc[i] - mn);
         l_part += p[i];
       }
+      __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);
+      if constexpr (V_AFF) {
+        const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
+        const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
+        if (vfold) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float si = vok[i] ? __half2float(vs[rr[i]]) : 0.0f;
+            const float zi = vok[i] ? __half2float(vz[rr[i]]) : 0.0f;
+            zacc = fmaf(p[i], zi, zacc);
+            p[i] *= si;
+          }
+        } else {
+          const __half h0 = __ushort_as_half(0);
+          sAB = __halves2half2(vok[0] ? vs[rr[0] * vng + vgi] : h0, vok[1] ? vs[rr[1] * vng + vgi] : h0);
+          zAB = __halves2half2(vok[0] ? vz[rr[0] * vng + vgi] : h0, vok[1] ? vz[rr[1] * vng + vgi] : h0);
+          sCD = __halves2half2(vok[2] ? vs[rr[2] * vng + vgi] : h0, vok[3] ? vs[rr[3] * vng + vgi] : h0);
+          zCD = __halves2half2(vok[2] ? vz[rr[2] * vng + vgi] : h0, vok[3] ? vz[rr[3] * vng + vgi] : h0);
+        }
+      }
+      // ------------------------------------------------------------ O += P V
       uint32_t pa[4];
       {
         const __half2 ph0 = __floats2half2_rn(p[0], p[1]);
@@ -324,24 +430,6 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
         pa[1] = h2u(__floats2half2_rn(p[0] - pf0.x, p[1] - pf0.y));
         pa[2] = h2u(ph1);
         pa[3] = h2u(__floats2half2_rn(p[2] - pf1.x, p[3] - pf1.y));
-      }
-
-      // ------------------------------------------------------------ O += P V
-      // Rows past the split's end were copied as whatever the buffer holds: their
-      // weight is 0, and their value scale / zero (or fp16 values) are zeroed so
-      // that no NaN reaches the MMA.
-      bool vok[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
-      __half2 sAB, zAB, sCD, zCD;
-      if constexpr (V_AFF) {
-        const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
-        const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
-        const __half h0 = __ushort_as_half(0);
-        sAB = __halves2half2(vok[0] ? vs[rr[0] * vng + vgi] : h0, vok[1] ? vs[rr[1] * vng + vgi] : h0);
-        zAB = __halves2half2(vok[0] ? vz[rr[0] * vng + vgi] : h0, vok[1] ? vz[rr[1] * vng + vgi] : h0);
-        sCD = __halves2half2(vok[2] ? vs[rr[2] * vng + vgi] : h0, vok[3] ? vs[rr[3] * vng + vgi] : h0);
-        zCD = __halves2half2(vok[2] ? vz[rr[2] * vng + vgi] : h0, vok[3] ? vz[rr[3] * vng + vgi] : h0);
       }
       constexpr int NW = VTB / 4;
       uint32_t A[NW], B[NW], C[NW], E[NW];
@@ -361,51 +449,10 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
           }
         }
       }
-      if constexpr (VB == 4) {
-#pragma unroll
-        for (int wi = 0; wi < NW; ++wi) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t sel = half ? 0x7632u : 0x5410u;
-            __half2 h0[4], h1[4];
-            nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // channels 8 wi + 4 half + 0..3 of tokens A, B
-            nibbles_to_h2(__byte_perm(C[wi], E[wi], sel), h1);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if constexpr (V_AFF) {
-                h0[i] = __hfma2(h0[i], sAB, zAB);
-                h1[i] = __hfma2(h1[i], sCD, zCD);
-              }
-              mma_f16(oacc[8 * wi + 4 * half + i], pa, h2u(h0[i]), h2u(h1[i]));
-            }
-          }
-        }
-      } else if constexpr (VB == 8) {
-#pragma unroll
-        for (int wi = 0; wi < NW; ++wi) {
-          const uint32_t a_ = A[wi] ^ 0x80808080u, b_ = B[wi] ^ 0x80808080u;
-          const uint32_t c_ = C[wi] ^ 0x80808080u, e_ = E[wi] ^ 0x80808080u;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t sel = half ? 0x7362u : 0x5140u;
-            __half2 l0, h0, l1, h1;
-            bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
-            bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
-            if constexpr (V_AFF) {
-              l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
-              l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
-            }
-            mma_f16(oacc[4 * wi + 2 * half], pa, h2u(l0), h2u(l1));
-            mma_f16(oacc[4 * wi + 2 * half + 1], pa, h2u(h0), h2u(h1));
-          }
-        }
-      } else {
-#pragma unroll
-        for (int wi = 0; wi < NW; ++wi) {
-          mma_f16(oacc[2 * wi], pa, __byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x5410u));
-          mma_f16(oacc[2 * wi + 1], pa, __byte_perm(A[wi], B[wi], 0x7632u), __byte_perm(C[wi], E[wi], 0x7632u));
-        }
-      }
+      if (V_AFF && !vfold)
+        pv_mma<VB, NW, NT, true>(oacc, pa, A, B, C, E, sAB, zAB, sCD, zCD);
+      else
+        pv_mma<VB, NW, NT, false>(oacc, pa, A, B, C, E, sAB, zAB, sCD, zCD);
     }
     // Release the stage.  The group's last warp to finish it copies the tile
     // NSTAGE ahead into it (the fences order the four warps' reads of the
@@ -440,11 +487,13 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   // n-tile nt sits in column g' = 2t + e.
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+  zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
+  zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
   if (g < G) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       *reinterpret_cast<float2*>(&sm_acc[warp][g][nt * 8 + 2 * t]) =
-          make_float2(oacc[nt][0] + oacc[nt][2], oacc[nt][1] + oacc[nt][3]);
+          make_float2((oacc[nt][0] + oacc[nt][2]) + zacc, (oacc[nt][1] + oacc[nt][3]) + zacc);
     }
     if (t == 0) {
       sm_m[warp][g] = m_run;

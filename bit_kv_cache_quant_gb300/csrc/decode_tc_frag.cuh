@@ -29,17 +29,36 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
 
 // Eight nibbles of w (channel i in bits 4i..4i+3) as exact fp16 pairs:
 // h[0] = (c0, c4), h[1] = (c1, c5), h[2] = (c2, c6), h[3] = (c3, c7).
-// 0x6400 | n is 1024 + n; 0x6400 | (n << 4) is 1024 + 16 n.
+// 0x6400 | n is 1024 + n; 0x6400 | (n << 4) is 1024 + 16 n.  OFF = 8 gives the
+// signed levels n - 8 (Q4_0) instead.
+template <int OFF = 0>
 __device__ __forceinline__ void nibbles_to_h2(uint32_t w, __half2 (&h)[4]) {
+  static_assert(OFF == 0 || OFF == 8, "offset");
   const uint32_t M = 0x64006400u;
-  const __half2 k1024 = u2h(0x64006400u);
-  const __half2 k16th = u2h(0x2C002C00u);   // 1/16
-  const __half2 km64 = u2h(0xD400D400u);    // -64
+  const __half2 kLow = u2h(OFF ? 0x64086408u : 0x64006400u);    // 1024 + OFF
+  const __half2 k16th = u2h(0x2C002C00u);                         // 1/16
+  const __half2 kHigh = u2h(OFF ? 0xD480D480u : 0xD400D400u);    // -(64 + OFF)
   const uint32_t w8 = w >> 8;
-  h[0] = __hsub2(u2h((w & 0x000F000Fu) | M), k1024);
-  h[1] = __hfma2(u2h((w & 0x00F000F0u) | M), k16th, km64);
-  h[2] = __hsub2(u2h((w8 & 0x000F000Fu) | M), k1024);
-  h[3] = __hfma2(u2h((w8 & 0x00F000F0u) | M), k16th, km64);
+  h[0] = __hsub2(u2h((w & 0x000F000Fu) | M), kLow);
+  h[1] = __hfma2(u2h((w & 0x00F000F0u) | M), k16th, kHigh);
+  h[2] = __hsub2(u2h((w8 & 0x000F000Fu) | M), kLow);
+  h[3] = __hfma2(u2h((w8 & 0x00F000F0u) | M), k16th, kHigh);
+}
+
+// N consecutive fp16 values (N = 1, 2 or 4; 2N-byte aligned) as fp32.
+template <int N>
+__device__ __forceinline__ void load_halves(const uint8_t* p, float (&f)[N]) {
+  static_assert(N == 1 || N == 2 || N == 4, "count");
+  if constexpr (N == 1) {
+    f[0] = __half2float(*reinterpret_cast<const __half*>(p));
+  } else if constexpr (N == 2) {
+    const float2 a = __half22float2(u2h(*reinterpret_cast<const uint32_t*>(p)));
+    f[0] = a.x; f[1] = a.y;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(u2h(u.x)), b = __half22float2(u2h(u.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
 }
 
 // Four unsigned bytes of x as exact fp16 pairs: lo = (b0, b1), hi = (b2, b3).
