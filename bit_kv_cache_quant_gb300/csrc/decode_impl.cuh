@@ -139,6 +139,15 @@ __host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
   return L;
 }
 
+// Threads per output float4 in the cross-split merge: the largest of 8, 4, 2
+// that fits the CTA with a whole number of warps, else 1.
+__host__ __device__ constexpr int merge_lanes(int items, int threads) {
+  return (items * 8 <= threads && (items * 8) % 32 == 0)   ? 8
+         : (items * 4 <= threads && (items * 4) % 32 == 0) ? 4
+         : (items * 2 <= threads && (items * 2) % 32 == 0) ? 2
+                                                            : 1;
+}
+
 // Merges the per-warp (max, sum, accumulator) triples in shared memory and writes
 // the output (one split) or this split's partial; the last split of a (b, kv head)
 // to finish merges every partial with the online-softmax rule.
@@ -198,6 +207,24 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   __syncthreads();
   if (!s_last) return;
   const float* P0 = a.partials + bh * a.nsplit * G * PROW;
+  // Thread layout of the merge: SPL threads (adjacent lanes) per float4 of the
+  // G x D output, each summing every SPL-th split.  The first PF partial
+  // vectors of a thread's first float4 are requested before the weights are
+  // known, so the partial data costs about one round trip to L2.
+  constexpr int ITEMS = G * D / 4;
+  constexpr int SPL = merge_lanes(ITEMS, NTHR);
+  constexpr int PF = SPL <= 2 ? 16 : 8;
+  constexpr int kStrideF4 = G * PROW / 4;   // float4 stride between splits
+  float4 pre[PF];
+  if (threadIdx.x < ITEMS * SPL) {
+    const int item = threadIdx.x / SPL, sub = threadIdx.x % SPL;
+    const float4* src = reinterpret_cast<const float4*>(P0 + (item / (D / 4)) * PROW) + item % (D / 4);
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      const int sp = sub + j * SPL;
+      pre[j] = sp < a.nsplit ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   // Every split's (max, sum) at once; then one warp per head reduces them with
   // shuffles and leaves one weight per (split, head).
   for (int i = threadIdx.x; i < a.nsplit * G; i += NTHR) {
@@ -226,25 +253,51 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D / 4; idx += NTHR) {
-    const int h = idx / (D / 4), d4 = idx % (D / 4);
+  // ITEMS * SPL is a multiple of 32 whenever SPL > 1, so every lane of a warp
+  // runs the same iterations and the shuffles below see the whole warp.
+  for (int base = threadIdx.x; base < ITEMS * SPL; base += NTHR) {
+    const int item = base / SPL, sub = base % SPL;
+    const int h = item / (D / 4), d4 = item % (D / 4);
     const float4* src = reinterpret_cast<const float4*>(P0 + h * PROW) + d4;
-    constexpr int kStrideF4 = G * PROW / 4;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < a.nsplit; sp0 += 8) {
+    int j0 = 0;
+    if (base == threadIdx.x) {
+#pragma unroll
+      for (int j = 0; j < PF; ++j) {
+        const int sp = sub + j * SPL;
+        const float e = sp < a.nsplit ? sm_w[sp][h] : 0.0f;
+        A.x = fmaf(pre[j].x, e, A.x);
+        A.y = fmaf(pre[j].y, e, A.y);
+        A.z = fmaf(pre[j].z, e, A.z);
+        A.w = fmaf(pre[j].w, e, A.w);
+      }
+      j0 = PF;
+    }
+    for (int j1 = j0; sub + j1 * SPL < a.nsplit; j1 += 8) {
       float4 p[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        p[j] = (sp0 + j < a.nsplit) ? __ldcg(src + (size_t)(sp0 + j) * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 8; ++j) {
+        const int sp = sub + (j1 + j) * SPL;
+        p[j] = sp < a.nsplit ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float e = (sp0 + j < a.nsplit) ? sm_w[sp0 + j][h] : 0.0f;
+        const int sp = sub + (j1 + j) * SPL;
+        const float e = sp < a.nsplit ? sm_w[sp][h] : 0.0f;
         A.x = fmaf(p[j].x, e, A.x);
         A.y = fmaf(p[j].y, e, A.y);
         A.z = fmaf(p[j].z, e, A.z);
         A.w = fmaf(p[j].w, e, A.w);
       }
     }
+#pragma unroll
+    for (int o = SPL / 2; o > 0; o >>= 1) {
+      A.x += __shfl_xor_sync(0xffffffffu, A.x, o);
+      A.y += __shfl_xor_sync(0xffffffffu, A.y, o);
+      A.z += __shfl_xor_sync(0xffffffffu, A.z, o);
+      A.w += __shfl_xor_sync(0xffffffffu, A.w, o);
+    }
+    if (sub != 0) continue;
     const float inv = sm_inv[h];
     const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + 4 * d4;
     store_io(a.out, oo + 0, a.io_dtype, A.x * inv);

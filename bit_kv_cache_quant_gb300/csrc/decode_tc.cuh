@@ -177,12 +177,13 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const int vng = c.v.n_groups;
   const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
 
-  // Thread 0 reads the stored length, sets up the barriers and starts the
-  // first NSTAGE tile copies; warp 1 meanwhile builds the query fragments.
+  // Thread 0 reads the stored length and sets up the barriers while warp 1
+  // builds the query fragments; then warp w starts the copy of tile w.
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
-    const int T = c.state->stored;
+    s_T = c.state->stored;
+    s_fail = 0;
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&mbar[s], 1);
@@ -191,19 +192,6 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_async_smem();   // the initialised barriers are visible to the copy engine
-    int per = (T + a.nsplit - 1) / a.nsplit;
-    per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
-    const int t0 = min(T, split * per);
-    const int ntiles = (min(T, t0 + per) - t0 + kTileTokens - 1) / kTileTokens;
-#pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) {
-      if (s < ntiles) {
-        issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
-        s_last_tile[s] = s;
-      }
-    }
-    s_T = T;
-    s_fail = 0;
   }
   if (warp == 1) {
     float qb[NB];
@@ -256,6 +244,12 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const int t0 = min(T, split * per);
   const int t1 = min(T, t0 + per);
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
+  if (lane == 0) {
+    for (int s = warp; s < NSTAGE && s < ntiles; s += NWARP) {
+      issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
+      s_last_tile[s] = s;
+    }
+  }
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 
