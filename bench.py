@@ -424,20 +424,34 @@ def run_reference(a, rank, world):
     print(json.dumps(line))
 
 
-def decode_traffic(w, kvq_dir):
-    """DRAM bytes per decode launch from the committed ncu summary, if it matches this kernel source."""
+DECODE_SOURCES = ("kvq_internal.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh")
+
+
+def decode_source_sha(kvq_dir):
+    """sha256 over the decode kernels' sources: a committed ncu figure holds only for these bytes."""
     import hashlib
 
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(kvq_dir, "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_kernel_name(w):
+    """The decode kernel the library launches for this workload (tensor-core path for 16-bit io, D 64/128)."""
+    return "decode_tc_kernel" if w.io_dtype != "float32" and w.head_dim in (64, 128) else "decode_kernel"
+
+
+def decode_traffic(w, kvq_dir):
+    """DRAM bytes per decode launch from the committed ncu summary, if it matches this kernel source."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    src = os.path.join(kvq_dir, "csrc", "decode_impl.cuh")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
     entry = d.get(w.name)
-    if not entry or entry.get("kernel_source_sha256") != sha:
+    if not entry or entry.get("kernel_source_sha256") != decode_source_sha(kvq_dir):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -478,7 +492,7 @@ def bench_decode(a, kvq, w, rank, world):
         "gpu_launches": (ds.launches_append + ds.launches_decode) * a.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": decode_traffic(w, os.path.dirname(kvq.__file__)),
-                     "kernel": "decode_kernel", "bytes_per_launch": dec_bytes_launch,
+                     "kernel": decode_kernel_name(w), "bytes_per_launch": dec_bytes_launch,
                      "avg_launch_us": avg_dec_launch_s * 1e6, "peak_kind": f"{peak_kind} copy bandwidth"},
         "clocks": clk,
     }
