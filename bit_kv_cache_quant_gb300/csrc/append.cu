@@ -102,11 +102,10 @@ __device__ __forceinline__ float group_min(float x, int width) {
   return x;
 }
 
-template <typename T, int E>
-__device__ __forceinline__ void quantize_row(const SideView& s, const float* __restrict__ bias, const T* __restrict__ src,
+// Codes lane `lane`'s E channels x (already loaded as fp32) of one row.
+template <int E>
+__device__ __forceinline__ void quantize_row(const SideView& s, const float* __restrict__ bias, float (&x)[E],
                                              size_t bh, int cap_alloc, int slot, int lane) {
-  float x[E];
-  load_row_slice<T, E>(src + lane * E, x);
   uint8_t* row = s.codes + ((size_t)bh * cap_alloc + slot) * s.row_bytes;
   const size_t meta_row = ((size_t)bh * cap_alloc + slot) * s.n_groups;
 
@@ -168,13 +167,26 @@ __device__ __forceinline__ void quantize_row(const SideView& s, const float* __r
   if (lane % width == 0) s.tok_scale[meta_row + lane / width] = __float2half_rn(d);
 }
 
-// One warp per (b, kv head, token) row of the append; 4 warps per CTA.
+// One warp per (b, kv head, token) row of the append; 8 warps per CTA.  The
+// input rows are requested before the counters are read (they do not depend
+// on them).  With more than one CTA the last to arrive advances the counters,
+// once every CTA has read them; a one-CTA append advances them directly.
+constexpr int kAppendWarps = 8;
+
 template <typename T, int E>
-__global__ void __launch_bounds__(128) append_kernel(CacheView c, const T* __restrict__ k, const T* __restrict__ v,
-                                                     int n, long long rows) {
+__global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, const T* __restrict__ k,
+                                                                    const T* __restrict__ v, int n, long long rows) {
   __shared__ long long s_pos;
   __shared__ int s_stored;
   __shared__ int s_ok;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kAppendWarps + warp;
+  float xk[E], xv[E];
+  if (row < rows) {
+    load_row_slice<T, E>(k + row * c.D + lane * E, xk);
+    load_row_slice<T, E>(v + row * c.D + lane * E, xv);
+  }
   if (threadIdx.x == 0) {
     s_pos = c.state->pos;
     s_stored = c.state->stored;
@@ -183,9 +195,6 @@ __global__ void __launch_bounds__(128) append_kernel(CacheView c, const T* __res
     if (!ok && blockIdx.x == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 4 + warp;
   if (s_ok && row < rows) {
     const int i = (int)(row % n);
     const long long bh = row / n;
@@ -206,26 +215,29 @@ __global__ void __launch_bounds__(128) append_kernel(CacheView c, const T* __res
     }
     if (write) {
       const float* bias = c.k_bias ? c.k_bias + (size_t)kvh * c.D : nullptr;
-      quantize_row<T, E>(c.k, bias, k + row * c.D, bh, c.cap_alloc, slot, lane);
-      quantize_row<T, E>(c.v, nullptr, v + row * c.D, bh, c.cap_alloc, slot, lane);
+      quantize_row<E>(c.k, bias, xk, bh, c.cap_alloc, slot, lane);
+      quantize_row<E>(c.v, nullptr, xv, bh, c.cap_alloc, slot, lane);
     }
   }
-  // The last CTA to arrive advances the counters (every CTA has read them).
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x != 0) return;
+  bool last = true;
+  if (gridDim.x > 1) {
     __threadfence();
-    const unsigned prev = atomicAdd(&c.state->append_arrive, 1u);
-    if (prev == gridDim.x - 1) {
-      if (s_ok) {
-        const long long np = s_pos + n;
-        c.state->pos = np;
-        if (c.layout == KVQ_LAYOUT_RING) {
-          const long long w = (long long)c.sink + c.window;
-          c.state->stored = (int)(np < w ? np : w);
-        } else {
-          c.state->stored = s_stored + n;
-        }
+    last = atomicAdd(&c.state->append_arrive, 1u) == gridDim.x - 1;
+  }
+  if (last) {
+    if (s_ok) {
+      const long long np = s_pos + n;
+      c.state->pos = np;
+      if (c.layout == KVQ_LAYOUT_RING) {
+        const long long w = (long long)c.sink + c.window;
+        c.state->stored = (int)(np < w ? np : w);
+      } else {
+        c.state->stored = s_stored + n;
       }
+    }
+    if (gridDim.x > 1) {
       c.state->append_arrive = 0u;
       __threadfence();
     }
@@ -242,13 +254,13 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
     note_launch();
   }
   const long long rows = (long long)c.B * c.Hkv * n;
-  const unsigned grid = (unsigned)((rows + 3) / 4);
+  const unsigned grid = (unsigned)((rows + kAppendWarps - 1) / kAppendWarps);
   const T* kk = static_cast<const T*>(k);
   const T* vv = static_cast<const T*>(v);
   switch (c.D) {
-    case 32: append_kernel<T, 1><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
-    case 64: append_kernel<T, 2><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
-    case 128: append_kernel<T, 4><<<grid, 128, 0, st>>>(c, kk, vv, n, rows); break;
+    case 32: append_kernel<T, 1><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
+    case 64: append_kernel<T, 2><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
+    case 128: append_kernel<T, 4><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
     default: return cudaErrorInvalidValue;
   }
   note_launch();

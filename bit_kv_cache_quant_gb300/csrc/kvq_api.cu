@@ -223,13 +223,15 @@ bool encode_rows_map(CUtensorMap* m, void* base, size_t rows, int row_bytes) {
 }
 
 int decode_nsplit(const kvq_cache_s* c) {
-  // About eight CTAs per SM in all (even waves), at least 256 rows per split.
+  // About eight CTAs per SM in all (even waves); at least 256 rows per split
+  // (one 64-row tile for caches under 4096 rows, where latency dominates).
   const int units = c->cfg.batch * c->cfg.n_kv_heads;
   int rows = c->cfg.capacity;
   if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);
   const int target = 8 * c->sms;
   int ns = (target + units / 2) / units;
-  const int max_by_len = rows / 256 > 1 ? rows / 256 : 1;
+  const int min_rows = rows >= 4096 ? 256 : 64;
+  const int max_by_len = rows / min_rows > 1 ? rows / min_rows : 1;
   if (ns > max_by_len) ns = max_by_len;
   if (ns > kvq::kMaxSplits) ns = kvq::kMaxSplits;
   if (ns < 1) ns = 1;
