@@ -112,19 +112,27 @@ template <int NGRP> struct TcShape {
   static constexpr int ctas_per_sm = 4 / NGRP;
 };
 
-// Pipeline depth: as many 64-token stages (a multiple of NGRP, 2 to 8) as fit
-// next to one CTA's static shared memory at TcShape::ctas_per_sm CTAs per SM.
+// Pipeline depth.  Four-warp CTAs (four per SM, several waves) use two
+// stages: deeper rings measured slower on the 32K and ring workloads, whose
+// time is instruction issue, not latency.  Eight-warp CTAs (one wave) take as
+// many stages (a multiple of NGRP, up to 8) as fit next to the static shared
+// memory, so that a short split is requested in one go.
 template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
   static constexpr int stage = ((64 * D * FmtBits<KF>::v / 8 + 64 * D * FmtBits<VF>::v / 8 +
                                  ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * (D / 32) * 2 +
                                  ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * (D / 16) * 2) +
                                 1023) / 1024 * 1024;
   static constexpr int warps = TcShape<NGRP>::warps;
-  static constexpr int static_smem = warps * G * (D + 8) * 4 + 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 +
-                                     (D / 16) * 512 + 1024;
+  // per-warp (head, channel) accumulators, written over the stages after the loop
+  static constexpr int acc_bytes = warps * G * (D + 8) * 4;
+  static constexpr int static_smem = 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 + (D / 16) * 512 + 1024;
   static constexpr int budget = 227 * 1024 / TcShape<NGRP>::ctas_per_sm - 2048 - static_smem;
   static constexpr int raw = (budget / stage) / NGRP * NGRP;
-  static constexpr int v = raw < 2 ? 2 : (raw > 8 ? 8 : raw);
+  static constexpr int v = NGRP == 1 ? 2 : (raw < 2 ? 2 : (raw > 8 ? 8 : raw));
+  // dynamic shared memory for a stage size (+ 1 KB to align the ring to 1024)
+  static constexpr int dyn_bytes(int stage_bytes) {
+    return (v * stage_bytes > acc_bytes ? v * stage_bytes : acc_bytes) + 1024;
+  }
 };
 
 template <int D, int G, int KF, int VF, int NGRP>
@@ -153,7 +161,6 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ float sm_m[NWARP][G];
   __shared__ float sm_l[NWARP][G];
-  __shared__ __align__(16) float sm_acc[NWARP][G][D + 8];   // channel d at (d % VCH) * 8 + d / VCH
   __shared__ __align__(8) uint64_t mbar[NSTAGE];
   __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (4 per tile)
   __shared__ int s_last_tile[NSTAGE];     // last tile copied into a stage, -1 if none
@@ -477,8 +484,10 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     return;
   }
 
-  // Per-warp results to shared memory: head g, channel g' * VCH + nt of
-  // n-tile nt sits in column g' = 2t + e.
+  // Per-warp results to shared memory, over the stage ring (every copy has
+  // landed and been read): head g, channel g' * VCH + nt of n-tile nt sits in
+  // column g' = 2t + e, at (d % VCH) * 8 + d / VCH.
+  float(*sm_acc)[G][D + 8] = reinterpret_cast<float(*)[G][D + 8]>(smem);
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
   zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
@@ -500,14 +509,14 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
 
 template <int D, int G, int KF, int VF, int NGRP>
 cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  constexpr int NSTAGE = TcStages<D, G, KF, VF, NGRP>::v;
   const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
-  const int smem = NSTAGE * L.bytes + 1024;   // + alignment slack
+  using S = TcStages<D, G, KF, VF, NGRP>;
+  const int smem = S::dyn_bytes(L.bytes);
   static int configured = 0;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, KF, VF, NGRP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         NSTAGE * tc_layout<D, KF, VF>(D / 16, D / 16).bytes + 1024);
+                                         S::dyn_bytes(tc_layout<D, KF, VF>(D / 16, D / 16).bytes));
     if (e != cudaSuccess) return e;
     configured = 1;
   }
