@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
 
   // Thread 0 reads the stored length and sets up the barriers while warp 1
-  // builds the query fragments; then warp w starts the copy of tile w.
+  // builds the query fragments.
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
@@ -251,11 +251,15 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const int t0 = min(T, split * per);
   const int t1 = min(T, t0 + per);
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
-  if (lane == 0) {
-    for (int s = warp; s < NSTAGE && s < ntiles; s += NWARP) {
-      issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
-      s_last_tile[s] = s;
-    }
+  // Each warp group's first tile is requested alone, so that it reaches the
+  // SM ahead of the rest of the split (which every CTA would otherwise ask
+  // for at the same moment); the group's first warp requests the group's
+  // other initial tiles once that tile has landed.
+  const int grp = warp >> 2;
+  const bool leader = (warp & 3) == 0 && lane == 0;
+  if (leader && grp < ntiles) {
+    issue_tile_tma<D, KF, VF>(smem + grp * TL.bytes, TL, c, bh, t0 + grp * kTileTokens, &mbar[grp]);
+    s_last_tile[grp] = grp;
   }
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
@@ -270,7 +274,6 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.0f;
 
-  const int grp = warp >> 2;
   const int blk = (warp & 3) * 16;                      // this warp's 16 rows of each tile
   // rows of the four tokens this thread's scores / value pairs belong to
   const int rr[4] = {blk + tau<VROW>(2 * t), blk + tau<VROW>(2 * t + 1), blk + tau<VROW>(2 * t + 8),
@@ -282,6 +285,12 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar[stg], (it / NSTAGE) & 1))) {
       s_fail = 1;
       break;
+    }
+    if (it == grp && leader) {
+      for (int s = grp + NGRP; s < NSTAGE && s < ntiles; s += NGRP) {
+        issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
+        s_last_tile[s] = s;
+      }
     }
     const uint8_t* st = smem + stg * TL.bytes;
     const int tok0 = t0 + it * kTileTokens + blk;

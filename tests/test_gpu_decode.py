@@ -133,3 +133,24 @@ def test_repeated_calls_are_identical(kvq):
     b = cache.decode_attn(q)
     assert torch.equal(a, b)
     assert kvq.kvq_decode_workspace_bytes(cache.handle, 24) > 0
+
+
+# The tensor-core decode picks its launch shape from the number of (batch row,
+# kv head) pairs and the cache length.  On a 152-SM GB300 these cases land on
+# each shape: eight-warp CTAs with a global split merge (the grid fits one
+# wave at two CTAs per SM), with one or many splits; four-warp CTAs (larger
+# grids).  Whatever the shape, the result must match the oracle.
+LAUNCH_SHAPES = [
+    ("eight_warps_32_splits", 1, 8, 8192 + 37, None),
+    ("eight_warps_4_splits", 2, 4, 300, None),
+    ("eight_warps_2_splits", 13, 8, 150, 150),
+    ("four_warps", 16, 8, 2000, None),
+]
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}{p[1]}-{p[3]}{p[4]}")
+@pytest.mark.parametrize("name,B,H,T,cap", LAUNCH_SHAPES, ids=[s[0] for s in LAUNCH_SHAPES])
+def test_decode_launch_shapes(kvq, pair, name, B, H, T, cap):
+    cache, oc = _build(kvq, pair, B, H, 128, T, torch.bfloat16, seed=T + B, cap=cap, bias=pair[0] == "q4_0")
+    for G in (3, 8):
+        _check(kvq, cache, oc, G, torch.bfloat16, seed=G + 11, what=f"{name} G={G}")
