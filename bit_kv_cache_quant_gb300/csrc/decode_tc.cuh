@@ -184,12 +184,18 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   const int vng = c.v.n_groups;
   const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
 
-  // Thread 0 reads the stored length and sets up the barriers while warp 1
-  // builds the query fragments.
+  // Before the grids this launch depends on have finished (programmatic
+  // dependent launch), touch only what they cannot change: the tensor maps,
+  // this CTA's barriers, and L2 / address-translation hints for the first
+  // rows this split would read at full capacity.
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
-    s_T = c.state->stored;
+    const size_t row0 = bh * c.cap_alloc + (size_t)split * ((c.cap + a.nsplit - 1) / a.nsplit);
+    prefetch_l2(c.k.codes + row0 * KROW);
+    prefetch_l2(c.v.codes + row0 * VROW);
+    if constexpr (KG) prefetch_l2(c.k.tok_scale + row0 * c.k.n_groups);
+    if constexpr (V_AFF) prefetch_l2(c.v.tok_scale + row0 * c.v.n_groups);
     s_fail = 0;
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) {
@@ -200,6 +206,9 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_async_smem();   // the initialised barriers are visible to the copy engine
   }
+  grid_dependency_wait();
+  // Thread 0 reads the stored length while warp 1 builds the query fragments.
+  if (threadIdx.x == 0) s_T = c.state->stored;
   if (warp == 1) {
     float qb[NB];
 #pragma unroll
@@ -482,6 +491,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     }
   }
   __syncthreads();
+  grid_launch_dependents();   // the next launch may start its prologue during this merge
   if (s_fail) {
     // A stage never arrived: report it, wait (bounded) for the copies still
     // in flight into this CTA's shared memory, and leave the outputs alone.
@@ -529,10 +539,23 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
     if (e != cudaSuccess) return e;
     configured = 1;
   }
-  const dim3 grid(a.nsplit, c.Hkv, c.B);
-  decode_tc_kernel<D, G, KF, VF, NGRP><<<grid, TcShape<NGRP>::threads, smem, st>>>(c, a);
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: its CTAs may start once that kernel's CTAs have all triggered
+  // (this kernel triggers after its main loop) and wait in the kernel for it
+  // to complete before reading anything.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nsplit, c.Hkv, c.B);
+  cfg.blockDim = dim3(TcShape<NGRP>::threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, G, KF, VF, NGRP>, c, a);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 template <int D, int G, int KF, int VF>

@@ -202,6 +202,19 @@ __host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
   return L;
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed (a no-op for a launch without the attribute), and allow the
+// next dependent launch to start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// A hint: bring the line at p into L2 (and its page translation into the TLBs).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 // Key channel order: k-step ks, mma k index 2t + jj (jj in {0, 1}) and
 // 2t + 8 + jj of quad thread t.  4-bit codes: thread t reads word t of chunk
 // ks / 2 (channels 32 (ks / 2) + 8 t + 0..7), nibble pairs (c0, c4), (c2, c6)
