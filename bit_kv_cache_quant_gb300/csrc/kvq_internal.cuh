@@ -156,7 +156,7 @@ cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, 
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
                         cudaStream_t st);
 
-constexpr int kSnapChunk = 512;   // keys per CTA of the SnapKV scoring kernels
+constexpr int kSnapChunk = 256;   // keys per CTA of the SnapKV scoring kernels
 constexpr int kTmaRows = 64;      // rows per TMA box of a code plane (one decode tile)
 constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)
 constexpr int kPartialPad = 4;    // decode partial row: D accumulators, max, sum, 2 pad (16-byte rows)

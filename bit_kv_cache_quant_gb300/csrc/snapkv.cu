@@ -9,14 +9,17 @@
 // Scoring is a [w x D] x [D x S] contraction per head, run on the tensor
 // cores (fp16 inputs, fp32 accumulation, mma.sync m16n8k16) in two passes
 // over the keys: pass 1 gives each CTA's per-row (max, sum of exp) over its
-// 512 keys, pass 2 merges those row statistics and turns every logit into
-// its probability, summing over the w rows.  The second read of K is served
-// by L2 for the prompt sizes the page discusses (16K keys x 8 heads x 256 B).
+// kSnapChunk keys, pass 2 merges those row statistics and turns every logit
+// into its probability, summing over the w rows.  Each warp keeps the next
+// 8 keys' fragments in flight while it multiplies the current ones.  The
+// second read of K is served by L2 for the prompt sizes the page discusses
+// (16K keys x 8 heads x 256 B).
 //
 // Selection is a radix select on the fp32 score bit patterns (4 passes of 8
-// bits) that finds the (budget - n_sink)-th largest score exactly, followed
-// by one ordered pass that keeps every larger score and the lowest-indexed
-// equal ones, emitting positions in ascending order with a block scan.
+// bits, the scores held in shared memory) that finds the (budget - n_sink)-th
+// largest score exactly, followed by one ordered pass that keeps every larger
+// score and the lowest-indexed equal ones, emitting positions in ascending
+// order with a block scan.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -55,19 +58,24 @@ __device__ __forceinline__ void load_obs(uint32_t (&A)[MT][D / 16][4], const __h
   }
 }
 
-// Logits of 8 keys [key0, key0 + 8) against the 16*MT observation rows.
-// cacc[mt][0..1] = rows mt*16+g, keys key0+2t, +1; cacc[mt][2..3] = rows +8.
-template <int D, int MT>
-__device__ __forceinline__ void tile_logits(float (&cacc)[MT][4], const uint32_t (&A)[MT][D / 16][4],
-                                            const __half* kh, int key0, int S, int g, int t) {
-  const int kr = min(key0 + g, S - 1);
-  const __half* p = kh + (size_t)kr * D;
-  uint32_t Bf[D / 16][2];
+// B fragments of 8 keys [key0, key0 + 8): thread (g, t) holds key key0 + g,
+// channels ks*16 + 2t (+1) and ks*16 + 2t + 8 (+9).  Keys past the end repeat
+// the last key (their logits are never used).
+template <int D>
+__device__ __forceinline__ void load_keys(uint32_t (&Bf)[D / 16][2], const __half* kh, int key0, int S, int g, int t) {
+  const __half* p = kh + (size_t)min(key0 + g, S - 1) * D;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     Bf[ks][0] = ld_pair(p + ks * 16 + 2 * t);
     Bf[ks][1] = ld_pair(p + ks * 16 + 2 * t + 8);
   }
+}
+
+// Logits of those 8 keys against the 16*MT observation rows.
+// cacc[mt][0..1] = rows mt*16+g, keys key0+2t, +1; cacc[mt][2..3] = rows +8.
+template <int D, int MT>
+__device__ __forceinline__ void tile_logits(float (&cacc)[MT][4], const uint32_t (&A)[MT][D / 16][4],
+                                            const uint32_t (&Bf)[D / 16][2]) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     cacc[mt][0] = cacc[mt][1] = cacc[mt][2] = cacc[mt][3] = 0.0f;
@@ -101,11 +109,17 @@ __global__ void __launch_bounds__(128) snapkv_stats_kernel(const __half* __restr
 
   constexpr int kPerWarp = kSnapChunk / 4;
   const int wbase = chunk * kSnapChunk + warp * kPerWarp;
-  for (int tile = 0; tile < kPerWarp / 8; ++tile) {
+  const int ntile = max(0, min(kPerWarp / 8, (S - wbase + 7) / 8));
+  uint32_t Bn[D / 16][2];
+  if (ntile > 0) load_keys<D>(Bn, kh, wbase, S, g, t);
+  for (int tile = 0; tile < ntile; ++tile) {
     const int key0 = wbase + tile * 8;
-    if (key0 >= S) break;
+    uint32_t Bc[D / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) Bc[ks][0] = Bn[ks][0], Bc[ks][1] = Bn[ks][1];
+    if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);   // next tile's keys in flight
     float cacc[MT][4];
-    tile_logits<D, MT>(cacc, A, kh, key0, S, g, t);
+    tile_logits<D, MT>(cacc, A, Bc);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -178,21 +192,39 @@ __global__ void __launch_bounds__(128) snapkv_scores_kernel(const __half* __rest
   const int chunk = blockIdx.x;
   const __half* kh = k + bh * head_stride * D;
 
-  if (threadIdx.x < MT * 16) {
-    const int r = threadIdx.x;
-    float M = 0.0f, iz = 0.0f;
-    if (r < w) {
-      M = ninf();
-      for (int cch = 0; cch < nchunk; ++cch) M = fmaxf(M, stats[(bh * nchunk + cch) * 64 + r].x);
-      float Z = 0.0f;
-      for (int cch = 0; cch < nchunk; ++cch) {
+  // Merge every chunk's (max, sum) of each observation row: TPR adjacent
+  // threads per row, each over every TPR-th chunk, then a shuffle merge.
+  {
+    constexpr int R = MT * 16;
+    constexpr int TPR = (128 / R) >= 4 ? 4 : ((128 / R) >= 2 ? 2 : 1);
+    const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
+    float M = ninf(), Z = 0.0f;
+    if (r < R && r < w) {
+#pragma unroll 8
+      for (int cch = part; cch < nchunk; cch += TPR) {
         const float2 st = stats[(bh * nchunk + cch) * 64 + r];
-        if (st.x != ninf()) Z += st.y * exp2f(st.x - M);
+        if (st.x != ninf()) {
+          const float mn = fmaxf(M, st.x);
+          Z = Z * exp2f(M - mn) + st.y * exp2f(st.x - mn);
+          M = mn;
+        }
       }
-      iz = 1.0f / Z;
     }
-    row_m[r] = M;
-    row_iz[r] = iz;
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1) {
+      const float mo = __shfl_xor_sync(0xffffffffu, M, o);
+      const float zo = __shfl_xor_sync(0xffffffffu, Z, o);
+      const float mn = fmaxf(M, mo);
+      const float ea = (M == ninf()) ? 0.0f : exp2f(M - mn);
+      const float eb = (mo == ninf()) ? 0.0f : exp2f(mo - mn);
+      Z = Z * ea + zo * eb;
+      M = mn;
+    }
+    if (r < R && part == 0) {
+      const bool live = r < w;
+      row_m[r] = live ? M : 0.0f;
+      row_iz[r] = live ? 1.0f / Z : 0.0f;
+    }
   }
   __syncthreads();
 
@@ -210,11 +242,17 @@ __global__ void __launch_bounds__(128) snapkv_scores_kernel(const __half* __rest
   const float inv_w = 1.0f / (float)w;
   constexpr int kPerWarp = kSnapChunk / 4;
   const int wbase = chunk * kSnapChunk + warp * kPerWarp;
-  for (int tile = 0; tile < kPerWarp / 8; ++tile) {
+  const int ntile = max(0, min(kPerWarp / 8, (S - wbase + 7) / 8));
+  uint32_t Bn[D / 16][2];
+  if (ntile > 0) load_keys<D>(Bn, kh, wbase, S, g, t);
+  for (int tile = 0; tile < ntile; ++tile) {
     const int key0 = wbase + tile * 8;
-    if (key0 >= S) break;
+    uint32_t Bc[D / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) Bc[ks][0] = Bn[ks][0], Bc[ks][1] = Bn[ks][1];
+    if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);   // next tile's keys in flight
     float cacc[MT][4];
-    tile_logits<D, MT>(cacc, A, kh, key0, S, g, t);
+    tile_logits<D, MT>(cacc, A, Bc);
     float col[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -277,8 +315,48 @@ __device__ __forceinline__ int block_excl_count(bool flag, int* total, int* warp
   return r;
 }
 
+// The (budget - n_sink)-th largest key among `need` remaining: given the
+// 256-bin histogram of the current digit, warp 0 finds the bin where the
+// count of larger-or-equal digits reaches `need` (a suffix scan, 8 bins per
+// lane) and how many of that bin are still needed.
+__device__ __forceinline__ void pick_bin(const unsigned* hist, unsigned need, unsigned* s_bin, unsigned* s_need) {
+  const int lane = threadIdx.x & 31;
+  // lane l owns bins 255 - 8l ... 248 - 8l (descending digit order)
+  unsigned cnt[8], own = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cnt[i] = hist[255 - 8 * lane - i];
+    own += cnt[i];
+  }
+  unsigned incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const unsigned before = incl - own;   // keys in larger digits than this lane's bins
+  const bool here = before < need && incl >= need;
+  if (here) {
+    unsigned cum = before;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (cum + cnt[i] >= need) {
+        *s_bin = 255u - 8u * lane - i;
+        *s_need = need - cum;
+        break;
+      }
+      cum += cnt[i];
+    }
+  }
+}
+
+// Scores live in shared memory when they fit (dynamic size S floats); larger
+// prompts read them from global memory on every pass.
+constexpr int kTopkSmemKeys = 48 * 1024;
+
 __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int S, int budget, int n_sink,
                                                     int* __restrict__ idx_out) {
+  extern __shared__ float sm_sc[];
   __shared__ unsigned hist[256];
   __shared__ unsigned s_bin, s_need;
   __shared__ int warp_sums[33];
@@ -290,6 +368,18 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
     for (int j = threadIdx.x; j < S; j += blockDim.x) out[j] = j;
     return;
   }
+  const bool in_smem = S <= kTopkSmemKeys;
+  if (in_smem) {
+    // coalesced copy; the row start is 16-byte aligned when S % 4 == 0
+    if ((S & 3) == 0 && (reinterpret_cast<uintptr_t>(sc) & 15) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(sc);
+      for (int i = threadIdx.x; i < S / 4; i += blockDim.x) reinterpret_cast<float4*>(sm_sc)[i] = __ldg(src + i);
+    } else {
+      for (int i = threadIdx.x; i < S; i += blockDim.x) sm_sc[i] = __ldg(sc + i);
+    }
+    __syncthreads();
+  }
+  const float* src = in_smem ? sm_sc : sc;
   const int ns = min(n_sink, S);
   const int k = budget - ns;   // 0 <= k < S - ns
   unsigned prefix = 0u, mask = 0u, need = (unsigned)k;
@@ -299,22 +389,11 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
       for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
       __syncthreads();
       for (int j = ns + threadIdx.x; j < S; j += blockDim.x) {
-        const unsigned key = order_key(sc[j]);
+        const unsigned key = order_key(src[j]);
         if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        unsigned cum = 0u;
-        for (int bin = 255; bin >= 0; --bin) {
-          const unsigned hcount = hist[bin];
-          if (cum + hcount >= need) {
-            s_bin = (unsigned)bin;
-            s_need = need - cum;
-            break;
-          }
-          cum += hcount;
-        }
-      }
+      if (threadIdx.x < 32) pick_bin(hist, need, &s_bin, &s_need);
       __syncthreads();
       prefix |= s_bin << shift;
       mask |= 0xFFu << shift;
@@ -327,7 +406,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
   for (int base = 0; base < S; base += blockDim.x) {
     const int j = base + threadIdx.x;
     const bool in_rest = (j >= ns) && (j < S);
-    const unsigned key = (j < S) ? order_key(sc[j]) : 0u;
+    const unsigned key = (j < S) ? order_key(src[j]) : 0u;
     const bool tie = (k > 0) && in_rest && key == prefix;
     int tie_total;
     const int tie_rank = block_excl_count(tie, &tie_total, warp_sums) + tie_running;
@@ -369,7 +448,15 @@ static cudaError_t launch_snapkv_d(const void* k, long long hs, int B, int Hkv, 
 
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
                         cudaStream_t st) {
-  topk_kernel<<<B * Hkv, 1024, 0, st>>>(scores, S, budget, n_sink, idx);
+  const int smem = S <= kTopkSmemKeys ? S * (int)sizeof(float) : 0;
+  static int configured = 0;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kTopkSmemKeys * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    configured = 1;
+  }
+  topk_kernel<<<B * Hkv, 1024, smem, st>>>(scores, S, budget, n_sink, idx);
   note_launch();
   return cudaGetLastError();
 }
