@@ -387,8 +387,59 @@ class OracleSample:
                 f"{self.oc.stored} stored tokens): append + evict + float64 attention per step")
 
 
+class SnapKVOracleSample:
+    """The oracle's SnapKV episode on one (batch 0, kv head 0) slice: observation
+    window scores and sink-forced top-k over the prompt's keys, keep-set
+    gather, then the decode steps (fp16 append + float64 attention)."""
+
+    def __init__(self, w):
+        from oracle import attention as oatt
+        from oracle import snapkv as osnap
+        from oracle.cache import CacheSpec
+
+        self.oatt, self.osnap, self.w = oatt, osnap, w
+        self.G = w.group
+        k, v = synth.snapkv_prefill(w, batch=1)
+        self.k = k[:, :1].float().numpy()
+        self.v = v[:, :1].float().numpy()
+        self.spec = CacheSpec(batch=1, n_kv_heads=1, head_dim=w.head_dim, capacity=w.prompt_len + w.decode_steps,
+                              layout="linear", sink=0, window=0, k_format="fp16", k_bits=16, k_group=0,
+                              v_format="fp16", v_bits=16, v_group=0, k_bias=None)
+        self.steps = []
+        for t in range(w.decode_steps):
+            q, k1, v1 = synth.decode_token_inputs(w, 0, t, w.prompt_len + t, batch=1)
+            self.steps.append((q[:, :self.G].float().numpy(), k1[:, :1].float().numpy(), v1[:, :1].float().numpy()))
+        sel, gat, dec = snapkv_episode_bytes(w, 1, 1)
+        self.bytes = sel + gat + dec
+
+    def step(self):
+        """One episode; returns its algorithmic bytes."""
+        from oracle.cache import OracleCache
+
+        w = self.w
+        oc = OracleCache(self.spec)
+        oc.append(self.k, self.v)
+        _, idx = self.osnap.snapkv_select(self.k, w.obs_window, w.budget, w.n_sink)
+        oc.evict_keepset(idx)
+        for q, k1, v1 in self.steps:
+            oc.append(k1, v1)
+            kh, vh = oc.dequant()
+            self.oatt.decode_attention(q, kh, vh)
+        return self.bytes
+
+    def describe(self):
+        w = self.w
+        return (f"batch row 0, kv head 0 of {w.name} ({self.G} query heads): prompt of {w.prompt_len} keys, "
+                f"scores + top-{w.budget} + keep-set gather, then {w.decode_steps} fp16 append + float64 "
+                f"attention steps, per episode")
+
+
+def oracle_sample(w):
+    return SnapKVOracleSample(w) if w.prompt_len else OracleSample(w)
+
+
 def cpu_baseline(w, seconds):
-    s = OracleSample(w)
+    s = oracle_sample(w)
     s.step()
     nbytes, n, t0 = 0, 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds:
@@ -403,10 +454,7 @@ def run_reference(a, rank, world):
     if world > 1 and rank != 0:
         return
     w = synth.get_workload(a.workload)
-    if w.prompt_len:
-        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times decode workloads only"}))
-        return
-    s = OracleSample(w)
+    s = oracle_sample(w)
     for _ in range(a.warmup):
         s.step()
     nbytes, t0 = 0, time.perf_counter()
@@ -417,7 +465,8 @@ def run_reference(a, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3 / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample": "one (batch, kv head) slice of one layer per step"},
+            "config": {"workload": w.name, "sample": "one (batch, kv head) slice of one layer per step"
+                                                     if not w.prompt_len else "one (batch, kv head) slice per episode"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{a.steps} steps of {s.describe()}"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -505,39 +554,179 @@ def bench_decode(a, kvq, w, rank, world):
     return line
 
 
+def snapkv_episode_bytes(w, batch, n_kv_heads):
+    """Algorithmic bytes of one SnapKV episode: (select, keep-set gather, decode steps).
+
+    select: the prompt's K read, scores written and read back by the top-k,
+    indices written; gather: every kept K and V row read and written; decode:
+    each step's single-token append plus attention over the kept rows and the
+    tokens appended so far."""
+    S, D, budget = w.prompt_len, w.head_dim, w.budget
+    bh = batch * n_kv_heads
+    sel = bh * (S * D * 2 + 2 * S * 4 + budget * 4)
+    gather = 2 * bh * budget * 2 * D * 2
+    w1 = w.with_(batch=batch, n_kv_heads=n_kv_heads, n_q_heads=n_kv_heads * w.group)
+    dec = sum(decode_bytes(w1, budget + t + 1) + append_bytes(w1, 1) for t in range(w.decode_steps))
+    return sel, gather, dec
+
+
+class SnapKVEpisode:
+    """SnapKV prefill eviction and the decode that follows, on the device: the
+    prompt's K/V in an fp16 cache, observation-window scoring + top-k, keep-set
+    gather into the cache, then `decode_steps` single-token appends and decode
+    attentions.  The episode (everything after the prompt fill) is one CUDA
+    graph; each replay starts from a freshly filled cache."""
+
+    def __init__(self, kvq, w, device):
+        self.kvq, self.w = kvq, w
+        self.k, self.v = synth.snapkv_prefill(w, device=device)
+        B, H, S, D = self.k.shape
+        self.B, self.H, self.S, self.D = B, H, S, D
+        Hq, steps = w.n_q_heads, w.decode_steps
+        self.cache = kvq.KVCache(B, H, D, S + steps, "fp16", 16, 0, "fp16", 16, 0, device=device)
+        self.ws = torch.empty(kvq.snapkv_workspace_bytes(B, H, S, D, w.obs_window), dtype=torch.uint8, device=device)
+        self.scores = torch.empty((B, H, S), dtype=torch.float32, device=device)
+        self.idx = torch.empty((B, H, w.budget), dtype=torch.int32, device=device)
+        per = B * Hq * D + 2 * B * H * D
+        self.stage = torch.empty(steps * per, dtype=torch.float16, device=device)
+        self.q, self.k1, self.v1 = [], [], []
+        for t in range(steps):
+            q, k1, v1 = synth.decode_token_inputs(w, 0, t, S + t, device=device, batch=B)
+            base = t * per
+            views = []
+            for x, off in ((q, 0), (k1, q.numel()), (v1, q.numel() + k1.numel())):
+                vw = self.stage[base + off: base + off + x.numel()].view(x.shape)
+                vw.copy_(x)
+                views.append(vw)
+            self.q.append(views[0]), self.k1.append(views[1]), self.v1.append(views[2])
+        self.out = torch.empty((steps, B, Hq, D), dtype=torch.float16, device=device)
+        self.cache.workspace(Hq)
+        self.launches = 0
+
+    def fill(self):
+        self.cache.reset()
+        self.cache.append(self.k, self.v)
+
+    def episode(self):
+        kvq, w, c = self.kvq, self.w, self.cache
+        n = 0
+        kvq.snapkv_select(self.k, self.S, self.B, self.H, self.S, self.D, w.obs_window, w.budget, w.n_sink,
+                          self.scores, self.idx, self.ws)
+        n += kvq.kvq_last_launch_count()
+        c.launches = 0
+        c.evict_keepset(self.idx)
+        for t in range(w.decode_steps):
+            c.append(self.k1[t], self.v1[t])
+            c.decode_attn(self.q[t], out=self.out[t])
+        return n + c.launches
+
+    def capture(self):
+        self.fill()
+        self.episode()
+        self.fill()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.launches = self.episode()
+        torch.cuda.synchronize()
+
+
 def bench_snapkv(a, kvq, w, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
-    k, _ = synth.snapkv_prefill(w, device=device)
-    B, H, S, D = k.shape
-    ws = torch.empty(kvq.snapkv_workspace_bytes(B, H, S, D, w.obs_window), dtype=torch.uint8, device=device)
-    scores = torch.empty((B, H, S), dtype=torch.float32, device=device)
-    idx = torch.empty((B, H, w.budget), dtype=torch.int32, device=device)
+    ep = SnapKVEpisode(kvq, w, device)
+    ep.capture()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    sel_b, gat_b, dec_b = snapkv_episode_bytes(w, ep.B, ep.H)
+    total_b = sel_b + gat_b + dec_b
     for _ in range(a.warmup):
-        kvq.snapkv_select(k, S, B, H, S, D, w.obs_window, w.budget, w.n_sink, scores, idx, ws)
-    nbytes = k.numel() * 2 + scores.numel() * 4 + idx.numel() * 4
+        ep.fill()
+        ep.graph.replay()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    clocks = ClockSampler()
+    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     for i in range(a.steps):
+        ep.fill()
         flush.zero_()
         ev[i][0].record()
-        kvq.snapkv_select(k, S, B, H, S, D, w.obs_window, w.budget, w.n_sink, scores, idx, ws)
+        ep.graph.replay()
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
-    t = max_over_ranks(sum(s.elapsed_time(e) for s, e in ev) / 1e3, world)
+    clk = clocks.stop()
+    t = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in ev) / 1e3, world)
+    # the select alone, for the roofline of its two scoring passes + top-k
+    sel_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    for i in range(a.steps):
+        flush.zero_()
+        sel_ev[i][0].record()
+        kvq.snapkv_select(ep.k, ep.S, ep.B, ep.H, ep.S, ep.D, w.obs_window, w.budget, w.n_sink, ep.scores, ep.idx,
+                          ep.ws)
+        sel_ev[i][1].record()
+    torch.cuda.synchronize()
+    t_sel = sum(s_.elapsed_time(e_) for s_, e_ in sel_ev) / 1e3 / a.steps
     peak, peak_kind = read_peaks()
-    achieved = nbytes * a.steps / t / 1e9
-    return {"metric": METRIC, "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
-            "warmup": a.warmup, "ms_per_step": t * 1e3 / a.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
-            "config": {"workload": w.name, "prompt": S, "n_kv_heads": H, "head_dim": D, "obs_window": w.obs_window,
-                       "budget": w.budget, "n_sink": w.n_sink, "step": "snapkv_select (scores + top-k)",
-                       "l2": "flushed between timed steps"},
-            "gpu_launches": 3 * a.steps,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_kind": f"{peak_kind} copy bandwidth"}}
+    achieved = sel_b / t_sel / 1e9
+    line = {"metric": METRIC, "value": world * total_b * a.steps / t / 1e9, "unit": "GB/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": t * 1e3 / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
+            "config": {"workload": w.name, "prompt": ep.S, "n_kv_heads": ep.H, "n_q_heads": w.n_q_heads,
+                       "head_dim": ep.D, "obs_window": w.obs_window, "budget": w.budget, "n_sink": w.n_sink,
+                       "decode_steps": w.decode_steps,
+                       "step": "one episode: snapkv_select (scores + top-k), keep-set gather into the cache, "
+                               "then per decode step an fp16 append and decode attention (one CUDA graph)",
+                       "l2": "flushed (256 MiB write) after the prompt fill, before each timed episode",
+                       "parallelism": f"replicas x{world}"},
+            "snapkv_select_us": t_sel * 1e6,
+            "decode_steps_per_s": world * w.decode_steps * a.steps / t,
+            "gpu_launches": ep.launches * a.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "kernel": "snapkv_select (stats + scores + top-k)",
+                         "bytes_per_launch": sel_b, "avg_launch_us": t_sel * 1e6,
+                         "peak_kind": f"{peak_kind} copy bandwidth"},
+            "clocks": clk}
+    if not a.no_e2e:
+        line["e2e"] = e2e_snapkv(ep, max(3, min(a.steps, 20)), world, total_b)
+    return line
+
+
+def e2e_snapkv(ep, episodes, world, total_b):
+    """Public API, eager calls: the decode steps' inputs copied in from pinned host
+    memory, the selected indices and every step's output read back."""
+    host_in = torch.empty(ep.stage.shape, dtype=ep.stage.dtype, pin_memory=True)
+    host_in.copy_(ep.stage)
+    host_out = torch.empty(ep.out.shape, dtype=ep.out.dtype, pin_memory=True)
+    host_idx = torch.empty(ep.idx.shape, dtype=ep.idx.dtype, pin_memory=True)
+
+    def once():
+        ep.fill()
+        ep.stage.copy_(host_in, non_blocking=True)
+        ep.episode()
+        host_idx.copy_(ep.idx, non_blocking=True)
+        host_out.copy_(ep.out, non_blocking=True)
+
+    once()
+    torch.cuda.synchronize()
+    dt = 0.0
+    barrier(world)
+    for _ in range(episodes):
+        ep.fill()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ep.stage.copy_(host_in, non_blocking=True)
+        ep.episode()
+        host_idx.copy_(ep.idx, non_blocking=True)
+        host_out.copy_(ep.out, non_blocking=True)
+        torch.cuda.synchronize()
+        dt += time.perf_counter() - t0
+    barrier(world)
+    dt = max_over_ranks(dt, world)
+    return {"value": world * total_b * episodes / dt / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
+            "d2h_bytes_per_step": host_out.numel() * host_out.element_size() + host_idx.numel() * 4,
+            "how": "public Python API, eager calls per episode (prompt fill outside the timing), pinned host "
+                   "inputs copied in and outputs read back every episode (wall clock)"}
 
 
 def main(argv=None):
@@ -555,7 +744,7 @@ def main(argv=None):
     if a.layers > 0:
         w = w.with_(layers=a.layers)
     line = bench_snapkv(a, kvq, w, rank, world) if w.prompt_len else bench_decode(a, kvq, w, rank, world)
-    if rank == 0 and not a.no_cpu_baseline and not w.prompt_len:
+    if rank == 0 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, a.cpu_seconds)
     if rank == 0:
         print(json.dumps(line))

@@ -230,6 +230,12 @@ class KVCache:
             lib.kvq_cache_release(h)
             self.handle = None
 
+    def reset(self, stream=None) -> None:
+        """Empties the cache (counters to zero) on the same device buffer."""
+        lib.kvq_cache_release(self.handle)
+        self.handle = None
+        self.handle = kvq_cache_init(self.cfg, self.buf, stream)
+
     def append(self, k: torch.Tensor, v: torch.Tensor, calibrate_k: bool = False, stream=None) -> None:
         n = k.shape[2]
         kvq_append(self.handle, k, v, n, DTYPES[k.dtype], APPEND_CALIBRATE_K if calibrate_k else 0, stream)

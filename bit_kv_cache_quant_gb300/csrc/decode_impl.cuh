@@ -139,6 +139,21 @@ __host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
   return L;
 }
 
+// Rows [t0, t1) of split `split` and the number of live splits `nse` for a
+// cache holding T rows, with at most `nsplit` splits (the grid): whole 64-row
+// tiles spread evenly, at least 4 tiles per split from 4096 rows on and 1
+// below.  Every CTA reads the same T, so all agree on nse; splits past nse
+// have no rows and take no part in the merge.
+__device__ __forceinline__ void split_rows(int T, int nsplit, int split, int& t0, int& t1, int& nse) {
+  const int nt = (T + kTileTokens - 1) / kTileTokens;
+  int tps = (nt + nsplit - 1) / nsplit;
+  const int min_tiles = T >= 4096 ? 4 : 1;
+  if (tps < min_tiles) tps = min_tiles;
+  nse = nt > 0 ? (nt + tps - 1) / tps : 1;
+  t0 = min(T, split * tps * kTileTokens);
+  t1 = min(T, t0 + tps * kTileTokens);
+}
+
 // Threads per output float4 in the cross-split merge: the largest of 8, 4, 2
 // that fits the CTA with a whole number of warps, else 1.
 __host__ __device__ constexpr int merge_lanes(int items, int threads) {
@@ -154,7 +169,7 @@ __host__ __device__ constexpr int merge_lanes(int items, int threads) {
 // Accumulator layout: ACCPAD == 0: acc[warp][h][d]; ACCPAD > 0 (tensor-core
 // kernel): rows of D + ACCPAD floats, channel d at (d % (D/8)) * 8 + d / (D/8).
 template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps>
-__device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split,
+__device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split, int nse,
                                             float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc) {
   constexpr int PROW = D + kPartialPad;
   constexpr int AROW = D + ACCPAD;
@@ -180,7 +195,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
         L = fmaf(sm_l[w][h], e, L);
       }
     }
-    if (a.nsplit == 1) {
+    if (nse == 1) {
       const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;
       store_io(a.out, oo, a.io_dtype, L > 0.0f ? A / L : 0.0f);
     } else {
@@ -192,7 +207,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
       }
     }
   }
-  if (a.nsplit == 1) return;
+  if (nse == 1) return;
 
   // The last split of this (b, kv head) to finish merges all partials.  The
   // barrier orders every thread's partial stores before thread 0's device-scope
@@ -200,7 +215,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const bool last = atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(a.nsplit - 1);
+    const bool last = atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(nse - 1);
     if (last) __threadfence();   // the other splits' partials are visible to the whole CTA after the barrier
     s_last = last;
   }
@@ -222,12 +237,12 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
 #pragma unroll
     for (int j = 0; j < PF; ++j) {
       const int sp = sub + j * SPL;
-      pre[j] = sp < a.nsplit ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      pre[j] = sp < nse ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   // Every split's (max, sum) at once; then one warp per head reduces them with
   // shuffles and leaves one weight per (split, head).
-  for (int i = threadIdx.x; i < a.nsplit * G; i += NTHR) {
+  for (int i = threadIdx.x; i < nse * G; i += NTHR) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(P0 + i * PROW + D));
     sm_w[i / G][i % G] = ml.x;
     sm_lsum[i / G][i % G] = ml.y;
@@ -237,11 +252,11 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     const int lane = threadIdx.x & 31;
     for (int h = threadIdx.x >> 5; h < G; h += NWARP) {
       float M = neg_inf();
-      for (int sp = lane; sp < a.nsplit; sp += 32) M = fmaxf(M, sm_w[sp][h]);
+      for (int sp = lane; sp < nse; sp += 32) M = fmaxf(M, sm_w[sp][h]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       float L = 0.0f;
-      for (int sp = lane; sp < a.nsplit; sp += 32) {
+      for (int sp = lane; sp < nse; sp += 32) {
         const float ms = sm_w[sp][h];
         const float e = (ms == neg_inf()) ? 0.0f : exp2f(ms - M);
         L = fmaf(sm_lsum[sp][h], e, L);
@@ -265,7 +280,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
 #pragma unroll
       for (int j = 0; j < PF; ++j) {
         const int sp = sub + j * SPL;
-        const float e = sp < a.nsplit ? sm_w[sp][h] : 0.0f;
+        const float e = sp < nse ? sm_w[sp][h] : 0.0f;
         A.x = fmaf(pre[j].x, e, A.x);
         A.y = fmaf(pre[j].y, e, A.y);
         A.z = fmaf(pre[j].z, e, A.z);
@@ -273,17 +288,17 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
       }
       j0 = PF;
     }
-    for (int j1 = j0; sub + j1 * SPL < a.nsplit; j1 += 8) {
+    for (int j1 = j0; sub + j1 * SPL < nse; j1 += 8) {
       float4 p[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int sp = sub + (j1 + j) * SPL;
-        p[j] = sp < a.nsplit ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        p[j] = sp < nse ? __ldcg(src + (size_t)sp * kStrideF4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int sp = sub + (j1 + j) * SPL;
-        const float e = sp < a.nsplit ? sm_w[sp][h] : 0.0f;
+        const float e = sp < nse ? sm_w[sp][h] : 0.0f;
         A.x = fmaf(p[j].x, e, A.x);
         A.y = fmaf(p[j].y, e, A.y);
         A.z = fmaf(p[j].z, e, A.z);
@@ -385,10 +400,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   if (threadIdx.x == 0) s_T = c.state->stored;
   __syncthreads();
   const int T = s_T;
-  int per = (T + a.nsplit - 1) / a.nsplit;
-  per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
-  const int t0 = min(T, split * per);
-  const int t1 = min(T, t0 + per);
+  int t0, t1, nse;
+  split_rows(T, a.nsplit, split, t0, t1, nse);
+  if (split >= nse) return;   // no rows for this split
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
 
   // Start streaming before anything else.
@@ -576,7 +590,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   }
   __syncthreads();
 
-  merge_store<D, G, 0>(c, a, b, kvh, split, sm_m, sm_l, &sm_acc[0][0][0]);
+  merge_store<D, G, 0>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
 template <int D, int G, int KF, int VF>

@@ -255,10 +255,9 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   }
   __syncthreads();
   const int T = s_T;
-  int per = (T + a.nsplit - 1) / a.nsplit;
-  per = (per + kTileTokens - 1) / kTileTokens * kTileTokens;
-  const int t0 = min(T, split * per);
-  const int t1 = min(T, t0 + per);
+  int t0, t1, nse;
+  split_rows(T, a.nsplit, split, t0, t1, nse);
+  if (split >= nse) return;   // no rows for this split (no copy was issued)
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
   // Each warp group's first tile is requested alone, so that it reaches the
   // SM ahead of the rest of the split (which every CTA would otherwise ask
@@ -523,7 +522,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     }
   }
   __syncthreads();
-  merge_store<D, G, 8, NWARP>(c, a, b, kvh, split, sm_m, sm_l, &sm_acc[0][0][0]);
+  merge_store<D, G, 8, NWARP>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
 template <int D, int G, int KF, int VF, int NGRP>

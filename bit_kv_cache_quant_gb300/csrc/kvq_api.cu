@@ -223,8 +223,10 @@ bool encode_rows_map(CUtensorMap* m, void* base, size_t rows, int row_bytes) {
 }
 
 int decode_nsplit(const kvq_cache_s* c) {
-  // About eight CTAs per SM in all (even waves); at least 256 rows per split
-  // (one 64-row tile for caches under 4096 rows, where latency dominates).
+  // The grid's splits per (b, kv head), an upper bound: about eight CTAs per
+  // SM in all (even waves), at least 256 rows per split of the capacity (one
+  // 64-row tile under 4096 rows).  The kernel spreads the rows actually
+  // stored over at most this many splits.
   const int units = c->cfg.batch * c->cfg.n_kv_heads;
   int rows = c->cfg.capacity;
   if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);

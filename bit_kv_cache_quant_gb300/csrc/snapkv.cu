@@ -289,31 +289,6 @@ __device__ __forceinline__ unsigned order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix count of `flag` over the block (blockDim.x == 1024);
-// *total gets the block's count.
-__device__ __forceinline__ int block_excl_count(bool flag, int* total, int* warp_sums) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_sums[warp] = __popc(bal);
-  __syncthreads();
-  if (warp == 0) {
-    const int v = warp_sums[lane];
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    warp_sums[lane] = incl - v;
-    if (lane == 31) warp_sums[32] = incl;
-  }
-  __syncthreads();
-  const int r = warp_sums[warp] + in_warp;
-  *total = warp_sums[32];
-  __syncthreads();
-  return r;
-}
 
 // The (budget - n_sink)-th largest key among `need` remaining: given the
 // 256-bin histogram of the current digit, warp 0 finds the bin where the
@@ -353,6 +328,37 @@ __device__ __forceinline__ void pick_bin(const unsigned* hist, unsigned need, un
 // Scores live in shared memory when they fit (dynamic size S floats); larger
 // prompts read them from global memory on every pass.
 constexpr int kTopkSmemKeys = 48 * 1024;
+
+// Exclusive prefix sum of `v` over the block (blockDim.x a multiple of 32,
+// at most 1024); *total gets the block's sum.
+__device__ __forceinline__ int block_excl_count_n(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    const int ws = lane < nw ? warp_sums[lane] : 0;
+    int wincl = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += n;
+    }
+    warp_sums[lane] = wincl - ws;
+    if (lane == 31) warp_sums[32] = wincl;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl - v;
+  *total = warp_sums[32];
+  __syncthreads();
+  return r;
+}
 
 __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int S, int budget, int n_sink,
                                                     int* __restrict__ idx_out) {
@@ -401,21 +407,44 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
       __syncthreads();
     }
   }
-  // prefix is the exact key of the k-th largest score; `need` equal keys are kept.
-  int running = 0, tie_running = 0;
-  for (int base = 0; base < S; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    const bool in_rest = (j >= ns) && (j < S);
-    const unsigned key = (j < S) ? order_key(src[j]) : 0u;
-    const bool tie = (k > 0) && in_rest && key == prefix;
-    int tie_total;
-    const int tie_rank = block_excl_count(tie, &tie_total, warp_sums) + tie_running;
-    const bool sel = (j < ns) || ((k > 0) && in_rest && (key > prefix || (tie && tie_rank < (int)need)));
-    int sel_total;
-    const int rank = block_excl_count(sel, &sel_total, warp_sums) + running;
-    if (sel) out[rank] = j;
-    running += sel_total;
-    tie_running += tie_total;
+  // prefix is the exact key of the k-th largest score; `need` equal keys are
+  // kept, the lowest positions first.  Thread i owns positions
+  // [i * seg, (i + 1) * seg): it counts its sinks, larger keys and ties, two
+  // block scans place its ties and its selected positions, and it writes
+  // them in ascending order.
+  const int seg = (S + blockDim.x - 1) / blockDim.x;
+  const int j0 = min(S, (int)threadIdx.x * seg), j1 = min(S, j0 + seg);
+  int n_big = 0, n_tie = 0;
+  for (int j = j0; j < j1; ++j) {
+    if (j < ns) {
+      ++n_big;
+    } else if (k > 0) {
+      const unsigned key = order_key(src[j]);
+      n_big += key > prefix;
+      n_tie += key == prefix;
+    }
+  }
+  int tie_total;
+  const int tie_before = block_excl_count_n(n_tie, &tie_total, warp_sums);
+  const int ties_kept = max(0, min(n_tie, (int)need - tie_before));
+  int sel_total;
+  int pos = block_excl_count_n(n_big + ties_kept, &sel_total, warp_sums);
+  int ties_left = ties_kept;
+  for (int j = j0; j < j1; ++j) {
+    bool sel;
+    if (j < ns) {
+      sel = true;
+    } else if (k > 0) {
+      const unsigned key = order_key(src[j]);
+      sel = key > prefix;
+      if (key == prefix && ties_left > 0) {
+        sel = true;
+        --ties_left;
+      }
+    } else {
+      sel = false;
+    }
+    if (sel) out[pos++] = j;
   }
 }
 
