@@ -447,7 +447,7 @@ kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int3
   if (obs_window < 1 || obs_window > 64) return fail(KVQ_ERR_UNSUPPORTED, "obs_window must be in 1..64");
   if (budget < 1 || n_sink < 0) return fail(KVQ_ERR_INVALID_ARG, "budget >= 1 and n_sink >= 0 required");
   if (n_sink > budget) return fail(KVQ_ERR_INVALID_ARG, "n_sink must not exceed budget");
-  if (((uintptr_t)k & 3) != 0) return fail(KVQ_ERR_INVALID_ARG, "k must be 4-byte aligned");
+  if (((uintptr_t)k & 7) != 0) return fail(KVQ_ERR_INVALID_ARG, "k must be 8-byte aligned");
   const size_t need = snapkv_workspace_bytes(batch, n_kv_heads, S, head_dim, obs_window);
   if (!workspace || ws_bytes < need)
     return fail(KVQ_ERR_CAPACITY, "snapkv workspace needs %zu bytes, got %zu", need, ws_bytes);

@@ -32,16 +32,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ uint32_t ld_pair(const __half* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
+__device__ __forceinline__ uint2 ld_quad(const __half* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
+// Channel order shared by the observation rows (A) and the keys (B): k-step
+// ks, mma k index 2t + j (j < 2) is channel 16 ks + 4t + j and 2t + 8 + j is
+// 16 ks + 4t + 2 + j, so each thread reads 8 contiguous bytes of a row per
+// k-step.  Both operands use it, so the dot products are unchanged.
+
 // Observation rows as A fragments: row r (0..16*MT) is key S - w + r, zero when r >= w.
 template <int D, int MT>
-__device__ __forceinline__ void load_obs(uint32_t (&A)[MT][D / 16][4], const __half* kh, int S, int w, int g,
-                                         int t) {
+__device__ __forceinline__ void load_obs_perm(uint32_t (&A)[MT][D / 16][4], const __half* kh, int S, int w, int g,
+                                              int t) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const int r0 = mt * 16 + g, r1 = r0 + 8;
@@ -49,94 +52,56 @@ __device__ __forceinline__ void load_obs(uint32_t (&A)[MT][D / 16][4], const __h
     const __half* p1 = kh + (size_t)(S - w + r1) * D;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const int c0 = ks * 16 + 2 * t;
-      A[mt][ks][0] = r0 < w ? ld_pair(p0 + c0) : 0u;
-      A[mt][ks][1] = r1 < w ? ld_pair(p1 + c0) : 0u;
-      A[mt][ks][2] = r0 < w ? ld_pair(p0 + c0 + 8) : 0u;
-      A[mt][ks][3] = r1 < w ? ld_pair(p1 + c0 + 8) : 0u;
+      const int c0 = ks * 16 + 4 * t;
+      const uint2 v0 = r0 < w ? ld_quad(p0 + c0) : make_uint2(0u, 0u);
+      const uint2 v1 = r1 < w ? ld_quad(p1 + c0) : make_uint2(0u, 0u);
+      A[mt][ks][0] = v0.x;
+      A[mt][ks][1] = v1.x;
+      A[mt][ks][2] = v0.y;
+      A[mt][ks][3] = v1.y;
     }
   }
 }
 
 // B fragments of 8 keys [key0, key0 + 8): thread (g, t) holds key key0 + g,
-// channels ks*16 + 2t (+1) and ks*16 + 2t + 8 (+9).  Keys past the end repeat
-// the last key (their logits are never used).
+// channels 16 ks + 4t .. 4t + 3.  Keys past the end repeat the last key (their
+// logits are never used).
 template <int D>
 __device__ __forceinline__ void load_keys(uint32_t (&Bf)[D / 16][2], const __half* kh, int key0, int S, int g, int t) {
   const __half* p = kh + (size_t)min(key0 + g, S - 1) * D;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    Bf[ks][0] = ld_pair(p + ks * 16 + 2 * t);
-    Bf[ks][1] = ld_pair(p + ks * 16 + 2 * t + 8);
+    const uint2 v = ld_quad(p + ks * 16 + 4 * t);
+    Bf[ks][0] = v.x;
+    Bf[ks][1] = v.y;
   }
 }
 
 // Logits of those 8 keys against the 16*MT observation rows.
 // cacc[mt][0..1] = rows mt*16+g, keys key0+2t, +1; cacc[mt][2..3] = rows +8.
+// Even and odd k-steps accumulate apart (two short dependency chains).
 template <int D, int MT>
 __device__ __forceinline__ void tile_logits(float (&cacc)[MT][4], const uint32_t (&A)[MT][D / 16][4],
                                             const uint32_t (&Bf)[D / 16][2]) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
+    float odd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     cacc[mt][0] = cacc[mt][1] = cacc[mt][2] = cacc[mt][3] = 0.0f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint32_t b[2] = {Bf[ks][0], Bf[ks][1]};
-      mma16816(cacc[mt], A[mt][ks], b);
+      mma16816((ks & 1) ? odd : cacc[mt], A[mt][ks], b);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cacc[mt][i] += odd[i];
   }
 }
 
-// Pass 1: per-row (max, sum 2^(logit - max)) over this CTA's keys, log2 domain.
-template <int D, int MT>
-__global__ void __launch_bounds__(128) snapkv_stats_kernel(const __half* __restrict__ k, long long head_stride,
-                                                           int Hkv, int S, int w, float cscale, float2* stats,
-                                                           int nchunk) {
-  __shared__ float sm_m[4][MT * 16];
-  __shared__ float sm_z[4][MT * 16];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const size_t bh = (size_t)blockIdx.z * Hkv + blockIdx.y;
-  const int chunk = blockIdx.x;
-  const __half* kh = k + bh * head_stride * D;
-
-  uint32_t A[MT][D / 16][4];
-  load_obs<D, MT>(A, kh, S, w, g, t);
-
-  float rm[MT][2], rz[MT][2];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) rm[mt][0] = rm[mt][1] = ninf(), rz[mt][0] = rz[mt][1] = 0.0f;
-
-  constexpr int kPerWarp = kSnapChunk / 4;
-  const int wbase = chunk * kSnapChunk + warp * kPerWarp;
-  const int ntile = max(0, min(kPerWarp / 8, (S - wbase + 7) / 8));
-  uint32_t Bn[D / 16][2];
-  if (ntile > 0) load_keys<D>(Bn, kh, wbase, S, g, t);
-  for (int tile = 0; tile < ntile; ++tile) {
-    const int key0 = wbase + tile * 8;
-    uint32_t Bc[D / 16][2];
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) Bc[ks][0] = Bn[ks][0], Bc[ks][1] = Bn[ks][1];
-    if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);   // next tile's keys in flight
-    float cacc[MT][4];
-    tile_logits<D, MT>(cacc, A, Bc);
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (key0 + 2 * t + e < S) {
-            const float v = cacc[mt][2 * hf + e] * cscale;
-            const float mn = fmaxf(rm[mt][hf], v);
-            rz[mt][hf] = rz[mt][hf] * exp2f(rm[mt][hf] - mn) + exp2f(v - mn);
-            rm[mt][hf] = mn;
-          }
-        }
-      }
-    }
-  }
-  // merge the 4 lanes that share a row
+// Per-row (max, sum) of this CTA: the 4 lanes sharing a row merge by
+// shuffles, the 4 warps through shared memory; written as stats[r], r < 64.
+template <int MT>
+__device__ __forceinline__ void snap_row_stats(float (&rm)[MT][2], float (&rz)[MT][2], float (*sm_m)[MT * 16],
+                                               float (*sm_z)[MT * 16], float2* stats, int g, int t, int warp) {
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
 #pragma unroll
@@ -174,8 +139,130 @@ __global__ void __launch_bounds__(128) snapkv_stats_kernel(const __half* __restr
         if (sm_m[wi][r] != ninf()) Z += sm_z[wi][r] * exp2f(sm_m[wi][r] - M);
       }
     }
-    stats[(bh * nchunk + chunk) * 64 + r] = make_float2(M, Z);
+    stats[r] = make_float2(M, Z);
   }
+}
+
+// Every chunk's (max, sum) of each observation row merged into the row's max
+// and 1 / sum (rows >= w: 0, 0): TPR adjacent threads per row, each over every
+// TPR-th chunk, then a shuffle merge.  Ends with a barrier.
+template <int MT>
+__device__ __forceinline__ void merge_row_stats(const float2* __restrict__ stats, int nchunk, int w, float* row_m,
+                                                float* row_iz) {
+  constexpr int R = MT * 16;
+  constexpr int TPR = (128 / R) >= 4 ? 4 : ((128 / R) >= 2 ? 2 : 1);
+  const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
+  float M = ninf(), Z = 0.0f;
+  if (r < R && r < w) {
+#pragma unroll 8
+    for (int cch = part; cch < nchunk; cch += TPR) {
+      const float2 st = stats[cch * 64 + r];
+      if (st.x != ninf()) {
+        const float mn = fmaxf(M, st.x);
+        Z = Z * exp2f(M - mn) + st.y * exp2f(st.x - mn);
+        M = mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < TPR; o <<= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, M, o);
+    const float zo = __shfl_xor_sync(0xffffffffu, Z, o);
+    const float mn = fmaxf(M, mo);
+    const float ea = (M == ninf()) ? 0.0f : exp2f(M - mn);
+    const float eb = (mo == ninf()) ? 0.0f : exp2f(mo - mn);
+    Z = Z * ea + zo * eb;
+    M = mn;
+  }
+  if (r < R && part == 0) {
+    const bool live = r < w;
+    row_m[r] = live ? M : 0.0f;
+    row_iz[r] = live ? 1.0f / Z : 0.0f;
+  }
+  __syncthreads();
+}
+
+// score[key] = (1/w) sum_r 2^(logit_r,key - M_r) / Z_r for the tile's 8 keys.
+template <int MT>
+__device__ __forceinline__ void snap_score_tile(const float (&cacc)[MT][4], const float (&Mr)[MT][2],
+                                                const float (&Ir)[MT][2], float cscale, float inv_w,
+                                                float* __restrict__ score_row, int key0, int S, int g, int t) {
+  float col[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        // padded rows carry Ir = 0 and logit 0, contributing exactly 0
+        col[e] += exp2f(cacc[mt][2 * hf + e] * cscale - Mr[mt][hf]) * Ir[mt][hf];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) col[e] += __shfl_xor_sync(0xffffffffu, col[e], o);
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = key0 + 2 * t + e;
+      if (key < S) score_row[key] = col[e] * inv_w;
+    }
+  }
+}
+
+// Pass 1: per-row (max, sum 2^(logit - max)) over this CTA's keys, log2 domain.
+template <int D, int MT>
+__global__ void __launch_bounds__(128) snapkv_stats_kernel(const __half* __restrict__ k, long long head_stride,
+                                                           int Hkv, int S, int w, float cscale, float2* stats,
+                                                           int nchunk) {
+  __shared__ float sm_m[4][MT * 16];
+  __shared__ float sm_z[4][MT * 16];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const size_t bh = (size_t)blockIdx.z * Hkv + blockIdx.y;
+  const int chunk = blockIdx.x;
+  const __half* kh = k + bh * head_stride * D;
+
+  uint32_t A[MT][D / 16][4];
+  load_obs_perm<D, MT>(A, kh, S, w, g, t);
+
+  float rm[MT][2], rz[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) rm[mt][0] = rm[mt][1] = ninf(), rz[mt][0] = rz[mt][1] = 0.0f;
+
+  constexpr int kPerWarp = kSnapChunk / 4;
+  const int wbase = chunk * kSnapChunk + warp * kPerWarp;
+  const int ntile = max(0, min(kPerWarp / 8, (S - wbase + 7) / 8));
+  uint32_t Bn[D / 16][2];
+  if (ntile > 0) load_keys<D>(Bn, kh, wbase, S, g, t);
+  for (int tile = 0; tile < ntile; ++tile) {
+    const int key0 = wbase + tile * 8;
+    uint32_t Bc[D / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) Bc[ks][0] = Bn[ks][0], Bc[ks][1] = Bn[ks][1];
+    if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);   // next tile's keys in flight
+    float cacc[MT][4];
+    tile_logits<D, MT>(cacc, A, Bc);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (key0 + 2 * t + e < S) {
+            const float v = cacc[mt][2 * hf + e] * cscale;
+            const float mn = fmaxf(rm[mt][hf], v);
+            rz[mt][hf] = rz[mt][hf] * exp2f(rm[mt][hf] - mn) + exp2f(v - mn);
+            rm[mt][hf] = mn;
+          }
+        }
+      }
+    }
+  }
+  snap_row_stats<MT>(rm, rz, sm_m, sm_z, stats + (bh * nchunk + chunk) * 64, g, t, warp);
 }
 
 // Pass 2: score[j] = (1/w) sum_r 2^(logit_rj - M_r) / Z_r.
@@ -192,44 +279,10 @@ __global__ void __launch_bounds__(128) snapkv_scores_kernel(const __half* __rest
   const int chunk = blockIdx.x;
   const __half* kh = k + bh * head_stride * D;
 
-  // Merge every chunk's (max, sum) of each observation row: TPR adjacent
-  // threads per row, each over every TPR-th chunk, then a shuffle merge.
-  {
-    constexpr int R = MT * 16;
-    constexpr int TPR = (128 / R) >= 4 ? 4 : ((128 / R) >= 2 ? 2 : 1);
-    const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
-    float M = ninf(), Z = 0.0f;
-    if (r < R && r < w) {
-#pragma unroll 8
-      for (int cch = part; cch < nchunk; cch += TPR) {
-        const float2 st = stats[(bh * nchunk + cch) * 64 + r];
-        if (st.x != ninf()) {
-          const float mn = fmaxf(M, st.x);
-          Z = Z * exp2f(M - mn) + st.y * exp2f(st.x - mn);
-          M = mn;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, M, o);
-      const float zo = __shfl_xor_sync(0xffffffffu, Z, o);
-      const float mn = fmaxf(M, mo);
-      const float ea = (M == ninf()) ? 0.0f : exp2f(M - mn);
-      const float eb = (mo == ninf()) ? 0.0f : exp2f(mo - mn);
-      Z = Z * ea + zo * eb;
-      M = mn;
-    }
-    if (r < R && part == 0) {
-      const bool live = r < w;
-      row_m[r] = live ? M : 0.0f;
-      row_iz[r] = live ? 1.0f / Z : 0.0f;
-    }
-  }
-  __syncthreads();
+  merge_row_stats<MT>(stats + bh * nchunk * 64, nchunk, w, row_m, row_iz);   // ends with __syncthreads
 
   uint32_t A[MT][D / 16][4];
-  load_obs<D, MT>(A, kh, S, w, g, t);
+  load_obs_perm<D, MT>(A, kh, S, w, g, t);
   float Mr[MT][2], Ir[MT][2];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -253,30 +306,7 @@ __global__ void __launch_bounds__(128) snapkv_scores_kernel(const __half* __rest
     if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);   // next tile's keys in flight
     float cacc[MT][4];
     tile_logits<D, MT>(cacc, A, Bc);
-    float col[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          // padded rows carry Ir = 0 and logit 0, contributing exactly 0
-          col[e] += exp2f(cacc[mt][2 * hf + e] * cscale - Mr[mt][hf]) * Ir[mt][hf];
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) col[e] += __shfl_xor_sync(0xffffffffu, col[e], o);
-    }
-    if (g == 0) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = key0 + 2 * t + e;
-        if (key < S) scores[bh * S + key] = col[e] * inv_w;
-      }
-    }
+    snap_score_tile<MT>(cacc, Mr, Ir, cscale, inv_w, scores + bh * S, key0, S, g, t);
   }
 }
 
@@ -451,8 +481,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
 // ---------------------------------------------------------------- launch --
 
 template <int D, int MT>
-static cudaError_t launch_snapkv_dm(const void* k, long long hs, int B, int Hkv, int S, int w, float* scores,
-                                    float2* stats, int nchunk, cudaStream_t st) {
+static cudaError_t launch_snapkv_dm(const void* k, long long hs, int B, int Hkv, int S, int w,
+                                    float* scores, float2* stats, int nchunk, cudaStream_t st) {
   const float cscale = 1.4426950408889634f / sqrtf((float)D);
   const dim3 grid(nchunk, Hkv, B);
   const __half* kk = static_cast<const __half*>(k);
@@ -464,8 +494,8 @@ static cudaError_t launch_snapkv_dm(const void* k, long long hs, int B, int Hkv,
 }
 
 template <int D>
-static cudaError_t launch_snapkv_d(const void* k, long long hs, int B, int Hkv, int S, int w, float* scores,
-                                   float2* stats, int nchunk, cudaStream_t st) {
+static cudaError_t launch_snapkv_d(const void* k, long long hs, int B, int Hkv, int S, int w,
+                                   float* scores, float2* stats, int nchunk, cudaStream_t st) {
   switch ((w + 15) / 16) {
     case 1: return launch_snapkv_dm<D, 1>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);
     case 2: return launch_snapkv_dm<D, 2>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);

@@ -247,7 +247,8 @@ size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int3
    plus the top (budget - n_sink) of the rest by score (equal scores: lower position
    first), ascending.  scores_out: device fp32 [B, Hkv, S] or NULL; idx_out: device
    int32 [B, Hkv, min(budget, S)].  n_sink > budget -> INVALID_ARG.
-   obs_window in 1..64, head_dim in {32, 64, 128}, S >= 1. */
+   obs_window in 1..64, head_dim in {32, 64, 128}, S >= 1; k 8-byte aligned
+   (INVALID_ARG otherwise). */
 kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int32_t n_kv_heads, int32_t S,
                          int32_t head_dim, int32_t obs_window, int32_t budget, int32_t n_sink,
                          float* scores_out, int32_t* idx_out, void* workspace, size_t ws_bytes,
