@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (profiling small footprints; not a bench line)")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the other workloads' summary that a one-GPU run of the default workload adds")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     return a
@@ -729,6 +731,31 @@ def e2e_snapkv(ep, episodes, world, total_b):
                    "inputs copied in and outputs read back every episode (wall clock)"}
 
 
+def per_config(a, kvq):
+    """The other workloads measured in the same run (one GPU, device time only):
+    the metric is quoted per config.  Each entry holds that workload's bench
+    line essentials; a failure is recorded, not raised."""
+    out = {}
+    for name in ("tinygpt", "q4_0_32k", "snapkv", "ring"):
+        w = synth.get_workload(name)
+        sub = argparse.Namespace(**vars(a))
+        sub.steps, sub.warmup, sub.no_e2e = (20, 3, True) if w.batch > 1 or w.prompt_len else (50, 5, True)
+        try:
+            ln = bench_snapkv(sub, kvq, w, 0, 1) if w.prompt_len else bench_decode(sub, kvq, w, 0, 1)
+            r = ln["roofline"]
+            out[w.name] = {"value": ln["value"], "unit": ln["unit"], "ms_per_step": ln["ms_per_step"],
+                           "steps": sub.steps, "decode_steps_per_s": ln.get("decode_steps_per_s"),
+                           "roofline_kernel": r.get("kernel"), "kernel_us": r.get("avg_launch_us"),
+                           "frac": r["frac"], "clocks": ln.get("clocks")}
+            if "snapkv_select_us" in ln:
+                out[w.name]["snapkv_select_us"] = ln["snapkv_select_us"]
+        except Exception as e:  # noqa: BLE001 - the primary line must still print
+            out[w.name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     a = parse_args(argv)
     rank, world, local = dist_env()
@@ -746,6 +773,8 @@ def main(argv=None):
     line = bench_snapkv(a, kvq, w, rank, world) if w.prompt_len else bench_decode(a, kvq, w, rank, world)
     if rank == 0 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, a.cpu_seconds)
+    if world == 1 and not a.no_per_config and a.workload == DEFAULT_WORKLOAD and a.layers == 0:
+        line["per_config"] = per_config(a, kvq)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
