@@ -547,6 +547,8 @@ def bench_decode(a, kvq, w, rank, world):
                      "avg_launch_us": avg_dec_launch_s * 1e6, "peak_kind": f"{peak_kind} copy bandwidth"},
         "clocks": clk,
     }
+    if w.layout == "linear":
+        line["convert"] = bench_convert(kvq, w, device, a.warmup)
     if not a.no_e2e:
         e_bytes, e_dt, h2d, d2h = e2e_decode(ds, max(3, min(a.steps, 200)), world)
         line["e2e"] = {"value": world * e_bytes / e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -631,6 +633,35 @@ class SnapKVEpisode:
         with torch.cuda.graph(self.graph):
             self.launches = self.episode()
         torch.cuda.synchronize()
+
+
+def bench_convert(kvq, w, device, warmup):
+    """Bulk quantise-on-convert of one layer: the context's tokens of a dense cache
+    (the workload's io dtype) into a fresh quantised cache, timed alone."""
+    k, v = synth.layer_inputs(w, 0, 0, w.context, device=device)
+    bias = synth.k_bias(w, 0, device=device) if w.use_k_bias else None
+    cache = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, w.context, w.k_format, w.k_bits, w.k_group,
+                        w.v_format, w.v_bits, w.v_group, k_bias=bias, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    cal = w.k_format == "kivi_chan"
+    reps = 5
+    times = []
+    for i in range(warmup + reps):
+        cache.reset()
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cache.convert(k, v, w.context, calibrate_k=cal)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.median(times)
+    nbytes = append_bytes(w, w.context)
+    if cal:
+        nbytes += w.batch * w.n_kv_heads * w.context * w.head_dim * k.element_size()   # calibration pass over K
+    return {"tokens_per_s": w.batch * w.context / t, "gbs": nbytes / t / 1e9, "us": t * 1e6,
+            "tokens": w.context, "what": "one layer's dense cache, every (batch row, kv head), into a fresh cache"}
 
 
 def bench_snapkv(a, kvq, w, rank, world):
@@ -747,8 +778,9 @@ def per_config(a, kvq):
                            "steps": sub.steps, "decode_steps_per_s": ln.get("decode_steps_per_s"),
                            "roofline_kernel": r.get("kernel"), "kernel_us": r.get("avg_launch_us"),
                            "frac": r["frac"], "clocks": ln.get("clocks")}
-            if "snapkv_select_us" in ln:
-                out[w.name]["snapkv_select_us"] = ln["snapkv_select_us"]
+            for key in ("snapkv_select_us", "convert"):
+                if key in ln:
+                    out[w.name][key] = ln[key]
         except Exception as e:  # noqa: BLE001 - the primary line must still print
             out[w.name] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.synchronize()

@@ -79,6 +79,7 @@ _proto("kvq_cache_layout_query", c_int32, POINTER(kvq_config), POINTER(kvq_cache
 _proto("kvq_cache_init", c_int32, POINTER(kvq_config), c_void_p, c_size_t, c_void_p, POINTER(c_void_p))
 _proto("kvq_cache_release", None, c_void_p)
 _proto("kvq_append", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p)
+_proto("kvq_convert", c_int32, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32, c_void_p)
 _proto("kvq_evict", c_int32, c_void_p, c_int32, c_void_p, c_int32, c_void_p)
 _proto("kvq_decode_workspace_bytes", c_size_t, c_void_p, c_int32)
 _proto("kvq_decode_attn", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p, c_size_t,
@@ -155,6 +156,12 @@ def kvq_cache_init(cfg: kvq_config, buf: torch.Tensor, stream=None) -> c_void_p:
 def kvq_append(cache, k: torch.Tensor, v: torch.Tensor, n_tokens: int, in_dtype: int, flags: int = 0,
                stream=None) -> None:
     _check(lib.kvq_append(cache, _dev_ptr(k), _dev_ptr(v), n_tokens, in_dtype, flags, _stream(stream)))
+
+
+def kvq_convert(cache, k: torch.Tensor, v: torch.Tensor, head_stride: int, n_tokens: int, in_dtype: int,
+                flags: int = 0, stream=None) -> None:
+    _check(lib.kvq_convert(cache, _dev_ptr(k), _dev_ptr(v), head_stride, n_tokens, in_dtype, flags,
+                           _stream(stream)))
 
 
 def kvq_evict(cache, mode: int, keep_idx: Optional[torch.Tensor] = None, n_keep: int = 0, stream=None) -> None:
@@ -239,6 +246,16 @@ class KVCache:
     def append(self, k: torch.Tensor, v: torch.Tensor, calibrate_k: bool = False, stream=None) -> None:
         n = k.shape[2]
         kvq_append(self.handle, k, v, n, DTYPES[k.dtype], APPEND_CALIBRATE_K if calibrate_k else 0, stream)
+        self.launches += kvq_last_launch_count()
+
+    def convert(self, k: torch.Tensor, v: torch.Tensor, n_tokens: int, calibrate_k: bool = False,
+                stream=None) -> None:
+        """Quantises the first n_tokens tokens of a dense cache k, v [B, Hkv, C, D] (C >= n_tokens,
+        rows contiguous) into this cache."""
+        if k.shape != v.shape or k.dim() != 4 or not k.is_contiguous() or not v.is_contiguous():
+            raise ValueError("k and v must be contiguous [B, Hkv, C, D] tensors of one shape")
+        kvq_convert(self.handle, k, v, k.shape[2], n_tokens, DTYPES[k.dtype],
+                    APPEND_CALIBRATE_K if calibrate_k else 0, stream)
         self.launches += kvq_last_launch_count()
 
     def evict_middle(self, stream=None) -> None:

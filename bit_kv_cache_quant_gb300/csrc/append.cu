@@ -15,8 +15,10 @@ namespace kvq {
 // Per-channel K calibration: min / max over the n tokens of one (b, kv head),
 // then the fp32 scale / zero that codes are computed from and their fp16
 // stored copies.  One CTA of 256 threads per (b, kv head); 256 % D == 0.
+// Token t of (b, kv head) bh is row bh * hstride + t of k.
 template <typename T>
-__global__ void __launch_bounds__(256) calibrate_kivi_kernel(CacheView c, const T* __restrict__ k, int n) {
+__global__ void __launch_bounds__(256) calibrate_kivi_kernel(CacheView c, const T* __restrict__ k, int n,
+                                                             long long hstride) {
   __shared__ float smn[256];
   __shared__ float smx[256];
   const int D = c.D;
@@ -27,7 +29,7 @@ __global__ void __launch_bounds__(256) calibrate_kivi_kernel(CacheView c, const 
   const int ntg = blockDim.x / D;
   float mn = __int_as_float(0x7f800000);   // +inf
   float mx = __int_as_float(0xff800000);   // -inf
-  const T* base = k + (size_t)bh * n * D;
+  const T* base = k + (size_t)bh * hstride * D;
   for (int t = tg; t < n; t += ntg) {
     float x = In<T>::ld(base + (size_t)t * D + d);
     mn = fminf(mn, x);
@@ -175,7 +177,8 @@ constexpr int kAppendWarps = 8;
 
 template <typename T, int E>
 __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, const T* __restrict__ k,
-                                                                    const T* __restrict__ v, int n, long long rows) {
+                                                                    const T* __restrict__ v, int n, long long rows,
+                                                                    long long hstride) {
   __shared__ long long s_pos;
   __shared__ int s_stored;
   __shared__ int s_ok;
@@ -184,8 +187,10 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
   const long long row = (long long)blockIdx.x * kAppendWarps + warp;
   float xk[E], xv[E];
   if (row < rows) {
-    load_row_slice<T, E>(k + row * c.D + lane * E, xk);
-    load_row_slice<T, E>(v + row * c.D + lane * E, xv);
+    // token row % n of (b, kv head) row / n sits at row (row / n) * hstride + row % n of the input
+    const long long src = (row / n) * hstride + row % n;
+    load_row_slice<T, E>(k + src * c.D + lane * E, xk);
+    load_row_slice<T, E>(v + src * c.D + lane * E, xv);
   }
   if (threadIdx.x == 0) {
     s_pos = c.state->pos;
@@ -247,10 +252,10 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
 // ---------------------------------------------------------------- launch --
 
 template <typename T>
-static cudaError_t launch_append_t(const CacheView& c, const void* k, const void* v, int n, bool calibrate,
-                                   cudaStream_t st) {
+static cudaError_t launch_append_t(const CacheView& c, const void* k, const void* v, int n, long long hstride,
+                                   bool calibrate, cudaStream_t st) {
   if (calibrate) {
-    calibrate_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n);
+    calibrate_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n, hstride);
     note_launch();
   }
   const long long rows = (long long)c.B * c.Hkv * n;
@@ -258,21 +263,21 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
   const T* kk = static_cast<const T*>(k);
   const T* vv = static_cast<const T*>(v);
   switch (c.D) {
-    case 32: append_kernel<T, 1><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
-    case 64: append_kernel<T, 2><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
-    case 128: append_kernel<T, 4><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows); break;
+    case 32: append_kernel<T, 1><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
+    case 64: append_kernel<T, 2><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
+    case 128: append_kernel<T, 4><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
     default: return cudaErrorInvalidValue;
   }
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, int in_dtype, bool calibrate,
-                          cudaStream_t st) {
+cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, long long hstride, int in_dtype,
+                          bool calibrate, cudaStream_t st) {
   switch (in_dtype) {
-    case KVQ_DTYPE_F32: return launch_append_t<float>(c, k, v, n, calibrate, st);
-    case KVQ_DTYPE_BF16: return launch_append_t<__nv_bfloat16>(c, k, v, n, calibrate, st);
-    case KVQ_DTYPE_F16: return launch_append_t<__half>(c, k, v, n, calibrate, st);
+    case KVQ_DTYPE_F32: return launch_append_t<float>(c, k, v, n, hstride, calibrate, st);
+    case KVQ_DTYPE_BF16: return launch_append_t<__nv_bfloat16>(c, k, v, n, hstride, calibrate, st);
+    case KVQ_DTYPE_F16: return launch_append_t<__half>(c, k, v, n, hstride, calibrate, st);
     default: return cudaErrorInvalidValue;
   }
 }

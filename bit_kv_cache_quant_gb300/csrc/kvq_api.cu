@@ -336,12 +336,14 @@ kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cu
 
 void kvq_cache_release(kvq_cache cache) { delete cache; }
 
-kvq_status kvq_append(kvq_cache c, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype, int32_t flags,
-                      cudaStream_t stream) {
-  begin_call();
+namespace {
+
+kvq_status append_rows(kvq_cache c, const void* k, const void* v, int64_t head_stride, int32_t n_tokens,
+                       int32_t in_dtype, int32_t flags, cudaStream_t stream, const char* what) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "null cache");
   if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "null k or v");
   if (n_tokens < 1) return fail(KVQ_ERR_INVALID_ARG, "n_tokens must be >= 1");
+  if (head_stride < n_tokens) return fail(KVQ_ERR_INVALID_ARG, "head_stride must be >= n_tokens");
   if (!valid_dtype(in_dtype)) return fail(KVQ_ERR_INVALID_ARG, "unknown input dtype %d", in_dtype);
   if (flags & ~KVQ_APPEND_CALIBRATE_K) return fail(KVQ_ERR_INVALID_ARG, "unknown append flags 0x%x", flags);
   const bool calibrate = (flags & KVQ_APPEND_CALIBRATE_K) != 0;
@@ -351,10 +353,24 @@ kvq_status kvq_append(kvq_cache c, const void* k, const void* v, int32_t n_token
     return fail(KVQ_ERR_UNSUPPORTED, "per-channel K scales are not calibrated yet (pass KVQ_APPEND_CALIBRATE_K)");
   if (c->cfg.layout != KVQ_LAYOUT_RING && n_tokens > c->cfg.capacity)
     return fail(KVQ_ERR_CAPACITY, "append of %d tokens exceeds capacity %d", n_tokens, c->cfg.capacity);
-  cudaError_t e = kvq::launch_append(c->view, k, v, n_tokens, in_dtype, calibrate, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "kvq_append");
+  cudaError_t e = kvq::launch_append(c->view, k, v, n_tokens, head_stride, in_dtype, calibrate, stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
   if (calibrate) c->k_calibrated = true;
   return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kvq_append(kvq_cache c, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype, int32_t flags,
+                      cudaStream_t stream) {
+  begin_call();
+  return append_rows(c, k, v, n_tokens, n_tokens, in_dtype, flags, stream, "kvq_append");
+}
+
+kvq_status kvq_convert(kvq_cache c, const void* k, const void* v, int64_t head_stride, int32_t n_tokens,
+                       int32_t in_dtype, int32_t flags, cudaStream_t stream) {
+  begin_call();
+  return append_rows(c, k, v, head_stride, n_tokens, in_dtype, flags, stream, "kvq_convert");
 }
 
 kvq_status kvq_evict(kvq_cache c, int32_t mode, const int32_t* keep_idx, int32_t n_keep, cudaStream_t stream) {

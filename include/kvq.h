@@ -187,6 +187,18 @@ void kvq_cache_release(kvq_cache cache);
 kvq_status kvq_append(kvq_cache cache, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype,
                       int32_t flags, cudaStream_t stream);
 
+/* Bulk quantise-on-convert ([MLX] section 1: an existing full-precision cache is
+   turned into a quantised one in one pass once the context is long enough).
+   k, v: a dense cache the caller already holds, device f32 / bf16 / fp16 by
+   in_dtype, token t of (b, kv head) at row (b*Hkv + h)*head_stride + t, rows of D
+   elements (head_stride >= n_tokens: a dense cache with spare capacity).  The
+   first n_tokens tokens of every (b, kv head) are coded exactly as kvq_append
+   would code the same tokens given contiguously (same flags, same counters);
+   the source is only read.  head_stride < n_tokens -> INVALID_ARG; other errors as
+   kvq_append. */
+kvq_status kvq_convert(kvq_cache cache, const void* k, const void* v, int64_t head_stride, int32_t n_tokens,
+                       int32_t in_dtype, int32_t flags, cudaStream_t stream);
+
 /* KVQ_EVICT_MIDDLE ([SLK] "Implementation"): when stored > sink + window, drop
    logical [sink, stored - window).  COMPACT moves the window rows (codes and
    per-token metadata) down; RING needs no data movement and enqueues nothing;

@@ -192,3 +192,41 @@ def test_bad_keepset_sets_status(kvq):
     idx = torch.tensor([[[0, 5, 5, 9]]], dtype=torch.int32, device="cuda")     # not strictly ascending
     cache.evict_keepset(idx)
     assert gpu_planes(cache)["status"] == kvq.DEV_BAD_KEEPSET
+
+
+@pytest.mark.parametrize("fmt", FORMATS, ids=lambda f: f"{f[0]}{f[1]}-{f[3]}{f[4]}g{f[5]}")
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_convert_from_dense_cache(kvq, fmt, dtype):
+    """kvq_convert codes the first T tokens of a dense [B, Hkv, C, D] cache exactly as an
+    append of those tokens would; rows past T (huge values here) are never read."""
+    kf, kb, kg, vf, vb, vg = fmt
+    D, B, H, C, T = 128, 2, 3, 300, 233
+    kg, vg = _clip(D, kg), _clip(D, vg)
+    bias = None
+    if kf == "q4_0":
+        bias = (torch.randn(H, D, generator=torch.Generator().manual_seed(5)) * 1.5).float()
+    k = _inputs((B, H, C, D), 31, dtype)
+    v = _inputs((B, H, C, D), 32, dtype, 0.0)
+    k[:, :, T:] = 3.0e4
+    v[:, :, T:] = -3.0e4
+    cache = kvq.KVCache(B, H, D, T + 8, kf, kb, kg, vf, vb, vg, k_bias=None if bias is None else bias.cuda())
+    oc = OracleCache(oracle_spec(cache, None if bias is None else bias.numpy()))
+    calibrate = kf == "kivi_chan"
+    cache.convert(k.cuda(), v.cuda(), T, calibrate_k=calibrate)
+    kt, vt = k[:, :, :T].contiguous(), v[:, :, :T].contiguous()
+    if calibrate:
+        oc.calibrate_k(host(kt))
+    oc.append(host(kt), host(vt))
+    assert_cache_equal(cache, oc, "convert")
+    # the converted cache keeps appending like any other
+    k2, v2 = _inputs((B, H, 3, D), 33, dtype), _inputs((B, H, 3, D), 34, dtype, 0.0)
+    cache.append(k2.cuda(), v2.cuda())
+    oc.append(host(k2), host(v2))
+    assert_cache_equal(cache, oc, "append after convert")
+
+
+def test_convert_rejects_short_stride(kvq):
+    cache = kvq.KVCache(1, 2, 64, 32, "affine_token", 8, 64, "affine_token", 8, 64)
+    k = torch.zeros((1, 2, 10, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_convert(cache.handle, k, k, 8, 10, kvq.DTYPES[torch.float16])
