@@ -10,6 +10,14 @@ exactly min(budget, S) indices come back, budget >= S keeps everything.
 
 Readings where the page is silent: no causal mask (the formula prints
 none); equal scores are ordered by the lower position first.
+
+Variants the page lists ("Proxy limitation", "Evidence"): the SnapKV paper's
+max-pool smoothing of the scores, which the page leaves out (reading: an odd
+window centred on each position, clipped at the ends, applied to all
+positions before the sink-forced selection); chunked prefill, where each new
+chunk is appended to the kept rows and the whole is selected down to the
+budget again; and the attention coverage of a kept set (its share of the
+score mass) against a random set of the same size.
 """
 from __future__ import annotations
 
@@ -73,3 +81,32 @@ def keepset_gather(rows: np.ndarray, idx: np.ndarray) -> np.ndarray:
         for h in range(H):
             out[b, h] = rows[b, h, idx[b, h]]
     return out
+
+
+def max_pool(scores: np.ndarray, kernel_size: int) -> np.ndarray:
+    """out[j] = max(scores[max(0, j - r) : min(S, j + r + 1)]) with r = kernel_size // 2 (odd kernel)."""
+    if kernel_size < 1 or kernel_size % 2 == 0:
+        raise ValueError("kernel_size must be odd and >= 1")
+    scores = np.asarray(scores)
+    S = scores.shape[-1]
+    r = kernel_size // 2
+    out = np.empty_like(scores)
+    for j in range(S):
+        out[..., j] = scores[..., max(0, j - r): min(S, j + r + 1)].max(axis=-1)
+    return out
+
+
+def coverage(scores: np.ndarray, idx: np.ndarray) -> float:
+    """Share of one head's score mass [S] held by the kept positions idx."""
+    scores = np.asarray(scores, dtype=np.float64)
+    return float(scores[np.asarray(idx)].sum() / scores.sum())
+
+
+def random_coverage(scores: np.ndarray, budget: int, n_sink: int) -> float:
+    """Expected coverage of the sinks plus (budget - n_sink) positions drawn uniformly from the rest."""
+    scores = np.asarray(scores, dtype=np.float64)
+    S = scores.shape[0]
+    if budget >= S:
+        return 1.0
+    ns = min(n_sink, S)
+    return float((scores[:ns].sum() + (budget - ns) / (S - ns) * scores[ns:].sum()) / scores.sum())

@@ -177,3 +177,39 @@ def test_keepset_gather_order():
     idx = np.array([[[0, 4, 9]] * 3] * 2)
     out = sk.keepset_gather(rows, idx)
     np.testing.assert_array_equal(out[1, 2], rows[1, 2, [0, 4, 9]])
+
+
+# ---- variants: max-pool smoothing, coverage --------------------------------
+
+@pytest.mark.parametrize("k", [1, 3, 5, 7])
+def test_max_pool_matches_torch_max_pool1d(k):
+    rng = np.random.default_rng(20 + k)
+    s = rng.random((2, 3, 41))
+    ref = torch.nn.functional.max_pool1d(torch.from_numpy(s).reshape(6, 1, 41), k, stride=1, padding=k // 2)
+    np.testing.assert_array_equal(sk.max_pool(s, k), ref.reshape(2, 3, 41).numpy())
+
+
+def test_max_pool_identity_spike_and_bounds():
+    rng = np.random.default_rng(21)
+    s = rng.random(30) * 1e-3
+    np.testing.assert_array_equal(sk.max_pool(s, 1), s)
+    s[10] = 1.0
+    p = sk.max_pool(s, 5)
+    assert np.all(p >= s)
+    assert np.all(p[8:13] == 1.0) and p[7] < 1.0 and p[13] < 1.0
+    with pytest.raises(ValueError):
+        sk.max_pool(s, 4)
+
+
+def test_coverage_and_random_baseline():
+    s = np.array([0.4, 0.1, 0.1, 0.1, 0.1, 0.1, 0.1])
+    assert sk.coverage(s, [0, 1, 2]) == pytest.approx(0.6)
+    # sinks {0} plus 2 of the 6 others drawn uniformly: 0.4 + 2/6 * 0.6
+    assert sk.random_coverage(s, 3, 1) == pytest.approx(0.6)
+    assert sk.random_coverage(s, 7, 1) == 1.0
+    # planted scores: the top-k keeps more mass than a random set of the same size
+    rng = np.random.default_rng(22)
+    sc = rng.random(500) * 1e-4
+    sc[[50, 90, 300]] = 0.3
+    idx = sk.select_indices(sc, 20, 4)
+    assert sk.coverage(sc, idx) > sk.random_coverage(sc, 20, 4) + 0.5
