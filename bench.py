@@ -701,6 +701,11 @@ def bench_snapkv(a, kvq, w, rank, world):
     t_sel = sum(s_.elapsed_time(e_) for s_, e_ in sel_ev) / 1e3 / a.steps
     peak, peak_kind = read_peaks()
     achieved = sel_b / t_sel / 1e9
+    from oracle import snapkv as osk   # host arithmetic on the device's scores and indices
+
+    sc, ix = ep.scores.double().cpu().numpy(), ep.idx.cpu().numpy()
+    cov = [osk.coverage(sc[b, h], ix[b, h]) for b in range(ep.B) for h in range(ep.H)]
+    rnd = [osk.random_coverage(sc[b, h], w.budget, w.n_sink) for b in range(ep.B) for h in range(ep.H)]
     line = {"metric": METRIC, "value": world * total_b * a.steps / t / 1e9, "unit": "GB/s", "n_gpus": world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": t * 1e3 / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
@@ -712,6 +717,9 @@ def bench_snapkv(a, kvq, w, rank, world):
                        "l2": "flushed (256 MiB write) after the prompt fill, before each timed episode",
                        "parallelism": f"replicas x{world}"},
             "snapkv_select_us": t_sel * 1e6,
+            "coverage": {"kept": sum(cov) / len(cov), "random_same_size": sum(rnd) / len(rnd),
+                         "what": "share of the observation-window score mass held by the kept rows, mean over "
+                                 "heads, against sinks plus a uniformly random set of the same size"},
             "decode_steps_per_s": world * w.decode_steps * a.steps / t,
             "gpu_launches": ep.launches * a.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

@@ -85,6 +85,7 @@ _proto("kvq_decode_workspace_bytes", c_size_t, c_void_p, c_int32)
 _proto("kvq_decode_attn", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p, c_size_t,
        c_void_p)
 _proto("snapkv_workspace_bytes", c_size_t, c_int32, c_int32, c_int32, c_int32, c_int32)
+_proto("snapkv_pool", c_int32, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p)
 _proto("snapkv_select", c_int32, c_void_p, c_int64, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32,
        c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
 _proto("snapkv_topk", c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p)
@@ -189,6 +190,13 @@ def snapkv_select(k: torch.Tensor, head_stride: int, batch: int, n_kv_heads: int
     _check(lib.snapkv_select(_dev_ptr(k), head_stride, batch, n_kv_heads, S, head_dim, obs_window, budget, n_sink,
                              _dev_ptr(scores_out), _dev_ptr(idx_out), _dev_ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def snapkv_pool(scores: torch.Tensor, pooled: torch.Tensor, kernel_size: int, stream=None) -> torch.Tensor:
+    """Max-pool smoothing of scores [B, Hkv, S] (fp32, device) into pooled (same shape)."""
+    B, H, S = scores.shape
+    _check(lib.snapkv_pool(_dev_ptr(scores), _dev_ptr(pooled), B, H, S, kernel_size, _stream(stream)))
+    return pooled
 
 
 def snapkv_topk(scores: torch.Tensor, batch: int, n_kv_heads: int, S: int, budget: int, n_sink: int,

@@ -480,6 +480,19 @@ kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int3
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "snapkv_select");
 }
 
+kvq_status snapkv_pool(const float* scores, float* pooled, int32_t batch, int32_t n_kv_heads, int32_t S,
+                       int32_t kernel_size, cudaStream_t stream) {
+  begin_call();
+  if (!scores || !pooled) return fail(KVQ_ERR_INVALID_ARG, "null scores or pooled");
+  if (batch < 1 || n_kv_heads < 1 || S < 1) return fail(KVQ_ERR_INVALID_ARG, "batch, n_kv_heads, S must be >= 1");
+  if (kernel_size < 1 || kernel_size % 2 == 0 || kernel_size > 63)
+    return fail(KVQ_ERR_INVALID_ARG, "kernel_size must be odd, 1..63 (got %d)", kernel_size);
+  const size_t n = (size_t)batch * n_kv_heads * S;
+  if (scores < pooled + n && pooled < scores + n) return fail(KVQ_ERR_INVALID_ARG, "scores and pooled overlap");
+  const cudaError_t e = kvq::launch_snapkv_pool(scores, pooled, batch * n_kv_heads, S, kernel_size, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "snapkv_pool");
+}
+
 kvq_status snapkv_topk(const float* scores, int32_t batch, int32_t n_kv_heads, int32_t S, int32_t budget,
                        int32_t n_sink, int32_t* idx_out, cudaStream_t stream) {
   begin_call();

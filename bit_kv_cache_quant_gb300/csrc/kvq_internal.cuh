@@ -154,6 +154,8 @@ cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaSt
 
 cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, int S, int D, int w, int budget,
                           int n_sink, float* scores, int* idx, float2* stats, int nchunk, cudaStream_t st);
+// Max-pool smoothing of [BH][S] scores, odd kernel_size <= 63, in != out.
+cudaError_t launch_snapkv_pool(const float* in, float* out, int BH, int S, int kernel_size, cudaStream_t st);
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
                         cudaStream_t st);
 

@@ -478,6 +478,44 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
   }
 }
 
+// ------------------------------------------------------------ smoothing --
+// The SnapKV paper's max-pool smoothing of the scores (the page leaves it out,
+// "Proxy limitation"): out[j] = max of in[j - r .. j + r] clipped to [0, S),
+// r = kernel_size / 2.  One CTA of 256 threads per 256 positions of one
+// (b, kv head), with the positions and an r-wide halo on each side staged in
+// shared memory.
+
+constexpr int kPoolTile = 256;
+constexpr int kPoolMaxR = 31;
+
+__global__ void __launch_bounds__(kPoolTile) snapkv_pool_kernel(const float* __restrict__ in,
+                                                                float* __restrict__ out, int S, int r) {
+  __shared__ float tile[kPoolTile + 2 * kPoolMaxR];
+  const size_t bh = blockIdx.y;
+  const int j0 = blockIdx.x * kPoolTile;
+  const float* row = in + bh * S;
+  for (int i = threadIdx.x; i < kPoolTile + 2 * r; i += kPoolTile) {
+    const int j = j0 - r + i;
+    tile[i] = (j >= 0 && j < S) ? row[j] : ninf();
+  }
+  __syncthreads();
+  const int j = j0 + threadIdx.x;
+  if (j < S) {
+    float m = tile[threadIdx.x];
+    for (int i = 1; i <= 2 * r; ++i) m = fmaxf(m, tile[threadIdx.x + i]);
+    out[bh * S + j] = m;
+  }
+}
+
+cudaError_t launch_snapkv_pool(const float* in, float* out, int BH, int S, int kernel_size, cudaStream_t st) {
+  const int r = kernel_size / 2;
+  if (r > kPoolMaxR) return cudaErrorInvalidValue;
+  const dim3 grid((S + kPoolTile - 1) / kPoolTile, BH);
+  snapkv_pool_kernel<<<grid, kPoolTile, 0, st>>>(in, out, S, r);
+  note_launch();
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- launch --
 
 template <int D, int MT>

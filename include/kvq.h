@@ -266,6 +266,15 @@ kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int3
                          float* scores_out, int32_t* idx_out, void* workspace, size_t ws_bytes,
                          cudaStream_t stream);
 
+/* Max-pool smoothing of SnapKV scores, the SnapKV paper's step that [SKV] "Proxy
+   limitation" says the page leaves out: pooled[b,h,j] = max of scores[b,h,i] over
+   i in [j - r, j + r] clipped to [0, S), r = kernel_size / 2.  scores, pooled: device
+   fp32 [B, Hkv, S], not overlapping.  Compose snapkv_select (scores_out) ->
+   snapkv_pool -> snapkv_topk to select on smoothed scores (sinks still forced).
+   kernel_size odd in 1..63, else INVALID_ARG. */
+kvq_status snapkv_pool(const float* scores, float* pooled, int32_t batch, int32_t n_kv_heads, int32_t S,
+                       int32_t kernel_size, cudaStream_t stream);
+
 /* The selection step of snapkv_select alone, on caller-given fp32 scores
    [B, Hkv, S] (device), with the same rule.  Needs no workspace. */
 kvq_status snapkv_topk(const float* scores, int32_t batch, int32_t n_kv_heads, int32_t S, int32_t budget,

@@ -127,3 +127,101 @@ def test_select_on_cache_rows_with_head_stride(kvq):
     kvq.snapkv_select(kplane, cache.layout.cap_alloc, B, H, S, D, 32, 100, 4, None, idx, ws)
     _, ref = kvq.snapkv(k.cuda(), 32, 100, 4)
     assert torch.equal(idx, ref)
+
+
+# ---- variants: max-pool smoothing, chunked prefill ---------------------------
+
+@pytest.mark.parametrize("S,ksize", [(1, 1), (17, 3), (300, 5), (1000, 7), (5000, 63), (257, 9)])
+def test_pool_matches_oracle(kvq, S, ksize):
+    rng = np.random.default_rng(S + ksize)
+    scores = (rng.random((2, 3, S)) * 1e-3).astype(np.float32)
+    scores[:, :, rng.integers(0, S, size=min(S, 9))] = 0.5
+    got = torch.empty((2, 3, S), dtype=torch.float32, device="cuda")
+    kvq.snapkv_pool(torch.from_numpy(scores).cuda(), got, ksize)
+    np.testing.assert_array_equal(got.cpu().numpy(), osk.max_pool(scores, ksize))
+
+
+def test_pool_rejects_even_kernel_and_overlap(kvq):
+    s = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(kvq.KvqError):
+        kvq.snapkv_pool(s, torch.empty_like(s), 4)
+    with pytest.raises(kvq.KvqError):
+        kvq.snapkv_pool(s, s, 3)
+
+
+def test_select_on_pooled_scores(kvq):
+    # snapkv_select -> snapkv_pool -> snapkv_topk equals the oracle's selection on the pooled fp32 scores
+    B, H, S, D, w, budget, ns = 1, 4, 3000, 128, 32, 256, 4
+    k = _keys(B, H, S, D, seed=77)
+    scores, _ = kvq.snapkv(k.cuda(), w, budget, ns)
+    pooled = torch.empty_like(scores)
+    kvq.snapkv_pool(scores, pooled, 7)
+    idx = torch.empty((B, H, budget), dtype=torch.int32, device="cuda")
+    kvq.snapkv_topk(pooled, B, H, S, budget, ns, idx)
+    p = pooled.cpu().numpy()
+    np.testing.assert_array_equal(p, osk.max_pool(scores.cpu().numpy(), 7))
+    for h in range(H):
+        np.testing.assert_array_equal(idx.cpu().numpy()[0, h], osk.select_indices(p[0, h], budget, ns))
+
+
+def _assert_valid_topk(ig, ref, eps, budget, n_sink):
+    """ig is the exact top-k of ref when the cutoff gap exceeds 2 eps, else a valid one within eps."""
+    S = len(ref)
+    ns = min(n_sink, S)
+    rest = np.sort(ref[ns:])[::-1]
+    kk = budget - ns
+    gap = rest[kk - 1] - rest[kk] if 0 < kk < len(rest) else np.inf
+    if gap > 2 * eps:
+        np.testing.assert_array_equal(ig, osk.select_indices(ref, budget, n_sink))
+        return
+    sel = set(ig.tolist())
+    assert set(range(ns)) <= sel and len(sel) == budget
+    cut = rest[kk - 1]
+    for j in range(ns, S):
+        if ref[j] > cut + 2 * eps:
+            assert j in sel
+        if ref[j] < cut - 2 * eps:
+            assert j not in sel
+
+
+def test_chunked_prefill_reenforces_budget(kvq):
+    """Prefill in chunks: each chunk is appended to the kept rows, and when the cache holds more
+    than the budget it is scored (the chunk's last w keys as proxies, read in place from the
+    cache's fp16 K plane) and gathered back down to the budget.  Stored rows stay capped at the
+    budget while the absolute position counts every prompt token."""
+    from kvq_helpers import assert_cache_equal, host, oracle_spec
+    from oracle.cache import OracleCache
+
+    B, H, D, w, budget, ns = 1, 2, 64, 8, 48, 4
+    chunks = [40, 30, 25, 50, 7, 64]
+    cap = budget + max(chunks)
+    cache = kvq.KVCache(B, H, D, cap, "fp16", 16, 0, "fp16", 16, 0)
+    oc = OracleCache(oracle_spec(cache, None))
+    ca = cache.layout.cap_alloc
+    ws = torch.empty(kvq.snapkv_workspace_bytes(B, H, cap, D, w), dtype=torch.uint8, device="cuda")
+    kplane = cache.plane("k_codes", B * H * ca * 2 * D).view(torch.float16)
+    pos = 0
+    for i, n in enumerate(chunks):
+        k = _keys(B, H, n, D, seed=100 + i, sink_rows=4 if i == 0 else 0)
+        v = _keys(B, H, n, D, seed=200 + i, sink_rows=0)
+        cache.append(k.cuda(), v.cuda())
+        oc.append(host(k), host(v))
+        pos += n
+        stored = oc.stored
+        if stored > budget:
+            idx = torch.empty((B, H, budget), dtype=torch.int32, device="cuda")
+            scores = torch.empty((B, H, stored), dtype=torch.float32, device="cuda")
+            kvq.snapkv_select(kplane, ca, B, H, stored, D, w, budget, ns, scores, idx, ws)
+            kh, _ = oc.dequant()
+            ig, sg = idx.cpu().numpy(), scores.cpu().numpy().astype(np.float64)
+            for h in range(H):
+                ref = osk.obs_window_scores(kh[0, h], w)
+                eps = np.abs(sg[0, h] - ref).max()
+                assert eps <= 1e-5 * ref.max() + 1e-9
+                _assert_valid_topk(ig[0, h], ref, eps, budget, ns)
+            cache.evict_keepset(idx)
+            oc.evict_keepset(ig)    # the validated GPU choice, so both caches stay identical
+        st = cache.stats()
+        assert st.stored == oc.stored == min(stored, budget)
+        assert st.pos == pos
+        assert_cache_equal(cache, oc, f"chunk {i}")
