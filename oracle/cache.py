@@ -198,6 +198,35 @@ class OracleCache:
                     side.tok_zero[:, :, slot] = zr[:, :, i]
         self.pos += n
 
+    def append_recompute_k(self, k: np.ndarray, v: np.ndarray):
+        """Append with the per-channel K range recomputed ("StreamingLLM + KIVI", "KIVI" and
+        "Caveats": the range may shift with every new token, so the whole K block is coded
+        again; O(T D) per append).  Reading: the stored keys are dequantised in fp32 from the
+        stored fp16 scale and zero (the page casts them to fp32 before dequantising), u * s
+        then + z, each rounded once; the range is taken over those values and the new keys;
+        every stored key is coded again against the new fp32 scale and zero, and the new
+        tokens are appended with them.  KIVI per-channel keys, linear or compact layouts."""
+        spec = self.spec
+        if spec.k_format != "kivi_chan" or spec.layout == "ring":
+            raise ValueError("recompute-on-append needs kivi_chan keys and a linear or compact layout")
+        k = np.asarray(k, np.float32)
+        n_old = self.stored
+        if n_old + k.shape[2] > spec.capacity:
+            raise OverflowError("append beyond capacity")
+        if n_old > 0:
+            u = self.k.codes(n_old).astype(np.float32)
+            s16 = self.k.ch_scale.astype(np.float32)[:, :, None, :]
+            z16 = self.k.ch_zero.astype(np.float32)[:, :, None, :]
+            x_old = (u * s16).astype(np.float32) + z16            # two fp32 roundings
+            allx = np.concatenate([x_old, k], axis=2)
+        else:
+            x_old, allx = None, k
+        self.k.calibrate(allx)
+        if n_old > 0:
+            self.k.rows[:, :, :n_old] = self.k._pack(
+                qz.kivi_channel_codes(x_old, self.k.ch_scale32, self.k.ch_zero32, self.k.bits))
+        self.append(k, v)
+
     def evict_middle(self):
         """StreamingLLM: drop logical [sink, len - window) when len > sink + window."""
         spec = self.spec

@@ -201,3 +201,80 @@ def test_decode_read_bytes_of_the_workloads():
     assert acc.decode_read_bytes(1, 8, 24, 128, 8192, "affine_token", 4, 64, "affine_token", 4, 64, 2) == 9449472
     assert acc.decode_read_bytes(8, 8, 32, 128, 32768, "q4_0", 4, 32, "affine_token", 8, 128, 2) == 427950080
     assert acc.decode_read_bytes(64, 8, 32, 128, 4100, "kivi_chan", 4, 0, "affine_token", 4, 32, 2) == 303595520
+
+
+# ---- recompute-on-append K scales ("KIVI", "Caveats") ------------------------
+
+def _kivi_cache(bits, cap=200, layout="linear", D=16, H=2):
+    return OracleCache(CacheSpec(batch=1, n_kv_heads=H, head_dim=D, capacity=cap, layout=layout,
+                                 sink=4 if layout == "compact" else 0, window=64 if layout == "compact" else 0,
+                                 k_format="kivi_chan", k_bits=bits, k_group=0,
+                                 v_format="affine_token", v_bits=bits, v_group=D))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_recompute_first_append_equals_calibrated_append(bits):
+    rng = np.random.default_rng(40 + bits)
+    k = (rng.standard_normal((1, 2, 30, 16)) * 2).astype(np.float32)
+    v = rng.standard_normal((1, 2, 30, 16)).astype(np.float32)
+    a, b = _kivi_cache(bits), _kivi_cache(bits)
+    a.append_recompute_k(k, v)
+    b.calibrate_k(k)
+    b.append(k, v)
+    np.testing.assert_array_equal(a.k.rows, b.k.rows)
+    np.testing.assert_array_equal(a.k.ch_scale, b.k.ch_scale)
+    np.testing.assert_array_equal(a.k.ch_zero, b.k.ch_zero)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_recompute_recodes_to_nearest_level_without_clamping(bits):
+    rng = np.random.default_rng(50 + bits)
+    c = _kivi_cache(bits)
+    L = qz.levels(bits)
+    c.append_recompute_k((rng.standard_normal((1, 2, 20, 16))).astype(np.float32),
+                         rng.standard_normal((1, 2, 20, 16)).astype(np.float32))
+    for step in range(4):
+        # the new tokens widen some channels' range (x3), so the stored keys must move
+        u_prev = c.k.codes(c.stored).astype(np.float32)
+        x_prev = (u_prev * c.k.ch_scale.astype(np.float32)[:, :, None, :]).astype(np.float32) \
+            + c.k.ch_zero.astype(np.float32)[:, :, None, :]
+        k_new = (rng.standard_normal((1, 2, 3, 16)) * (1 + step)).astype(np.float32)
+        n_prev = c.stored
+        c.append_recompute_k(k_new, rng.standard_normal((1, 2, 3, 16)).astype(np.float32))
+        s = c.k.ch_scale32.astype(np.float64)[:, :, None, :]
+        z = c.k.ch_zero32.astype(np.float64)[:, :, None, :]
+        vals = np.concatenate([x_prev, k_new], axis=2).astype(np.float64)
+        # the new range brackets every value: nothing is clamped
+        assert np.all(vals >= z - 1e-6 * np.abs(z)) and np.all(vals <= z + L * s + 1e-5 * (np.abs(z) + L * s))
+        # every stored code is the nearest of the L + 1 levels (float64 brute force), ties excepted
+        u = c.k.codes(c.stored).astype(np.float64)
+        lv = np.arange(L + 1, dtype=np.float64)
+        dist = np.abs(vals[..., None] - (lv * s[..., None] + z[..., None]))
+        best = dist.min(axis=-1)
+        mine = np.take_along_axis(dist, u[..., None].astype(np.int64), axis=-1)[..., 0]
+        assert np.all(mine <= best + 1e-6 * s), f"step {step}: a code is not the nearest level"
+        assert c.stored == n_prev + 3
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_recompute_inside_range_moves_zero_by_one_fp16_rounding_at_most(bits):
+    rng = np.random.default_rng(60 + bits)
+    c = _kivi_cache(bits)
+    k0 = (rng.standard_normal((1, 2, 40, 16)) * 3).astype(np.float32)
+    c.append_recompute_k(k0, k0)
+    z32, z16 = c.k.ch_zero32.copy(), c.k.ch_zero.astype(np.float32)
+    # a new key strictly inside every channel's range
+    mid = ((k0.min(axis=2) + k0.max(axis=2)) / 2)[:, :, None, :].astype(np.float32)
+    c.append_recompute_k(mid, mid)
+    # the smallest stored key dequantises to the fp16 zero, so the new zero is that value
+    np.testing.assert_array_equal(c.k.ch_zero32, z16)
+    assert np.all(np.abs(c.k.ch_zero32 - z32) <= np.abs(z32) * 2.0 ** -11 + 1e-12)
+
+
+def test_recompute_gate():
+    c = OracleCache(CacheSpec(batch=1, n_kv_heads=1, head_dim=16, capacity=20, layout="linear", sink=0, window=0,
+                              k_format="affine_token", k_bits=8, k_group=16,
+                              v_format="affine_token", v_bits=8, v_group=16))
+    x = np.zeros((1, 1, 2, 16), np.float32)
+    with pytest.raises(ValueError):
+        c.append_recompute_k(x, x)
