@@ -42,6 +42,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 EVICT_MIDDLE = 0
 EVICT_KEEPSET = 1
 APPEND_CALIBRATE_K = 1
+APPEND_RECOMPUTE_K = 2
 DEV_OK, DEV_OVERFLOW, DEV_BAD_KEEPSET = 0, 1, 2
 
 
@@ -251,9 +252,11 @@ class KVCache:
         self.handle = None
         self.handle = kvq_cache_init(self.cfg, self.buf, stream)
 
-    def append(self, k: torch.Tensor, v: torch.Tensor, calibrate_k: bool = False, stream=None) -> None:
+    def append(self, k: torch.Tensor, v: torch.Tensor, calibrate_k: bool = False, recompute_k: bool = False,
+               stream=None) -> None:
         n = k.shape[2]
-        kvq_append(self.handle, k, v, n, DTYPES[k.dtype], APPEND_CALIBRATE_K if calibrate_k else 0, stream)
+        flags = (APPEND_CALIBRATE_K if calibrate_k else 0) | (APPEND_RECOMPUTE_K if recompute_k else 0)
+        kvq_append(self.handle, k, v, n, DTYPES[k.dtype], flags, stream)
         self.launches += kvq_last_launch_count()
 
     def convert(self, k: torch.Tensor, v: torch.Tensor, n_tokens: int, calibrate_k: bool = False,

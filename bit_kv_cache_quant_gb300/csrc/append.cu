@@ -55,6 +55,94 @@ __global__ void __launch_bounds__(256) calibrate_kivi_kernel(CacheView c, const 
 }
 
 // ---------------------------------------------------------------------------
+// Recompute-on-append of the per-channel K range ("StreamingLLM + KIVI",
+// "KIVI" and "Caveats": any new token may shift a channel's min / max, so the
+// whole K block is coded again, O(T D) per append).  One CTA of 256 threads
+// per (b, kv head): the stored keys are dequantised in fp32 from the stored
+// fp16 scale and zero (u * s, then + z, each rounded once), the range is
+// taken over them and the n new keys, the new fp32 scale / zero and their
+// fp16 copies are written, and every stored key is coded again against them
+// (byte by byte, so a 4-bit byte's two nibbles stay with one thread).  The new
+// tokens are then coded by append_kernel with the new scales.  An append that
+// would overflow changes nothing here (append_kernel reports it).
+template <typename T>
+__global__ void __launch_bounds__(256) recompute_kivi_kernel(CacheView c, const T* __restrict__ k, int n,
+                                                             long long hstride) {
+  __shared__ float s_old[128], z_old[128], s_new[128], z_new[128];
+  __shared__ float smn[256];
+  __shared__ float smx[256];
+  __shared__ int s_T, s_ok;
+  const int D = c.D;
+  const size_t bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int d = tid % D;
+  const int tg = tid / D;
+  const int ntg = blockDim.x / D;
+  if (tid == 0) {
+    s_T = c.state->stored;
+    s_ok = c.layout != KVQ_LAYOUT_RING && s_T + n <= c.cap;
+  }
+  if (tid < D) {
+    s_old[tid] = __half2float(c.k.ch_scale[bh * D + tid]);
+    z_old[tid] = __half2float(c.k.ch_zero[bh * D + tid]);
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const int Tn = s_T;
+  const int bits = c.k.bits;
+  const int rb = c.k.row_bytes;
+  const float levels = (bits == 8) ? 255.0f : 15.0f;
+  uint8_t* codes = c.k.codes + bh * c.cap_alloc * rb;
+  float mn = __int_as_float(0x7f800000);   // +inf
+  float mx = __int_as_float(0xff800000);   // -inf
+  for (int t = tg; t < Tn; t += ntg) {
+    const uint8_t byte = codes[(size_t)t * rb + (bits == 8 ? d : d / 2)];
+    const int u = bits == 8 ? (byte ^ 0x80) : ((byte >> (4 * (d & 1))) & 15);
+    const float x = __fadd_rn(__fmul_rn((float)u, s_old[d]), z_old[d]);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  const T* base = k + bh * hstride * D;
+  for (int t = tg; t < n; t += ntg) {
+    const float x = In<T>::ld(base + (size_t)t * D + d);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  smn[tid] = mn;
+  smx[tid] = mx;
+  __syncthreads();
+  if (tg == 0) {
+    for (int i = 1; i < ntg; ++i) {
+      mn = fminf(mn, smn[i * D + d]);
+      mx = fmaxf(mx, smx[i * D + d]);
+    }
+    const float sc = affine_scale(mn, mx, levels);
+    s_new[d] = sc;
+    z_new[d] = mn;
+    const size_t o = bh * D + d;
+    c.k.ch_scale32[o] = sc;
+    c.k.ch_zero32[o] = mn;
+    c.k.ch_scale[o] = __float2half_rn(sc);
+    c.k.ch_zero[o] = __float2half_rn(mn);
+  }
+  __syncthreads();
+  for (int i = tid; i < Tn * rb; i += blockDim.x) {
+    uint8_t* p = codes + i;
+    const int j = i % rb;
+    if (bits == 8) {
+      const float x = __fadd_rn(__fmul_rn((float)(*p ^ 0x80), s_old[j]), z_old[j]);
+      *p = (uint8_t)(affine_code(x, s_new[j], z_new[j], levels) ^ 0x80);
+    } else {
+      const int c0 = 2 * j, c1 = 2 * j + 1;
+      const float x0 = __fadd_rn(__fmul_rn((float)(*p & 15), s_old[c0]), z_old[c0]);
+      const float x1 = __fadd_rn(__fmul_rn((float)(*p >> 4), s_old[c1]), z_old[c1]);
+      *p = (uint8_t)(affine_code(x0, s_new[c0], z_new[c0], levels) | (affine_code(x1, s_new[c1], z_new[c1], levels) << 4));
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) c.state->k_calibrated = 1;
+}
+
+// ---------------------------------------------------------------------------
 // Row quantiser: one warp codes one token row of D = 32 * E channels; lane l
 // holds channels [l*E, l*E + E).
 
@@ -253,9 +341,13 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
 
 template <typename T>
 static cudaError_t launch_append_t(const CacheView& c, const void* k, const void* v, int n, long long hstride,
-                                   bool calibrate, cudaStream_t st) {
+                                   bool calibrate, bool recompute, cudaStream_t st) {
   if (calibrate) {
     calibrate_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n, hstride);
+    note_launch();
+  }
+  if (recompute) {
+    recompute_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n, hstride);
     note_launch();
   }
   const long long rows = (long long)c.B * c.Hkv * n;
@@ -273,11 +365,11 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
 }
 
 cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, long long hstride, int in_dtype,
-                          bool calibrate, cudaStream_t st) {
+                          bool calibrate, bool recompute, cudaStream_t st) {
   switch (in_dtype) {
-    case KVQ_DTYPE_F32: return launch_append_t<float>(c, k, v, n, hstride, calibrate, st);
-    case KVQ_DTYPE_BF16: return launch_append_t<__nv_bfloat16>(c, k, v, n, hstride, calibrate, st);
-    case KVQ_DTYPE_F16: return launch_append_t<__half>(c, k, v, n, hstride, calibrate, st);
+    case KVQ_DTYPE_F32: return launch_append_t<float>(c, k, v, n, hstride, calibrate, recompute, st);
+    case KVQ_DTYPE_BF16: return launch_append_t<__nv_bfloat16>(c, k, v, n, hstride, calibrate, recompute, st);
+    case KVQ_DTYPE_F16: return launch_append_t<__half>(c, k, v, n, hstride, calibrate, recompute, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -345,17 +345,23 @@ kvq_status append_rows(kvq_cache c, const void* k, const void* v, int64_t head_s
   if (n_tokens < 1) return fail(KVQ_ERR_INVALID_ARG, "n_tokens must be >= 1");
   if (head_stride < n_tokens) return fail(KVQ_ERR_INVALID_ARG, "head_stride must be >= n_tokens");
   if (!valid_dtype(in_dtype)) return fail(KVQ_ERR_INVALID_ARG, "unknown input dtype %d", in_dtype);
-  if (flags & ~KVQ_APPEND_CALIBRATE_K) return fail(KVQ_ERR_INVALID_ARG, "unknown append flags 0x%x", flags);
+  if (flags & ~(KVQ_APPEND_CALIBRATE_K | KVQ_APPEND_RECOMPUTE_K))
+    return fail(KVQ_ERR_INVALID_ARG, "unknown append flags 0x%x", flags);
   const bool calibrate = (flags & KVQ_APPEND_CALIBRATE_K) != 0;
-  if (calibrate && c->cfg.k_format != KVQ_FMT_KIVI_CHAN)
-    return fail(KVQ_ERR_UNSUPPORTED, "KVQ_APPEND_CALIBRATE_K applies to KIVI_CHAN keys only");
-  if (c->cfg.k_format == KVQ_FMT_KIVI_CHAN && !calibrate && !c->k_calibrated)
+  const bool recompute = (flags & KVQ_APPEND_RECOMPUTE_K) != 0;
+  if (calibrate && recompute)
+    return fail(KVQ_ERR_INVALID_ARG, "KVQ_APPEND_CALIBRATE_K and KVQ_APPEND_RECOMPUTE_K exclude each other");
+  if ((calibrate || recompute) && c->cfg.k_format != KVQ_FMT_KIVI_CHAN)
+    return fail(KVQ_ERR_UNSUPPORTED, "K calibration flags apply to KIVI_CHAN keys only");
+  if (recompute && c->cfg.layout == KVQ_LAYOUT_RING)
+    return fail(KVQ_ERR_UNSUPPORTED, "KVQ_APPEND_RECOMPUTE_K needs a LINEAR or COMPACT layout");
+  if (c->cfg.k_format == KVQ_FMT_KIVI_CHAN && !calibrate && !recompute && !c->k_calibrated)
     return fail(KVQ_ERR_UNSUPPORTED, "per-channel K scales are not calibrated yet (pass KVQ_APPEND_CALIBRATE_K)");
   if (c->cfg.layout != KVQ_LAYOUT_RING && n_tokens > c->cfg.capacity)
     return fail(KVQ_ERR_CAPACITY, "append of %d tokens exceeds capacity %d", n_tokens, c->cfg.capacity);
-  cudaError_t e = kvq::launch_append(c->view, k, v, n_tokens, head_stride, in_dtype, calibrate, stream);
+  cudaError_t e = kvq::launch_append(c->view, k, v, n_tokens, head_stride, in_dtype, calibrate, recompute, stream);
   if (e != cudaSuccess) return cuda_fail(e, what);
-  if (calibrate) c->k_calibrated = true;
+  if (calibrate || recompute) c->k_calibrated = true;
   return KVQ_OK;
 }
 

@@ -131,8 +131,9 @@ kvq_status report_error(kvq_status s, const char* msg);
 
 // Launchers (defined in the kernel files).
 // Token t of (b, kv head) bh is row bh * hstride + t of k and v (hstride >= n).
+// recompute: KIVI keys, recompute the per-channel range over the stored and new keys first.
 cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, long long hstride, int in_dtype,
-                          bool calibrate, cudaStream_t st);
+                          bool calibrate, bool recompute, cudaStream_t st);
 cudaError_t launch_evict_middle(const CacheView& c, cudaStream_t st);
 cudaError_t launch_evict_keepset(const CacheView& c, const int* idx, int n_keep, cudaStream_t st);
 

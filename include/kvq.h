@@ -98,6 +98,13 @@ typedef enum kvq_evict_mode {
 /* kvq_append flags */
 #define KVQ_APPEND_CALIBRATE_K 1   /* KIVI_CHAN keys: compute and freeze the per-channel
                                       scales from this call's tokens before coding them */
+#define KVQ_APPEND_RECOMPUTE_K 2   /* KIVI_CHAN keys, LINEAR / COMPACT layouts ([SLK] "KIVI",
+                                      "Caveats": the range is recomputed on every append):
+                                      dequantise the stored keys in fp32 from the stored fp16
+                                      scale and zero (u * s, then + z), take each channel's
+                                      range over them and the new keys, code every stored key
+                                      again and the new ones with the new scale / zero.
+                                      O(stored * D) per call; excludes CALIBRATE_K. */
 
 /* Device status codes (kvq_stats.device_status). */
 #define KVQ_DEV_OK 0

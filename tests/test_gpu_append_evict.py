@@ -230,3 +230,48 @@ def test_convert_rejects_short_stride(kvq):
     k = torch.zeros((1, 2, 10, 64), dtype=torch.float16, device="cuda")
     with pytest.raises(kvq.KvqError):
         kvq.kvq_convert(cache.handle, k, k, 8, 10, kvq.DTYPES[torch.float16])
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("layout", ["linear", "compact"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_recompute_k_on_append_bit_exact(kvq, bits, layout, D):
+    """KVQ_APPEND_RECOMPUTE_K: every append recomputes the per-channel K range over the stored
+    (dequantised) and new keys and codes the whole block again; bit-exact against the oracle,
+    through evictions, and decode attention over the result matches."""
+    from kvq_helpers import assert_attention_close
+    from oracle import attention as oatt
+
+    B, H = 2, 2
+    sink, window = (4, 48) if layout == "compact" else (0, 0)
+    cap = 120 if layout == "linear" else sink + window + 8
+    cache = kvq.KVCache(B, H, D, cap, "kivi_chan", bits, 0, "affine_token", bits, D, layout=layout, sink=sink,
+                        window=window)
+    oc = OracleCache(oracle_spec(cache, None))
+    steps = [20, 1, 3, 1, 8, 1, 1] if layout == "linear" else [30, 8, 8, 8, 5, 1, 7]
+    for i, n in enumerate(steps):
+        k = _inputs((B, H, n, D), 70 + i, torch.bfloat16) * (1.0 + 0.4 * i)   # later tokens widen the range
+        v = _inputs((B, H, n, D), 90 + i, torch.bfloat16, 0.0)
+        cache.append(k.cuda(), v.cuda(), recompute_k=True)
+        oc.append_recompute_k(host(k), host(v))
+        if layout == "compact":
+            cache.evict_middle()
+            oc.evict_middle()
+        assert_cache_equal(cache, oc, f"step {i}")
+    q = torch.randn((B, 3 * H, D), generator=torch.Generator().manual_seed(99)).to(torch.bfloat16)
+    out = cache.decode_attn(q.cuda())
+    kh, vh = oc.dequant()
+    assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), "decode after recompute appends")
+
+
+def test_recompute_k_flag_gates(kvq):
+    x = torch.zeros((1, 1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    ring = kvq.KVCache(1, 1, 64, 36, "kivi_chan", 8, 0, "affine_token", 8, 64, layout="ring", sink=4, window=32)
+    with pytest.raises(kvq.KvqError):
+        ring.append(x, x, recompute_k=True)
+    aff = kvq.KVCache(1, 1, 64, 36, "affine_token", 8, 64, "affine_token", 8, 64)
+    with pytest.raises(kvq.KvqError):
+        aff.append(x, x, recompute_k=True)
+    kiv = kvq.KVCache(1, 1, 64, 36, "kivi_chan", 8, 0, "affine_token", 8, 64)
+    with pytest.raises(kvq.KvqError):
+        kiv.append(x, x, calibrate_k=True, recompute_k=True)
