@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
       const float mn = fmaxf(m_run, mb);                 // finite: row tok0 is valid
       if (mn > m_run) {
-        const float alpha = exp2f(m_run - mn);
+        const float alpha = fast_exp2(m_run - mn);
         l_part *= alpha;
         zacc *= alpha;
 #pragma unroll
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
       float p[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        p[i] = exp2f(sc[i] - mn);
+        p[i] = fast_exp2(sc[i] - mn);
         l_part += p[i];
       }
       __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);

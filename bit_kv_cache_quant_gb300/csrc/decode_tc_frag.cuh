@@ -202,6 +202,16 @@ __host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
   return L;
 }
 
+// 2^x with the hardware's approximate base-2 exponential (ex2.approx.ftz: a
+// couple of ulp, results below 2^-126 flushed to zero).  Used for softmax
+// weights 2^(s - max) in (0, 1], where that error is far below the
+// tolerance and the flushed weights are negligible.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Programmatic dependent launch: wait until the grids this launch depends on
 // have completed (a no-op for a launch without the attribute), and allow the
 // next dependent launch to start its prologue.
