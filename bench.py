@@ -549,6 +549,8 @@ def bench_decode(a, kvq, w, rank, world):
     }
     if w.layout == "linear":
         line["convert"] = bench_convert(kvq, w, device, a.warmup)
+    if w.k_format == "kivi_chan" and w.layout != "ring":
+        line["recompute_k_append"] = bench_recompute(kvq, w, device, a.warmup)
     if not a.no_e2e:
         e_bytes, e_dt, h2d, d2h = e2e_decode(ds, max(3, min(a.steps, 200)), world)
         line["e2e"] = {"value": world * e_bytes / e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -662,6 +664,33 @@ def bench_convert(kvq, w, device, warmup):
         nbytes += w.batch * w.n_kv_heads * w.context * w.head_dim * k.element_size()   # calibration pass over K
     return {"tokens_per_s": w.batch * w.context / t, "gbs": nbytes / t / 1e9, "us": t * 1e6,
             "tokens": w.context, "what": "one layer's dense cache, every (batch row, kv head), into a fresh cache"}
+
+
+def bench_recompute(kvq, w, device, warmup):
+    """One single-token append with the per-channel K range recomputed over the whole
+    stored block (KVQ_APPEND_RECOMPUTE_K), on one layer filled to the context."""
+    cap = w.sink + w.window + 1 if w.layout == "compact" else w.context + 64
+    cache = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, cap, w.k_format, w.k_bits, w.k_group, w.v_format,
+                        w.v_bits, w.v_group, layout=w.layout, sink=w.sink, window=w.window, device=device)
+    k, v = synth.layer_inputs(w, 0, 0, w.context, device=device)
+    cache.append(k, v, recompute_k=True)
+    _, k1, v1 = synth.decode_token_inputs(w, 0, 0, w.context, device=device)
+    reps = 20
+    times = []
+    for i in range(warmup + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cache.append(k1, v1, recompute_k=True)
+        e1.record()
+        if w.layout == "compact":
+            cache.evict_middle()
+        torch.cuda.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.median(times)
+    stored = cache.stats().stored
+    return {"us": t * 1e6, "stored_tokens": stored, "appends_per_s": 1.0 / t,
+            "what": "append of one token per (batch row, kv head) recoding every stored key"}
 
 
 def bench_snapkv(a, kvq, w, rank, world):
@@ -786,7 +815,7 @@ def per_config(a, kvq):
                            "steps": sub.steps, "decode_steps_per_s": ln.get("decode_steps_per_s"),
                            "roofline_kernel": r.get("kernel"), "kernel_us": r.get("avg_launch_us"),
                            "frac": r["frac"], "clocks": ln.get("clocks")}
-            for key in ("snapkv_select_us", "convert"):
+            for key in ("snapkv_select_us", "convert", "recompute_k_append"):
                 if key in ln:
                     out[w.name][key] = ln[key]
         except Exception as e:  # noqa: BLE001 - the primary line must still print
