@@ -168,7 +168,9 @@ __host__ __device__ constexpr int merge_lanes(int items, int threads) {
 // to finish merges every partial with the online-softmax rule.
 // Accumulator layout: ACCPAD == 0: acc[warp][h][d]; ACCPAD > 0 (tensor-core
 // kernel): rows of D + ACCPAD floats, channel d at (d % (D/8)) * 8 + d / (D/8).
-template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps>
+// HG > 1: warp w holds only heads 4 j .. 4 j + 3, j = (w / 4) % HG, and the
+// other heads' entries of that warp are not read.
+template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps, int HG = 1>
 __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split, int nse,
                                             float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc) {
   constexpr int PROW = D + kPartialPad;
@@ -183,13 +185,15 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   for (int idx = threadIdx.x; idx < G * D; idx += NTHR) {
     const int h = idx / D, d = idx % D;
     const int pos = h * AROW + (ACCPAD ? (d % (D / 8)) * 8 + d / (D / 8) : d);
-    float M = sm_m[0][h];
+    float M = neg_inf();
 #pragma unroll
-    for (int w = 1; w < NWARP; ++w) M = fmaxf(M, sm_m[w][h]);
+    for (int w = 0; w < NWARP; ++w)
+      if (HG == 1 || ((w >> 2) % HG) == (h >> 2)) M = fmaxf(M, sm_m[w][h]);
     float A = 0.0f, L = 0.0f;
     if (M != neg_inf()) {
 #pragma unroll
       for (int w = 0; w < NWARP; ++w) {
+        if (HG > 1 && ((w >> 2) % HG) != (h >> 2)) continue;
         const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
         A = fmaf(sm_acc[w * G * AROW + pos], e, A);
         L = fmaf(sm_l[w][h], e, L);

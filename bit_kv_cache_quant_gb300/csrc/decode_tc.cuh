@@ -7,23 +7,31 @@
 // the odd ones, each warp 16 tokens of a tile.  There is no CTA-wide barrier
 // in the loop: every warp waits on the stage's mbarrier itself, and the last of
 // the four warps to finish a stage copies the tile NSTAGE ahead into it.
-// Per warp and 16-token block:
-//   S[16 x 16] = Q[16 x D] . K^T : rows 0..7 of the A operand hold fp16(q) of
-//     the (up to 8) query heads of the kv head, rows 8..15 the residual
-//     q - fp16(q), so the score of head h is row h + row h + 8 and q enters
-//     exactly.  The key codes enter as exact small integers (Q4_0 as the
-//     signed levels u - 8); keys with per-token groups (affine, Q4_0) get one
-//     fp32 accumulator per 32-channel block and are scaled afterwards, per
-//     scale group, s * sum(q u) + z * sum(q) (Q4_0: d * sum(q (u - 8))), so
-//     the scores carry no fp16 rounding of the keys.  Per-channel KIVI scales
-//     are folded into q; their zero term is a per-row constant the softmax
-//     does not see and is dropped.
-//   O[16 x D] += P[16 x 16] . V_hat : the block's probabilities as A (value +
-//     residual rows again), the value block as B.  Values with several scale
+// Per warp and 16-token block, both contractions are taken transposed so that
+// the 16 rows of the MMA are tokens (scores) or value channels (outputs) and
+// the 8 columns hold four query heads as (fp16 part, residual) pairs:
+//   S^T[16 x 8] = K[16 x D] . Q^T : the key codes as A, exact small integers
+//     (Q4_0 as the signed levels u - 8); column 2j of Q^T holds fp16(q) of
+//     head j, column 2j + 1 the residual q - fp16(q), so the score of head j
+//     is the sum of the two columns and q enters exactly.  Keys with
+//     per-token groups (affine, Q4_0) get one fp32 accumulator per 32-channel
+//     block and are scaled afterwards, per scale group, s * sum(q u) +
+//     z * sum(q) (Q4_0: d * sum(q (u - 8))), so the scores carry no fp16
+//     rounding of the keys.  Per-channel KIVI scales are folded into q; their
+//     zero term is a per-row constant the softmax does not see and is dropped.
+//     Each thread then holds one head's scores for two tokens, and the
+//     online-softmax state of that head.
+//   O^T[16 x 8] += V^T[16 x 16] . P^T : the value block as A, the
+//     probabilities (again fp16 part + residual columns) as B, moved into the
+//     B layout with a warp transpose (movmatrix).  Values with several scale
 //     groups per token are dequantised to fp16 in registers (one HFMA2 with
 //     the token's fp16 scale and zero); values with one group per token enter
-//     as exact integer codes, the token's scale multiplies its probability and
-//     sum(p * zero) is accumulated apart in fp32 and added to every channel.
+//     as exact integer codes, the token's scale multiplies its probability
+//     and sum(p * zero) is accumulated apart in fp32 and added to every
+//     channel.  The accumulator columns of a thread belong to the same head
+//     as its scores, so the softmax rescale stays inside the thread.
+// With up to four query heads per kv head one column tile does it; five to
+// eight take two.
 // Codes become fp16 through the mantissa of 1024.0 (see nibbles_to_h2).
 #pragma once
 
@@ -48,34 +56,46 @@ __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* 
   }
 }
 
-// O += P . V for one 16-token block: A = the probabilities (pa), B = the value
-// codes of the thread's four tokens (words A, B, C, E), dequantised to fp16 in
-// registers with each token's scale and zero when DEQ, else taken as exact
-// integers (the scale then sits in pa and the zero in a separate sum).
-template <int VB, int NW, int NT, bool DEQ>
-__device__ __forceinline__ void pv_mma(float (&oacc)[NT][4], const uint32_t (&pa)[4], const uint32_t (&A)[NW],
-                                       const uint32_t (&B)[NW], const uint32_t (&C)[NW], const uint32_t (&E)[NW],
-                                       __half2 sAB, __half2 zAB, __half2 sCD, __half2 zCD) {
+// O^T += V^T . P^T for one 16-token block.  A = the value codes of the
+// thread's four tokens (words A, B, C, E: logical tokens 2t, 2t + 1, 2t + 8,
+// 2t + 9), paired per channel as the A fragment wants them; m-tile mt covers
+// this thread's value channels 2 mt (fragment row g) and 2 mt + 1 (row g + 8).
+// B = the transposed probabilities pb.  Codes are
+// dequantised to fp16 in registers with each token's scale and zero when DEQ,
+// else taken as exact integers (the scale then sits in pb and the zero in a
+// separate sum).
+// The NW words are words mo / (m-tiles per word) onward of the thread's value
+// bytes; they feed m-tiles mo onward.
+template <int VB, int NW, int MT, bool DEQ>
+__device__ __forceinline__ void pvt_mma(float (&oacc)[MT][4], const uint32_t (&pb)[2], int mo,
+                                        const uint32_t (&A)[NW], const uint32_t (&B)[NW], const uint32_t (&C)[NW],
+                                        const uint32_t (&E)[NW], __half2 sAB, __half2 zAB, __half2 sCD, __half2 zCD) {
   if constexpr (VB == 4) {
+    static_assert(4 * NW <= MT, "m-tiles");
 #pragma unroll
     for (int wi = 0; wi < NW; ++wi) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint32_t sel = half ? 0x7632u : 0x5410u;
         __half2 h0[4], h1[4];
-        nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // channels 8 wi + 4 half + 0..3 of tokens A, B
+        nibbles_to_h2(__byte_perm(A[wi], B[wi], sel), h0);   // h0[i]: channel 8 wi + 4 half + i of tokens A, B
         nibbles_to_h2(__byte_perm(C[wi], E[wi], sel), h1);
+        if constexpr (DEQ) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if constexpr (DEQ) {
+          for (int i = 0; i < 4; ++i) {
             h0[i] = __hfma2(h0[i], sAB, zAB);
             h1[i] = __hfma2(h1[i], sCD, zCD);
           }
-          mma_f16(oacc[8 * wi + 4 * half + i], pa, h2u(h0[i]), h2u(h1[i]));
+        }
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const uint32_t va[4] = {h2u(h0[2 * pp]), h2u(h0[2 * pp + 1]), h2u(h1[2 * pp]), h2u(h1[2 * pp + 1])};
+          mma_f16(oacc[mo + 4 * wi + 2 * half + pp], va, pb[0], pb[1]);
         }
       }
     }
   } else if constexpr (VB == 8) {
+    static_assert(2 * NW <= MT, "m-tiles");
 #pragma unroll
     for (int wi = 0; wi < NW; ++wi) {
       const uint32_t a_ = A[wi] ^ 0x80808080u, b_ = B[wi] ^ 0x80808080u;
@@ -90,26 +110,35 @@ __device__ __forceinline__ void pv_mma(float (&oacc)[NT][4], const uint32_t (&pa
           l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
           l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
         }
-        mma_f16(oacc[4 * wi + 2 * half], pa, h2u(l0), h2u(l1));
-        mma_f16(oacc[4 * wi + 2 * half + 1], pa, h2u(h0), h2u(h1));
+        const uint32_t va[4] = {h2u(l0), h2u(h0), h2u(l1), h2u(h1)};
+        mma_f16(oacc[mo + 2 * wi + half], va, pb[0], pb[1]);
       }
     }
   } else {
+    static_assert(NW <= MT, "m-tiles");
 #pragma unroll
     for (int wi = 0; wi < NW; ++wi) {
-      mma_f16(oacc[2 * wi], pa, __byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x5410u));
-      mma_f16(oacc[2 * wi + 1], pa, __byte_perm(A[wi], B[wi], 0x7632u), __byte_perm(C[wi], E[wi], 0x7632u));
+      const uint32_t va[4] = {__byte_perm(A[wi], B[wi], 0x5410u), __byte_perm(A[wi], B[wi], 0x7632u),
+                              __byte_perm(C[wi], E[wi], 0x5410u), __byte_perm(C[wi], E[wi], 0x7632u)};
+      mma_f16(oacc[mo + wi], va, pb[0], pb[1]);
     }
   }
 }
 
-// A CTA has NGRP groups of four warps; group gp consumes tiles gp, gp + NGRP, ...
-// Four-warp CTAs (four per SM) suit grids of several waves; eight-warp CTAs
-// (two per SM) halve the time per split when the whole grid fits in one wave.
-template <int NGRP> struct TcShape {
-  static constexpr int warps = 4 * NGRP;
+// A CTA has NGRP tile groups of HG head groups of four warps.  Tile group gp
+// consumes tiles gp, gp + NGRP, ...; within it, head group j computes query
+// heads 4 j .. 4 j + 3 over the same stages (HG = 2 for five to eight heads per
+// kv head).  Four-warp CTAs (four per SM) suit grids of several waves;
+// eight-warp tile pairs (two per SM) halve the time per split when the whole
+// grid fits in one wave.
+template <int NGRP, int HG> struct TcShape {
+  static constexpr int warps = 4 * NGRP * HG;
   static constexpr int threads = 32 * warps;
-  static constexpr int ctas_per_sm = 4 / NGRP;
+  static constexpr int ctas_per_sm = 4 / (NGRP * HG);
+};
+
+template <int G> struct TcHeads {
+  static constexpr int hg = (G + 3) / 4;   // head groups
 };
 
 // Pipeline depth.  Four-warp CTAs (four per SM, several waves) use two
@@ -122,13 +151,14 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
                                  ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * (D / 32) * 2 +
                                  ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * (D / 16) * 2) +
                                 1023) / 1024 * 1024;
-  static constexpr int warps = TcShape<NGRP>::warps;
+  using Shape = TcShape<NGRP, TcHeads<G>::hg>;
+  static constexpr int warps = Shape::warps;
   // per-warp (head, channel) accumulators, written over the stages after the loop
   static constexpr int acc_bytes = warps * G * (D + 8) * 4;
-  static constexpr int static_smem = 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 + (D / 16) * 512 + 1024;
-  static constexpr int budget = 227 * 1024 / TcShape<NGRP>::ctas_per_sm - 2048 - static_smem;
+  static constexpr int static_smem = 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 + (D / 32) * 32 + 1024;
+  static constexpr int budget = 227 * 1024 / Shape::ctas_per_sm - 2048 - static_smem;
   static constexpr int raw = (budget / stage) / NGRP * NGRP;
-  static constexpr int v = NGRP == 1 ? 2 : (raw < 2 ? 2 : (raw > 8 ? 8 : raw));
+  static constexpr int v = (NGRP == 1 && Shape::ctas_per_sm > 1) ? 2 : (raw < 2 ? 2 : (raw > 8 ? 8 : raw));
   // dynamic shared memory for a stage size (+ 1 KB to align the ring to 1024)
   static constexpr int dyn_bytes(int stage_bytes) {
     return (v * stage_bytes > acc_bytes ? v * stage_bytes : acc_bytes) + 1024;
@@ -136,17 +166,19 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
 };
 
 template <int D, int G, int KF, int VF, int NGRP>
-__global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_per_sm)
+__global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShape<NGRP, TcHeads<G>::hg>::ctas_per_sm)
     decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
+  constexpr int HG = TcHeads<G>::hg;
   constexpr int NSTAGE = TcStages<D, G, KF, VF, NGRP>::v;
-  constexpr int NWARP = TcShape<NGRP>::warps;
+  constexpr int NWARP = TcShape<NGRP, HG>::warps;
+  constexpr int TW = 4 * HG;       // warps reading each tile
   constexpr int KB = FmtBits<KF>::v;
   constexpr int VB = FmtBits<VF>::v;
   constexpr int KROW = D * KB / 8;
   constexpr int VROW = D * VB / 8;
-  constexpr int KS = D / 16;       // k-steps of Q K^T
-  constexpr int NT = D / 8;        // n-tiles of P V
+  constexpr int KS = D / 16;       // k-steps of K Q^T
   constexpr int NB = D / 32;       // 32-channel key blocks
+  constexpr int MT = D / 16;       // 16-channel m-tiles of O^T
   constexpr int VCH = D / 8;       // value channels owned by thread g
   constexpr int VTB = VROW / 8;    // value bytes per token owned by thread g
   constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
@@ -156,22 +188,17 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   constexpr int NACC = KG ? NB : 1;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per kv head");
-  static_assert(NSTAGE % NGRP == 0, "each stage serves one warp group");
+  static_assert(NSTAGE % NGRP == 0, "each stage serves one tile group");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ float sm_m[NWARP][G];
   __shared__ float sm_l[NWARP][G];
   __shared__ __align__(8) uint64_t mbar[NSTAGE];
-  __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (4 per tile)
+  __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (TW per tile)
   __shared__ int s_last_tile[NSTAGE];     // last tile copied into a stage, -1 if none
   __shared__ int s_T;
   __shared__ volatile int s_fail;
-  // Query fragments in key-channel order (lane-major, one 16-byte vector per
-  // k-step) and per-block sums of q for grouped keys.
-  __shared__ __align__(16) uint4 sm_qa[KS][32];
-  __shared__ float sm_qblk[NB][8];       // sum of q over each 32-channel block
-  __shared__ float sm_q64[NB / 2][8];    // ... over each 64-channel group
-  __shared__ float sm_q128[8];           // ... over all channels (D = 128)
+  __shared__ float sm_qsum[NB][8];        // sum of q of each head over each 32-channel key block
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int lane = threadIdx.x & 31;
@@ -207,32 +234,47 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     fence_async_smem();   // the initialised barriers are visible to the copy engine
   }
   grid_dependency_wait();
-  // Thread 0 reads the stored length while warp 1 builds the query fragments.
+  // Warp roles: 16-row block of each tile, head group, tile group.
+  const int blk = (warp & 3) * 16;
+  const int hg = (warp >> 2) % HG;
+  const int grp = (warp >> 2) / HG;
+  const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
+  // Thread 0 reads the stored length while the query fragments are built.
+  // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
+  // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
+  // columns and q enters exactly.  Thread (g, t) builds column g at the key
+  // channels of its fragment slots.
   if (threadIdx.x == 0) s_T = c.state->stored;
-  if (warp == 1) {
+  uint32_t qf[KS][2];
+  {
+    const int hq = 4 * hg + (g >> 1);
+    const bool live = hq < G;
+    const size_t qo = ((size_t)b * a.Hq + (size_t)kvh * G + (live ? hq : 0)) * D;
     float qb[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i) qb[i] = 0.0f;
-    const bool live = g < G;
-    const size_t qo = ((size_t)b * a.Hq + (size_t)kvh * G + (live ? g : 0)) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       int ch[4];
       key_channels<KB>(ks, t, ch);
-      float qv[4];
+      float x[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float x = live ? load_io(a.q, qo + ch[i], a.io_dtype) : 0.0f;
-        if constexpr (K_KIVI) x *= __half2float(c.k.ch_scale[bh * D + ch[i]]);
-        qv[i] = x;
+        float v = live ? load_io(a.q, qo + ch[i], a.io_dtype) : 0.0f;
+        if constexpr (K_KIVI) v *= __half2float(c.k.ch_scale[bh * D + ch[i]]);
+        x[i] = v;
       }
-      if constexpr (K_AFF) qb[ks >> 1] += (qv[0] + qv[1]) + (qv[2] + qv[3]);
-      const __half2 h01 = __floats2half2_rn(qv[0], qv[1]);
-      const __half2 h23 = __floats2half2_rn(qv[2], qv[3]);
-      const float2 f01 = __half22float2(h01);
-      const float2 f23 = __half22float2(h23);
-      sm_qa[ks][lane] = make_uint4(h2u(h01), h2u(__floats2half2_rn(qv[0] - f01.x, qv[1] - f01.y)), h2u(h23),
-                                   h2u(__floats2half2_rn(qv[2] - f23.x, qv[3] - f23.y)));
+      if constexpr (K_AFF) qb[ks >> 1] += (x[0] + x[1]) + (x[2] + x[3]);
+      const __half2 h01 = __floats2half2_rn(x[0], x[1]);
+      const __half2 h23 = __floats2half2_rn(x[2], x[3]);
+      qf[ks][0] = h2u(h01);
+      qf[ks][1] = h2u(h23);
+      if (g & 1) {
+        const float2 f01 = __half22float2(h01);
+        const float2 f23 = __half22float2(h23);
+        qf[ks][0] = h2u(__floats2half2_rn(x[0] - f01.x, x[1] - f01.y));
+        qf[ks][1] = h2u(__floats2half2_rn(x[2] - f23.x, x[3] - f23.y));
+      }
     }
     if constexpr (K_AFF) {
 #pragma unroll
@@ -240,16 +282,9 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
         qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 1);
         qb[i] += __shfl_xor_sync(0xffffffffu, qb[i], 2);
       }
-      if (t == 0) {
-        float all = 0.0f;
+      if ((warp & 3) == 0 && grp == 0 && t == 0 && !(g & 1) && live) {
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          sm_qblk[i][g] = qb[i];
-          all += qb[i];
-        }
-#pragma unroll
-        for (int j = 0; j < NB / 2; ++j) sm_q64[j][g] = qb[2 * j] + qb[2 * j + 1];
-        sm_q128[g] = all;
+        for (int i = 0; i < NB; ++i) sm_qsum[i][hq] = qb[i];
       }
     }
   }
@@ -259,12 +294,11 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   split_rows(T, a.nsplit, split, t0, t1, nse);
   if (split >= nse) return;   // no rows for this split (no copy was issued)
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
-  // Each warp group's first tile is requested alone, so that it reaches the
+  // Each tile group's first tile is requested alone, so that it reaches the
   // SM ahead of the rest of the split (which every CTA would otherwise ask
   // for at the same moment); the group's first warp requests the group's
   // other initial tiles once that tile has landed.
-  const int grp = warp >> 2;
-  const bool leader = (warp & 3) == 0 && lane == 0;
+  const bool leader = (warp % TW) == 0 && lane == 0;
   if (leader && grp < ntiles) {
     issue_tile_tma<D, KF, VF>(smem + grp * TL.bytes, TL, c, bh, t0 + grp * kTileTokens, &mbar[grp]);
     s_last_tile[grp] = grp;
@@ -278,12 +312,28 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   float m_run = neg_inf();
   float l_part = 0.0f;
   float zacc = 0.0f;   // sum of p * zero over this thread's tokens (vfold)
-  float oacc[NT][4];
+  float oacc[MT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.0f;
+  for (int mt = 0; mt < MT; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.0f;
+  // Sum of q of head hd over each key scale group (affine keys); padding
+  // heads take a live head's sums (their outputs are dropped).
+  float qg[NB];
+  if constexpr (K_AFF) {
+    const int h = min(hd, G - 1);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) qg[i] = sm_qsum[i][h];
+    if (2 * kng == NB) {
+#pragma unroll
+      for (int j = 0; j < NB / 2; ++j) qg[j] = qg[2 * j] + qg[2 * j + 1];
+    } else if constexpr (NB == 4) {
+      if (kng != NB) qg[0] = (qg[0] + qg[1]) + (qg[2] + qg[3]);
+    }
+  }
 
-  const int blk = (warp & 3) * 16;                      // this warp's 16 rows of each tile
-  // rows of the four tokens this thread's scores / value pairs belong to
+  // Tile rows of the two tokens whose scores this thread holds (logical g and
+  // g + 8) and of the four tokens its value fragments read (2t, 2t + 1,
+  // 2t + 8, 2t + 9).
+  const int rk[2] = {blk + tau<VROW>(g), blk + tau<VROW>(g + 8)};
   const int rr[4] = {blk + tau<VROW>(2 * t), blk + tau<VROW>(2 * t + 1), blk + tau<VROW>(2 * t + 8),
                      blk + tau<VROW>(2 * t + 9)};
 
@@ -303,107 +353,112 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
     const uint8_t* st = smem + stg * TL.bytes;
     const int tok0 = t0 + it * kTileTokens + blk;
     if (tok0 < t1) {   // warp-uniform
-      // ---------------------------------------------------------- S = Q K^T
-      // sc[2 nt + e]: head g, logical token 8 nt + 2t + e (tile row rr[2 nt + e]).
-      float sc[4];
+      // ------------------------------------------------------ S^T = K Q^T
+      // acc[.][2e + j]: token rk[e], column 2j (j = 0: fp16 part, 1: residual)
+      float acc[NACC][4];
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
       const uint8_t* kpl = st + TL.kc;
+      if constexpr (KB == 4) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float acc[NACC][4];
+        for (int p = 0; p < NB; ++p) {
+          __half2 h0[4], h1[4];
+          nibbles_to_h2<K_Q40 ? 8 : 0>(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(rk[0], 16 * p + 4 * t)), h0);
+          nibbles_to_h2<K_Q40 ? 8 : 0>(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(rk[1], 16 * p + 4 * t)), h1);
+          const uint32_t ka0[4] = {h2u(h0[0]), h2u(h1[0]), h2u(h0[2]), h2u(h1[2])};
+          const uint32_t ka1[4] = {h2u(h0[1]), h2u(h1[1]), h2u(h0[3]), h2u(h1[3])};
+          mma_f16(acc[KG ? p : 0], ka0, qf[2 * p][0], qf[2 * p][1]);
+          mma_f16(acc[KG ? p : 0], ka1, qf[2 * p + 1][0], qf[2 * p + 1][1]);
+        }
+      } else if constexpr (KB == 8) {
 #pragma unroll
-        for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-        const int r = blk + tau<VROW>(nt * 8 + g);
-        if constexpr (KB == 4) {
+        for (int ks = 0; ks < KS; ++ks) {
+          __half2 l0, h0, l1, h1;
+          bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(rk[0], 16 * ks + 4 * t)) ^ 0x80808080u,
+                      l0, h0);
+          bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(rk[1], 16 * ks + 4 * t)) ^ 0x80808080u,
+                      l1, h1);
+          const uint32_t ka[4] = {h2u(l0), h2u(l1), h2u(h0), h2u(h1)};
+          mma_f16(acc[KG ? (ks >> 1) : 0], ka, qf[ks][0], qf[ks][1]);
+        }
+      } else {
 #pragma unroll
-          for (int p = 0; p < NB; ++p) {
-            __half2 h[4];
-            nibbles_to_h2<K_Q40 ? 8 : 0>(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * p + 4 * t)), h);
-            const uint4 q0 = sm_qa[2 * p][lane], q1 = sm_qa[2 * p + 1][lane];
-            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
-            float(&dst)[4] = acc[KG ? p : 0];
-            mma_f16(dst, a0, h2u(h[0]), h2u(h[2]));
-            mma_f16(dst, a1, h2u(h[1]), h2u(h[3]));
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint2 v0 = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(rk[0], 32 * ks + 8 * t));
+          const uint2 v1 = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(rk[1], 32 * ks + 8 * t));
+          const uint32_t ka[4] = {v0.x, v1.x, v0.y, v1.y};
+          mma_f16(acc[0], ka, qf[ks][0], qf[ks][1]);
+        }
+      }
+      bool vk[2];
+      float sc[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        vk[e] = tok0 - blk + rk[e] < t1;
+        float v = 0.0f;
+        if constexpr (K_Q40) {
+          // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
+          float d[NB];
+          load_halves<NB>(st + TL.ks + rk[e] * (2 * NB), d);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            v = fmaf(d[nb], acc[nb][2 * e], v);
+            v = fmaf(d[nb], acc[nb][2 * e + 1], v);
           }
-        } else if constexpr (KB == 8) {
+        } else if constexpr (K_AFF) {
+          // s * sum(q u) + z * sum(q) per scale group of 32, 64 or 128 channels
+          float x[NB];
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            __half2 lo, hi;
-            bytes_to_h2(*reinterpret_cast<const uint32_t*>(kpl + swz_off<KROW>(r, 16 * ks + 4 * t)) ^ 0x80808080u, lo,
-                        hi);
-            const uint4 q0 = sm_qa[ks][lane];
-            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
-            mma_f16(acc[KG ? (ks >> 1) : 0], a0, h2u(lo), h2u(hi));
+          for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][2 * e] + acc[nb][2 * e + 1];
+          const uint8_t* srow = st + TL.ks + rk[e] * (2 * kng);
+          const uint8_t* zrow = st + TL.kz + rk[e] * (2 * kng);
+          if (kng == NB) {
+            float sg[NB], zg[NB];
+            load_halves<NB>(srow, sg);
+            load_halves<NB>(zrow, zg);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) v = fmaf(sg[nb], x[nb], fmaf(zg[nb], qg[nb], v));
+          } else if (2 * kng == NB) {
+            float sg[NB / 2], zg[NB / 2];
+            load_halves<NB / 2>(srow, sg);
+            load_halves<NB / 2>(zrow, zg);
+#pragma unroll
+            for (int j = 0; j < NB / 2; ++j) v = fmaf(sg[j], x[2 * j] + x[2 * j + 1], fmaf(zg[j], qg[j], v));
+          } else if constexpr (NB == 4) {
+            float sg[1], zg[1];
+            load_halves<1>(srow, sg);
+            load_halves<1>(zrow, zg);
+            v = fmaf(sg[0], (x[0] + x[1]) + (x[2] + x[3]), zg[0] * qg[0]);
           }
         } else {
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const uint2 v = *reinterpret_cast<const uint2*>(kpl + swz_off<KROW>(r, 32 * ks + 8 * t));
-            const uint4 q0 = sm_qa[ks][lane];
-            const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w};
-            mma_f16(acc[0], a0, v.x, v.y);
-          }
+          v = acc[0][2 * e] + acc[0][2 * e + 1];
         }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 2 * nt + e;
-          float v;
-          if constexpr (K_Q40) {
-            // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
-            float d[NB];
-            load_halves<NB>(st + TL.ks + rr[i] * (2 * NB), d);
-            v = 0.0f;
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              v = fmaf(d[nb], acc[nb][e], v);
-              v = fmaf(d[nb], acc[nb][2 + e], v);
-            }
-          } else if constexpr (K_AFF) {
-            // s * sum(q u) + z * sum(q) per scale group of 32, 64 or 128 channels
-            float x[NB];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][e] + acc[nb][2 + e];
-            const uint8_t* srow = st + TL.ks + rr[i] * (2 * kng);
-            const uint8_t* zrow = st + TL.kz + rr[i] * (2 * kng);
-            v = 0.0f;
-            if (kng == NB) {
-              float sg[NB], zg[NB];
-              load_halves<NB>(srow, sg);
-              load_halves<NB>(zrow, zg);
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb) v = fmaf(sg[nb], x[nb], fmaf(zg[nb], sm_qblk[nb][g], v));
-            } else if (2 * kng == NB) {
-              float sg[NB / 2], zg[NB / 2];
-              load_halves<NB / 2>(srow, sg);
-              load_halves<NB / 2>(zrow, zg);
-#pragma unroll
-              for (int j = 0; j < NB / 2; ++j) v = fmaf(sg[j], x[2 * j] + x[2 * j + 1], fmaf(zg[j], sm_q64[j][g], v));
-            } else if constexpr (NB == 4) {
-              float sg[1], zg[1];
-              load_halves<1>(srow, sg);
-              load_halves<1>(zrow, zg);
-              v = fmaf(sg[0], (x[0] + x[1]) + (x[2] + x[3]), zg[0] * sm_q128[g]);
-            }
-          } else {
-            v = acc[0][e] + acc[0][2 + e];
-          }
-          sc[i] = (tok0 - blk + rr[i] < t1) ? v * a.qscale : neg_inf();
-        }
+        sc[e] = vk[e] ? v * a.qscale : neg_inf();
       }
 
       // ------------------------------------------------- online softmax (log2)
-      float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      // The block's 16 tokens of head hd sit in the eight threads of quad
+      // position t.
+      float mb = fmaxf(sc[0], sc[1]);
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
       const float mn = fmaxf(m_run, mb);                 // finite: row tok0 is valid
       if (mn > m_run) {
         const float alpha = fast_exp2(m_run - mn);
         l_part *= alpha;
         zacc *= alpha;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          oacc[nt][0] *= alpha; oacc[nt][1] *= alpha; oacc[nt][2] *= alpha; oacc[nt][3] *= alpha;
+        for (int mt = 0; mt < MT; ++mt) {
+          oacc[mt][0] *= alpha; oacc[mt][1] *= alpha; oacc[mt][2] *= alpha; oacc[mt][3] *= alpha;
         }
         m_run = mn;
+      }
+      float p[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        p[e] = fast_exp2(sc[e] - mn);
+        l_part += p[e];
       }
       // Rows past the split's end were copied as whatever the buffer holds:
       // their weight is 0, and their value scale / zero (or fp16 values) are
@@ -411,23 +466,17 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
       bool vok[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
-      float p[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        p[i] = fast_exp2(sc[i] - mn);
-        l_part += p[i];
-      }
       __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);
       if constexpr (V_AFF) {
         const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
         const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
         if (vfold) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float si = vok[i] ? __half2float(vs[rr[i]]) : 0.0f;
-            const float zi = vok[i] ? __half2float(vz[rr[i]]) : 0.0f;
-            zacc = fmaf(p[i], zi, zacc);
-            p[i] *= si;
+          for (int e = 0; e < 2; ++e) {
+            const float si = vk[e] ? __half2float(vs[rk[e]]) : 0.0f;
+            const float zi = vk[e] ? __half2float(vz[rk[e]]) : 0.0f;
+            zacc = fmaf(p[e], zi, zacc);
+            p[e] *= si;
           }
         } else {
           const __half h0 = __ushort_as_half(0);
@@ -437,48 +486,57 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
           zCD = __halves2half2(vok[2] ? vz[rr[2] * vng + vgi] : h0, vok[3] ? vz[rr[3] * vng + vgi] : h0);
         }
       }
-      // ------------------------------------------------------------ O += P V
-      uint32_t pa[4];
+      // ---------------------------------------------------- O^T += V^T P^T
+      // P^T as the B operand: the thread holds (fp16 part, residual) of head
+      // hd for tokens g and g + 8, the accumulator layout of the 16 x 8 matrix
+      // P^T; one transpose per 8-row half gives the fragment layout.
+      uint32_t pb[2];
       {
-        const __half2 ph0 = __floats2half2_rn(p[0], p[1]);
-        const __half2 ph1 = __floats2half2_rn(p[2], p[3]);
-        const float2 pf0 = __half22float2(ph0);
-        const float2 pf1 = __half22float2(ph1);
-        pa[0] = h2u(ph0);
-        pa[1] = h2u(__floats2half2_rn(p[0] - pf0.x, p[1] - pf0.y));
-        pa[2] = h2u(ph1);
-        pa[3] = h2u(__floats2half2_rn(p[2] - pf1.x, p[3] - pf1.y));
+        const __half2 ph = __floats2half2_rn(p[0], p[1]);
+        const float2 pf = __half22float2(ph);
+        const __half2 pl = __floats2half2_rn(p[0] - pf.x, p[1] - pf.y);
+        pb[0] = movmatrix_t(h2u(__lows2half2(ph, pl)));
+        pb[1] = movmatrix_t(h2u(__highs2half2(ph, pl)));
       }
-      constexpr int NW = VTB / 4;
-      uint32_t A[NW], B[NW], C[NW], E[NW];
+      // The thread's value bytes of its four tokens, in chunks of at most 16
+      // bytes per token.
+      constexpr int NWT = VTB / 4;
+      constexpr int NW = NWT > 4 ? 4 : NWT;
       const uint8_t* vpl = st + TL.vc;
-      lds_row_words<VROW, NW>(A, vpl, rr[0], g * VTB);
-      lds_row_words<VROW, NW>(B, vpl, rr[1], g * VTB);
-      lds_row_words<VROW, NW>(C, vpl, rr[2], g * VTB);
-      lds_row_words<VROW, NW>(E, vpl, rr[3], g * VTB);
-      if constexpr (VB == 16) {
-        if (tok0 + 16 > t1) {   // warp-uniform: only the split's last block
 #pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            A[w] = vok[0] ? A[w] : 0u;
-            B[w] = vok[1] ? B[w] : 0u;
-            C[w] = vok[2] ? C[w] : 0u;
-            E[w] = vok[3] ? E[w] : 0u;
+      for (int w0 = 0; w0 < NWT; w0 += NW) {
+        // keep the next chunk's loads behind this one's MMAs (register pressure)
+        if (w0 > 0) asm volatile("" ::: "memory");
+        uint32_t A[NW], B[NW], C[NW], E[NW];
+        lds_row_words<VROW, NW>(A, vpl, rr[0], g * VTB + 4 * w0);
+        lds_row_words<VROW, NW>(B, vpl, rr[1], g * VTB + 4 * w0);
+        lds_row_words<VROW, NW>(C, vpl, rr[2], g * VTB + 4 * w0);
+        lds_row_words<VROW, NW>(E, vpl, rr[3], g * VTB + 4 * w0);
+        if constexpr (VB == 16) {
+          if (tok0 + 16 > t1) {   // warp-uniform: only the split's last block
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+              A[w] = vok[0] ? A[w] : 0u;
+              B[w] = vok[1] ? B[w] : 0u;
+              C[w] = vok[2] ? C[w] : 0u;
+              E[w] = vok[3] ? E[w] : 0u;
+            }
           }
         }
+        const int mo = w0 * (MT / NWT);
+        if (V_AFF && !vfold)
+          pvt_mma<VB, NW, MT, true>(oacc, pb, mo, A, B, C, E, sAB, zAB, sCD, zCD);
+        else
+          pvt_mma<VB, NW, MT, false>(oacc, pb, mo, A, B, C, E, sAB, zAB, sCD, zCD);
       }
-      if (V_AFF && !vfold)
-        pv_mma<VB, NW, NT, true>(oacc, pa, A, B, C, E, sAB, zAB, sCD, zCD);
-      else
-        pv_mma<VB, NW, NT, false>(oacc, pa, A, B, C, E, sAB, zAB, sCD, zCD);
     }
-    // Release the stage.  The group's last warp to finish it copies the tile
-    // NSTAGE ahead into it (the fences order the four warps' reads of the
+    // Release the stage.  The tile group's last warp to finish it copies the
+    // tile NSTAGE ahead into it (the fences order the warps' reads of the
     // stage before the copy engine's writes).
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
-      if ((atomicAdd(&s_done[stg], 1u) & 3u) == 3u) {
+      if ((atomicAdd(&s_done[stg], 1u) % TW) == TW - 1) {
         __threadfence_block();
         const int nx = it + NSTAGE;
         if (nx < ntiles) {
@@ -503,32 +561,34 @@ __global__ void __launch_bounds__(TcShape<NGRP>::threads, TcShape<NGRP>::ctas_pe
   }
 
   // Per-warp results to shared memory, over the stage ring (every copy has
-  // landed and been read): head g, channel g' * VCH + nt of n-tile nt sits in
-  // column g' = 2t + e, at (d % VCH) * 8 + d / VCH.
+  // landed and been read).  Thread (g, t) holds head hd at its value channels
+  // d = g * VCH + 2 mt + e, stored at (d % VCH) * 8 + d / VCH.
   float(*sm_acc)[G][D + 8] = reinterpret_cast<float(*)[G][D + 8]>(smem);
-  l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
-  l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
-  zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
-  zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
-  if (g < G) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      *reinterpret_cast<float2*>(&sm_acc[warp][g][nt * 8 + 2 * t]) =
-          make_float2((oacc[nt][0] + oacc[nt][2]) + zacc, (oacc[nt][1] + oacc[nt][3]) + zacc);
+  for (int o = 4; o < 32; o <<= 1) {
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+    zacc += __shfl_xor_sync(0xffffffffu, zacc, o);
+  }
+  if (hd < G) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      sm_acc[warp][hd][(2 * mt) * 8 + g] = (oacc[mt][0] + oacc[mt][1]) + zacc;
+      sm_acc[warp][hd][(2 * mt + 1) * 8 + g] = (oacc[mt][2] + oacc[mt][3]) + zacc;
     }
-    if (t == 0) {
-      sm_m[warp][g] = m_run;
-      sm_l[warp][g] = l_part;
+    if (g == 0) {
+      sm_m[warp][hd] = m_run;
+      sm_l[warp][hd] = l_part;
     }
   }
   __syncthreads();
-  merge_store<D, G, 8, NWARP>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
+  merge_store<D, G, 8, NWARP, HG>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
 template <int D, int G, int KF, int VF, int NGRP>
 cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
   const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   using S = TcStages<D, G, KF, VF, NGRP>;
+  using Shape = typename S::Shape;
   const int smem = S::dyn_bytes(L.bytes);
   static int configured = 0;
   if (!configured) {
@@ -544,7 +604,7 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   // to complete before reading anything.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, c.Hkv, c.B);
-  cfg.blockDim = dim3(TcShape<NGRP>::threads);
+  cfg.blockDim = dim3(Shape::threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];

@@ -45,6 +45,15 @@ __device__ __forceinline__ void nibbles_to_h2(uint32_t w, __half2 (&h)[4]) {
   h[3] = __hfma2(u2h((w8 & 0x00F000F0u) | M), k16th, kHigh);
 }
 
+// Transpose of an 8 x 8 fp16 matrix held as mma fragments: lane l holds
+// elements (l / 4, 2 (l % 4)) and (l / 4, 2 (l % 4) + 1) of the input and
+// receives the same elements of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // N consecutive fp16 values (N = 1, 2 or 4; 2N-byte aligned) as fp32.
 template <int N>
 __device__ __forceinline__ void load_halves(const uint8_t* p, float (&f)[N]) {

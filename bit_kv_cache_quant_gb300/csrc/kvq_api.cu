@@ -431,7 +431,8 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   a.Hq = n_q_heads;
   a.qscale = softmax_scale * 1.4426950408889634f;
   a.nsplit = decode_nsplit(c);
-  a.wide = (long long)c->cfg.batch * c->cfg.n_kv_heads * a.nsplit <= 2LL * c->sms;
+  // two tile groups: two CTAs per SM, or one with a second head group (over four query heads per kv head)
+  a.wide = (long long)c->cfg.batch * c->cfg.n_kv_heads * a.nsplit <= (G > 4 ? 1LL : 2LL) * c->sms;
   a.partials = need ? static_cast<float*>(workspace) : nullptr;
   const int kf = fmt_code(c->cfg.k_format, c->cfg.k_bits);
   const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);

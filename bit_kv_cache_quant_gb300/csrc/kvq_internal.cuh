@@ -145,8 +145,8 @@ struct DecodeArgs {
   float qscale;      // softmax scale * log2(e)
   float* partials;   // [B*Hkv][nsplit][G][D + kPartialPad] or null when nsplit == 1
   int nsplit;
-  int wide;          // tensor-core kernel: eight warps per CTA (the grid fits in one wave of
-                     // two CTAs per SM) instead of four
+  int wide;          // tensor-core kernel: two tile groups of warps per CTA (the grid fits in
+                     // one wave at the CTAs per SM of that shape) instead of one
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
 // an (D, G) outside the instantiated set.

@@ -110,7 +110,7 @@ def test_peaked_attention_and_custom_scale(kvq):
 
 
 @pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}{p[1]}-{p[3]}{p[4]}")
-@pytest.mark.parametrize("G", [5, 6, 8])
+@pytest.mark.parametrize("G", [5, 6, 7, 8])
 def test_decode_up_to_eight_heads_per_kv_head(kvq, pair, G):
     # bf16 io and head_dim 128 take the tensor-core kernel, which carries up to 8 heads
     cache, oc = _build(kvq, pair, 1, 2, 128, 700, torch.bfloat16, seed=G, bias=pair[0] == "q4_0")
@@ -139,7 +139,9 @@ def test_repeated_calls_are_identical(kvq):
 # kv head) pairs and the cache length.  On a 152-SM GB300 these cases land on
 # each shape: eight-warp CTAs with a global split merge (the grid fits one
 # wave at two CTAs per SM), with one or many splits; four-warp CTAs (larger
-# grids).  Whatever the shape, the result must match the oracle.
+# grids).  Over four query heads per kv head (G = 8 here) every CTA carries a
+# second head group of warps over the same tiles, and the one-wave shape
+# holds one CTA per SM.  Whatever the shape, the result must match the oracle.
 LAUNCH_SHAPES = [
     ("eight_warps_32_splits", 1, 8, 8192 + 37, None),
     ("eight_warps_4_splits", 2, 4, 300, None),
