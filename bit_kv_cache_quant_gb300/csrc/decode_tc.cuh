@@ -134,7 +134,7 @@ __device__ __forceinline__ void pvt_mma(float (&oacc)[MT][4], const uint32_t (&p
 template <int NGRP, int HG> struct TcShape {
   static constexpr int warps = 4 * NGRP * HG;
   static constexpr int threads = 32 * warps;
-  static constexpr int ctas_per_sm = 4 / (NGRP * HG);
+  static constexpr int ctas_per_sm = NGRP * HG == 1 ? kTcCtasPerSm : 4 / (NGRP * HG);
 };
 
 template <int G> struct TcHeads {
@@ -147,9 +147,12 @@ template <int G> struct TcHeads {
 // many stages (a multiple of NGRP, up to 8) as fit next to the static shared
 // memory, so that a short split is requested in one go.
 template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
+  // largest stage: key scale groups of 32 channels, value groups of D / 8
+  static constexpr int kng_max = D / 32;
+  static constexpr int vng_max = 8;
   static constexpr int stage = ((64 * D * FmtBits<KF>::v / 8 + 64 * D * FmtBits<VF>::v / 8 +
-                                 ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * (D / 32) * 2 +
-                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * (D / 16) * 2) +
+                                 ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * kng_max * 2 +
+                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * vng_max * 2) +
                                 1023) / 1024 * 1024;
   using Shape = TcShape<NGRP, TcHeads<G>::hg>;
   static constexpr int warps = Shape::warps;
@@ -590,11 +593,12 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   using S = TcStages<D, G, KF, VF, NGRP>;
   using Shape = typename S::Shape;
   const int smem = S::dyn_bytes(L.bytes);
+  static_assert(S::dyn_bytes(S::stage) + S::static_smem <= 227 * 1024, "shared memory per CTA");
   static int configured = 0;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, KF, VF, NGRP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::dyn_bytes(tc_layout<D, KF, VF>(D / 16, D / 16).bytes));
+                                         S::dyn_bytes(tc_layout<D, KF, VF>(S::kng_max, S::vng_max).bytes));
     if (e != cudaSuccess) return e;
     configured = 1;
   }
@@ -619,8 +623,10 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
 
 template <int D, int G, int KF, int VF>
 cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
-  return a.wide ? launch_decode_tc_shape<D, G, KF, VF, 2>(c, a, st) : launch_decode_tc_shape<D, G, KF, VF, 1>(c, a, st);
+  DecodeArgs at = a;
+  at.nsplit = a.nsplit_tc;
+  if (at.nsplit < 1 || at.nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  return a.wide ? launch_decode_tc_shape<D, G, KF, VF, 2>(c, at, st) : launch_decode_tc_shape<D, G, KF, VF, 1>(c, at, st);
 }
 
 template <int D, int KF, int VF>

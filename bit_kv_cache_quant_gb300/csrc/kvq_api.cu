@@ -240,6 +240,37 @@ int decode_nsplit(const kvq_cache_s* c) {
   return ns;
 }
 
+// Launch plan of kvq_decode_attn for G query heads per kv head.  nsplit
+// (decode_nsplit) drives the CUDA-core kernel and decides the tensor-core
+// kernel's shape: eight-warp CTAs when that grid fits in one wave (wide), with
+// the same splits; otherwise four-warp CTAs (kTcCtasPerSm per SM; eight-warp,
+// two per SM, over four heads per kv head) with as many splits as fill two
+// whole waves without starting a third.
+struct DecodePlan {
+  int nsplit;
+  int nsplit_tc;
+  int wide;
+};
+
+DecodePlan decode_plan(const kvq_cache_s* c, int G) {
+  DecodePlan p;
+  p.nsplit = decode_nsplit(c);
+  const long long units = (long long)c->cfg.batch * c->cfg.n_kv_heads;
+  p.wide = units * p.nsplit <= (G > 4 ? 1LL : 2LL) * c->sms;
+  p.nsplit_tc = p.nsplit;
+  if (!p.wide) {
+    const long long slots = 2LL * (G > 4 ? 2 : kvq::kTcCtasPerSm) * c->sms;
+    int rows = c->cfg.capacity;
+    if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);
+    const int min_rows = rows >= 4096 ? 256 : 64;
+    long long ns = slots / units;
+    if (ns > rows / min_rows) ns = rows / min_rows;
+    if (ns > kvq::kMaxSplits) ns = kvq::kMaxSplits;
+    p.nsplit_tc = ns < 1 ? 1 : (int)ns;
+  }
+  return p;
+}
+
 size_t live_bytes(const kvq_cache_s* c, int stored) {
   const kvq_config& f = c->cfg;
   const size_t BH = (size_t)f.batch * f.n_kv_heads;
@@ -401,9 +432,10 @@ kvq_status kvq_evict(kvq_cache c, int32_t mode, const int32_t* keep_idx, int32_t
 
 size_t kvq_decode_workspace_bytes(kvq_cache c, int32_t n_q_heads) {
   if (!c || n_q_heads < 1 || n_q_heads % c->cfg.n_kv_heads) return 0;
-  const int ns = decode_nsplit(c);
-  if (ns == 1) return 0;
   const size_t G = n_q_heads / c->cfg.n_kv_heads;
+  const DecodePlan p = decode_plan(c, (int)G);
+  const int ns = p.nsplit > p.nsplit_tc ? p.nsplit : p.nsplit_tc;
+  if (ns == 1) return 0;
   return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + kvq::kPartialPad) * sizeof(float);
 }
 
@@ -430,9 +462,10 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   a.io_dtype = io_dtype;
   a.Hq = n_q_heads;
   a.qscale = softmax_scale * 1.4426950408889634f;
-  a.nsplit = decode_nsplit(c);
-  // two tile groups: two CTAs per SM, or one with a second head group (over four query heads per kv head)
-  a.wide = (long long)c->cfg.batch * c->cfg.n_kv_heads * a.nsplit <= (G > 4 ? 1LL : 2LL) * c->sms;
+  const DecodePlan plan = decode_plan(c, G);
+  a.nsplit = plan.nsplit;
+  a.nsplit_tc = plan.nsplit_tc;
+  a.wide = plan.wide;
   a.partials = need ? static_cast<float*>(workspace) : nullptr;
   const int kf = fmt_code(c->cfg.k_format, c->cfg.k_bits);
   const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);

@@ -144,7 +144,8 @@ struct DecodeArgs {
   int Hq;
   float qscale;      // softmax scale * log2(e)
   float* partials;   // [B*Hkv][nsplit][G][D + kPartialPad] or null when nsplit == 1
-  int nsplit;
+  int nsplit;        // splits per (b, kv head): the CUDA-core kernel's grid x extent
+  int nsplit_tc;     // the same for the tensor-core kernel
   int wide;          // tensor-core kernel: two tile groups of warps per CTA (the grid fits in
                      // one wave at the CTAs per SM of that shape) instead of one
 };
@@ -163,6 +164,7 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
 constexpr int kSnapChunk = 256;   // keys per CTA of the SnapKV scoring kernels
 constexpr int kTmaRows = 64;      // rows per TMA box of a code plane (one decode tile)
 constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)
+constexpr int kTcCtasPerSm = 4;   // tensor-core decode, four-warp CTAs resident per SM (five measured slower: 96 registers)
 constexpr int kPartialPad = 4;    // decode partial row: D accumulators, max, sum, 2 pad (16-byte rows)
 
 }  // namespace kvq
