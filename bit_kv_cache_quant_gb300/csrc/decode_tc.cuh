@@ -63,7 +63,8 @@ __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* 
 // B = the transposed probabilities pb.  Codes are
 // dequantised to fp16 in registers with each token's scale and zero when DEQ,
 // else taken as exact integers (the scale then sits in pb and the zero in a
-// separate sum).
+// separate sum); 8-bit codes then enter as 1024 + u, the caller's zero sum
+// carrying -1024 times the scale.
 // The NW words are words mo / (m-tiles per word) onward of the thread's value
 // bytes; they feed m-tiles mo onward.
 template <int VB, int NW, int MT, bool DEQ>
@@ -104,11 +105,15 @@ __device__ __forceinline__ void pvt_mma(float (&oacc)[MT][4], const uint32_t (&p
       for (int half = 0; half < 2; ++half) {
         const uint32_t sel = half ? 0x7362u : 0x5140u;
         __half2 l0, h0, l1, h1;
-        bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
-        bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
         if constexpr (DEQ) {
+          bytes_to_h2(__byte_perm(a_, b_, sel), l0, h0);       // channels 4 wi + 2 half + 0 / 1
+          bytes_to_h2(__byte_perm(c_, e_, sel), l1, h1);
           l0 = __hfma2(l0, sAB, zAB); h0 = __hfma2(h0, sAB, zAB);
           l1 = __hfma2(l1, sCD, zCD); h1 = __hfma2(h1, sCD, zCD);
+        } else {
+          // 1024 + u: the offset leaves through the zero sum (see the vfold step)
+          bytes_to_h2_1024(__byte_perm(a_, b_, sel), l0, h0);
+          bytes_to_h2_1024(__byte_perm(c_, e_, sel), l1, h1);
         }
         const uint32_t va[4] = {h2u(l0), h2u(h0), h2u(l1), h2u(h1)};
         mma_f16(oacc[mo + 2 * wi + half], va, pb[0], pb[1]);
@@ -161,7 +166,8 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
   static constexpr int static_smem = 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 + (D / 32) * 32 + 1024;
   static constexpr int budget = 227 * 1024 / Shape::ctas_per_sm - 2048 - static_smem;
   static constexpr int raw = (budget / stage) / NGRP * NGRP;
-  static constexpr int v = (NGRP == 1 && Shape::ctas_per_sm > 1) ? 2 : (raw < 2 ? 2 : (raw > 8 ? 8 : raw));
+  static constexpr int cap = NGRP == 1 ? kTcStagesNarrow : 8;
+  static constexpr int v = raw < 2 ? 2 : (raw > cap ? cap : raw);
   // dynamic shared memory for a stage size (+ 1 KB to align the ring to 1024)
   static constexpr int dyn_bytes(int stage_bytes) {
     return (v * stage_bytes > acc_bytes ? v * stage_bytes : acc_bytes) + 1024;
@@ -442,25 +448,31 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       // ------------------------------------------------- online softmax (log2)
       // The block's 16 tokens of head hd sit in the eight threads of quad
       // position t.
+      // The block's scores are weighed against the running max; only when one
+      // of them exceeds it (one vote for the warp's four heads) is the block
+      // max reduced and the state rescaled, which gives the same result as
+      // doing so every block.
       float mb = fmaxf(sc[0], sc[1]);
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-      const float mn = fmaxf(m_run, mb);                 // finite: row tok0 is valid
-      if (mn > m_run) {
-        const float alpha = fast_exp2(m_run - mn);
-        l_part *= alpha;
-        zacc *= alpha;
+      if (__any_sync(0xffffffffu, mb > m_run)) {
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+        const float mn = fmaxf(m_run, mb);               // finite: row tok0 is valid
+        if (mn > m_run) {
+          const float alpha = fast_exp2(m_run - mn);
+          l_part *= alpha;
+          zacc *= alpha;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          oacc[mt][0] *= alpha; oacc[mt][1] *= alpha; oacc[mt][2] *= alpha; oacc[mt][3] *= alpha;
+          for (int mt = 0; mt < MT; ++mt) {
+            oacc[mt][0] *= alpha; oacc[mt][1] *= alpha; oacc[mt][2] *= alpha; oacc[mt][3] *= alpha;
+          }
+          m_run = mn;
         }
-        m_run = mn;
       }
       float p[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        p[e] = fast_exp2(sc[e] - mn);
+        p[e] = fast_exp2(sc[e] - m_run);
         l_part += p[e];
       }
       // Rows past the split's end were copied as whatever the buffer holds:
@@ -477,7 +489,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float si = vk[e] ? __half2float(vs[rk[e]]) : 0.0f;
-            const float zi = vk[e] ? __half2float(vz[rk[e]]) : 0.0f;
+            float zi = vk[e] ? __half2float(vz[rk[e]]) : 0.0f;
+            if constexpr (VB == 8) zi = fmaf(-1024.0f, si, zi);   // 8-bit codes enter as 1024 + u
             zacc = fmaf(p[e], zi, zacc);
             p[e] *= si;
           }

@@ -77,6 +77,12 @@ __device__ __forceinline__ void bytes_to_h2(uint32_t x, __half2& lo, __half2& hi
   hi = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x7362u)), k1024);
 }
 
+// The same pairs as fp16 1024 + b (exact), without the subtraction.
+__device__ __forceinline__ void bytes_to_h2_1024(uint32_t x, __half2& lo, __half2& hi) {
+  lo = u2h(__byte_perm(x, 0x64646464u, 0x5140u));
+  hi = u2h(__byte_perm(x, 0x64646464u, 0x7362u));
+}
+
 // Logical k index j of a 16-token block -> physical row inside the block.
 // The value fragments of quad thread t read rows tau(2t), tau(2t + 1),
 // tau(2t + 8), tau(2t + 9); the order is chosen so those reads are free of
