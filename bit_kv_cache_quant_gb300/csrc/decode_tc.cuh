@@ -347,7 +347,6 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
                      blk + tau<VROW>(2 * t + 9)};
 
   for (int it = grp; it < ntiles; it += NGRP) {
-    if (__any_sync(0xffffffffu, s_fail)) break;
     const int stg = it % NSTAGE;
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar[stg], (it / NSTAGE) & 1))) {
       s_fail = 1;
@@ -407,13 +406,12 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         float v = 0.0f;
         if constexpr (K_Q40) {
           // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
-          float d[NB];
+          float d[NB], x[NB];
           load_halves<NB>(st + TL.ks + rk[e] * (2 * NB), d);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            v = fmaf(d[nb], acc[nb][2 * e], v);
-            v = fmaf(d[nb], acc[nb][2 * e + 1], v);
-          }
+          for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][2 * e] + acc[nb][2 * e + 1];
+          v = fmaf(d[1], x[1], d[0] * x[0]);
+          if constexpr (NB == 4) v += fmaf(d[3], x[3], d[2] * x[2]);
         } else if constexpr (K_AFF) {
           // s * sum(q u) + z * sum(q) per scale group of 32, 64 or 128 channels
           float x[NB];
@@ -547,13 +545,13 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       }
     }
     // Release the stage.  The tile group's last warp to finish it copies the
-    // tile NSTAGE ahead into it (the fences order the warps' reads of the
-    // stage before the copy engine's writes).
+    // tile NSTAGE ahead into it (the warp barrier, the acquire-release count
+    // and the proxy fence order every warp's reads of the stage before the
+    // copy engine's writes).  A warp whose wait ran out stops; the others' waits
+    // then run out in turn.
     __syncwarp();
     if (lane == 0) {
-      __threadfence_block();
-      if ((atomicAdd(&s_done[stg], 1u) % TW) == TW - 1) {
-        __threadfence_block();
+      if ((atom_add_acq_rel_cta(&s_done[stg], 1u) % TW) == TW - 1) {
         const int nx = it + NSTAGE;
         if (nx < ntiles) {
           fence_async_smem();

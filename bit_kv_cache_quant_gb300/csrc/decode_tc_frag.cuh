@@ -153,6 +153,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity) 
   return true;
 }
 
+// Shared-memory add with acquire-release semantics at CTA scope; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_cta(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 // 64 rows of a code plane starting at row y (TMA tensor copy, swizzled).
