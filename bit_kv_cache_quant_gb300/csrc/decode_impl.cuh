@@ -154,6 +154,13 @@ __device__ __forceinline__ void split_rows(int T, int nsplit, int split, int& t0
   t1 = min(T, t0 + tps * kTileTokens);
 }
 
+// Global add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Threads per output float4 in the cross-split merge: the largest of 8, 4, 2
 // that fits the CTA with a whole number of warps, else 1.
 __host__ __device__ constexpr int merge_lanes(int items, int threads) {
@@ -214,13 +221,13 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   if (nse == 1) return;
 
   // The last split of this (b, kv head) to finish merges all partials.  The
-  // barrier orders every thread's partial stores before thread 0's device-scope
-  // fence, which orders them before its arrival.
+  // barrier orders every thread's partial stores before thread 0's arrival,
+  // whose release side publishes them at GPU scope and whose acquire side
+  // (for the last arrival) makes the other splits' partials visible to the
+  // whole CTA after the second barrier.
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const bool last = atomicAdd(&c.split_sem[bh], 1u) == (unsigned)(nse - 1);
-    if (last) __threadfence();   // the other splits' partials are visible to the whole CTA after the barrier
+    const bool last = atom_add_acq_rel_gpu(&c.split_sem[bh], 1u) == (unsigned)(nse - 1);
     s_last = last;
   }
   __syncthreads();

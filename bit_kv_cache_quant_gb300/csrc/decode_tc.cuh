@@ -248,12 +248,30 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const int hg = (warp >> 2) % HG;
   const int grp = (warp >> 2) / HG;
   const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
-  // Thread 0 reads the stored length while the query fragments are built.
+  // Thread 0 reads the stored length and requests each tile group's first
+  // tile (alone, so that it reaches the SM ahead of the rest of the split,
+  // which every CTA would otherwise ask for at the same moment) while the
+  // query fragments are built.
   // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
   // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
   // columns and q enters exactly.  Thread (g, t) builds column g at the key
   // channels of its fragment slots.
-  if (threadIdx.x == 0) s_T = c.state->stored;
+  if (threadIdx.x == 0) {
+    const int T0 = c.state->stored;
+    s_T = T0;
+    int a0, a1, ns0;
+    split_rows(T0, a.nsplit, split, a0, a1, ns0);
+    if (split < ns0) {
+      const int nt0 = (a1 - a0 + kTileTokens - 1) / kTileTokens;
+#pragma unroll
+      for (int gp = 0; gp < NGRP; ++gp) {
+        if (gp < nt0) {
+          issue_tile_tma<D, KF, VF>(smem + gp * TL.bytes, TL, c, bh, a0 + gp * kTileTokens, &mbar[gp]);
+          s_last_tile[gp] = gp;
+        }
+      }
+    }
+  }
   uint32_t qf[KS][2];
   {
     const int hq = 4 * hg + (g >> 1);
@@ -303,15 +321,9 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   split_rows(T, a.nsplit, split, t0, t1, nse);
   if (split >= nse) return;   // no rows for this split (no copy was issued)
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
-  // Each tile group's first tile is requested alone, so that it reaches the
-  // SM ahead of the rest of the split (which every CTA would otherwise ask
-  // for at the same moment); the group's first warp requests the group's
-  // other initial tiles once that tile has landed.
+  // The group's first warp requests the group's other initial tiles once
+  // its first tile has landed.
   const bool leader = (warp % TW) == 0 && lane == 0;
-  if (leader && grp < ntiles) {
-    issue_tile_tma<D, KF, VF>(smem + grp * TL.bytes, TL, c, bh, t0 + grp * kTileTokens, &mbar[grp]);
-    s_last_tile[grp] = grp;
-  }
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 

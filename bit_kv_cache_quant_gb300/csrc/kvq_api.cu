@@ -259,7 +259,7 @@ DecodePlan decode_plan(const kvq_cache_s* c, int G) {
   p.wide = units * p.nsplit <= (G > 4 ? 1LL : 2LL) * c->sms;
   p.nsplit_tc = p.nsplit;
   if (!p.wide) {
-    const long long slots = 2LL * (G > 4 ? 2 : kvq::kTcCtasPerSm) * c->sms;
+    const long long slots = (long long)kvq::kTcWaves * (G > 4 ? 2 : kvq::kTcCtasPerSm) * c->sms;
     int rows = c->cfg.capacity;
     if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);
     const int min_rows = rows >= 4096 ? 256 : 64;

@@ -165,6 +165,7 @@ constexpr int kSnapChunk = 256;   // keys per CTA of the SnapKV scoring kernels
 constexpr int kTmaRows = 64;      // rows per TMA box of a code plane (one decode tile)
 constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)
 constexpr int kTcStagesNarrow = 2;   // tensor-core decode, four-warp CTAs: pipeline stages at most
+constexpr int kTcWaves = 2;       // tensor-core decode, four-warp CTAs: waves of CTAs the splits fill
 constexpr int kTcCtasPerSm = 4;   // tensor-core decode, four-warp CTAs resident per SM (five measured slower: 96 registers)
 constexpr int kPartialPad = 4;    // decode partial row: D accumulators, max, sum, 2 pad (16-byte rows)
 
