@@ -215,12 +215,17 @@ __device__ __forceinline__ void issue_tile_tma(uint8_t* st, const TileLayout& L,
   }
 }
 
-// Stage layout with every stage a multiple of 1024 bytes (the 128-byte swizzle
-// pattern repeats every 1024 bytes and needs its destination aligned to it).
+// Stage layout: the planes placed for the largest group counts the kernel
+// accepts (key scale groups of 32 channels, value groups of D / 8), so that
+// every offset and the stage size are compile-time constants, with every
+// stage a multiple of 1024 bytes (the 128-byte swizzle pattern repeats every
+// 1024 bytes and needs its destination aligned to it); tx is what one tile of
+// this cache actually copies.
 template <int D, int KF, int VF>
 __host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
-  TileLayout L = tile_layout<D, KF, VF>(kng, vng);
+  TileLayout L = tile_layout<D, KF, VF>(D / 32, 8);
   L.bytes = (L.bytes + 1023) / 1024 * 1024;
+  L.tx = tile_layout<D, KF, VF>(kng, vng).bytes;
   return L;
 }
 
