@@ -35,6 +35,8 @@
 // Codes become fp16 through the mantissa of 1024.0 (see nibbles_to_h2).
 #pragma once
 
+#include <type_traits>
+
 #include "decode_tc_frag.cuh"
 
 namespace kvq {
@@ -372,7 +374,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     }
     const uint8_t* st = smem + stg * TL.bytes;
     const int tok0 = t0 + it * kTileTokens + blk;
-    if (tok0 < t1) {   // warp-uniform
+    // Blocks wholly inside the split skip the row masks; the last block of
+    // the split (rows past its end) takes them.
+    auto block = [&](auto masked) {
+      constexpr bool MASK = decltype(masked)::value;
       // ------------------------------------------------------ S^T = K Q^T
       // acc[.][2e + j]: token rk[e], column 2j (j = 0: fp16 part, 1: residual)
       float acc[NACC][4];
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       float sc[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        vk[e] = tok0 - blk + rk[e] < t1;
+        vk[e] = !MASK || tok0 - blk + rk[e] < t1;
         float v = 0.0f;
         if constexpr (K_Q40) {
           // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       // zeroed so that no NaN reaches the MMA.
       bool vok[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) vok[i] = tok0 - blk + rr[i] < t1;
+      for (int i = 0; i < 4; ++i) vok[i] = !MASK || tok0 - blk + rr[i] < t1;
       __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);
       if constexpr (V_AFF) {
         const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         lds_row_words<VROW, NW>(C, vpl, rr[2], g * VTB + 4 * w0);
         lds_row_words<VROW, NW>(E, vpl, rr[3], g * VTB + 4 * w0);
         if constexpr (VB == 16) {
-          if (tok0 + 16 > t1) {   // warp-uniform: only the split's last block
+          if (MASK) {   // only the split's last block
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
               A[w] = vok[0] ? A[w] : 0u;
@@ -555,7 +560,9 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         else
           pvt_mma<VB, NW, MT, false>(oacc, pb, mo, A, B, C, E, sAB, zAB, sCD, zCD);
       }
-    }
+    };
+    if (tok0 + 16 <= t1) block(std::false_type{});
+    else if (tok0 < t1) block(std::true_type{});   // warp-uniform
     // Release the stage.  The tile group's last warp to finish it copies the
     // tile NSTAGE ahead into it (the warp barrier, the acquire-release count
     // and the proxy fence order every warp's reads of the stage before the
