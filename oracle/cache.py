@@ -11,6 +11,15 @@ buffer, written here independently from that description):
 * per-channel metadata (KIVI keys) ``[B, Hkv, D]`` fp16 scale and zero, plus
   the fp32 values the codes were computed from.
 
+KIVI residual buffer (MLX memo, section 3, "What KIVI and KVQuant found";
+k_format "kivi_block", k_group = R): the most recent tokens stay at full
+precision in a tail of fewer than R rows (fp32, the values the caller gave);
+whenever the tail reaches R tokens its keys are quantised per channel over
+exactly those R tokens (a closed block: its own KIVI scale and zero per
+channel, fp16 planes [B, Hkv, cap / R, D]) and its values per token, the
+codes go to the next R rows of the quantised bulk and the tail empties.
+Attention runs over the dequantised bulk followed by the exact tail.
+
 Eviction, from "StreamingLLM + KIVI" ("Implementation"): when the stored
 length exceeds sink + window, logical positions [sink, len - window) are
 dropped and the rest is concatenated in order; K's per-channel scales are
@@ -39,7 +48,7 @@ class CacheSpec:
     layout: str = "linear"          # "linear" | "compact" | "ring"
     sink: int = 0
     window: int = 0
-    k_format: str = "fp16"          # "fp16" | "kivi_chan" | "affine_token" | "q4_0"
+    k_format: str = "fp16"          # "fp16" | "kivi_chan" | "affine_token" | "q4_0" | "kivi_block"
     k_bits: int = 16
     k_group: int = 0
     v_format: str = "fp16"          # "fp16" | "affine_token"
@@ -88,6 +97,10 @@ class _Side:
         self.ch_zero = np.zeros((B, H, D), np.float16) if fmt == "kivi_chan" else None
         self.ch_scale32 = None
         self.ch_zero32 = None
+        # closed-block per-channel metadata (kivi_block keys; group = block length R)
+        nblk = cap // group if fmt == "kivi_block" else 0
+        self.blk_scale = np.zeros((B, H, nblk, D), np.float16) if nblk else None
+        self.blk_zero = np.zeros((B, H, nblk, D), np.float16) if nblk else None
 
     # per-token planes move with their token on eviction
     def token_planes(self):
@@ -139,6 +152,9 @@ class _Side:
         u = self.codes(n)
         if self.fmt == "kivi_chan":
             return qz.dequant_affine(u, self.ch_scale[:, :, None, :], self.ch_zero[:, :, None, :])
+        if self.fmt == "kivi_block":
+            blk = np.arange(n) // self.group
+            return qz.dequant_affine(u, self.blk_scale[:, :, blk, :], self.blk_zero[:, :, blk, :])
         if self.fmt == "affine_token":
             g = self.group
             ug = u.reshape(B, H, n, D // g, g)
@@ -163,7 +179,14 @@ class OracleCache:
         self.k = _Side(spec, spec.k_format, spec.k_bits, spec.k_group)
         self.v = _Side(spec, spec.v_format, spec.v_bits, spec.v_group)
         self.pos = 0        # absolute position of the next token (tokens seen)
-        self.stored = 0     # physical rows holding live tokens
+        self.stored = 0     # physical rows holding live tokens (the quantised bulk)
+        if spec.k_format == "kivi_block":
+            if spec.layout != "linear" or spec.k_group < 1 or spec.v_format != "affine_token":
+                raise ValueError("kivi_block keys need a linear layout, k_group >= 1 and affine_token values")
+            B, H, D, R = spec.batch, spec.n_kv_heads, spec.head_dim, spec.k_group
+            self.tail_k = np.zeros((B, H, R, D), np.float32)   # full-precision recent tokens
+            self.tail_v = np.zeros((B, H, R, D), np.float32)
+            self.n_tail = 0
 
     def calibrate_k(self, k: np.ndarray):
         """Freeze per-channel K scales from k [B,H,n,D] (fp32 values of the io dtype)."""
@@ -175,6 +198,9 @@ class OracleCache:
         k = np.asarray(k, np.float32)
         v = np.asarray(v, np.float32)
         n = k.shape[2]
+        if spec.k_format == "kivi_block":
+            self._append_residual(k, v)
+            return
         kr, ks, kz = self.k.encode(k, spec.k_bias)
         vr, vs, vz = self.v.encode(v, None)
         if spec.layout == "ring":
@@ -196,6 +222,38 @@ class OracleCache:
                     side.tok_scale[:, :, slot] = sc[:, :, i]
                 if zr is not None:
                     side.tok_zero[:, :, slot] = zr[:, :, i]
+        self.pos += n
+
+    def _append_residual(self, k: np.ndarray, v: np.ndarray):
+        """KIVI residual buffer: the tail followed by the new tokens, taken in order; every
+        run of R tokens that completes is a closed block, quantised and moved to the bulk;
+        the rest stays in the tail.  Call boundaries do not matter."""
+        spec = self.spec
+        R = spec.k_group
+        n = k.shape[2]
+        seq_k = np.concatenate([self.tail_k[:, :, : self.n_tail], k], axis=2)
+        seq_v = np.concatenate([self.tail_v[:, :, : self.n_tail], v], axis=2)
+        nb = seq_k.shape[2] // R
+        if self.stored + nb * R > spec.capacity:
+            raise OverflowError("append beyond capacity")
+        for j in range(nb):
+            bk = seq_k[:, :, j * R:(j + 1) * R]
+            bv = seq_v[:, :, j * R:(j + 1) * R]
+            s32, z32 = qz.kivi_channel_calibrate(bk, spec.k_bits)
+            u = qz.kivi_channel_codes(bk, s32, z32, spec.k_bits)
+            r0 = self.stored
+            self.k.rows[:, :, r0:r0 + R] = self.k._pack(u)
+            self.k.blk_scale[:, :, r0 // R] = qz.to_fp16(s32)
+            self.k.blk_zero[:, :, r0 // R] = qz.to_fp16(z32)
+            vr, vs, vz = self.v.encode(bv, None)
+            self.v.rows[:, :, r0:r0 + R] = vr
+            self.v.tok_scale[:, :, r0:r0 + R] = vs
+            self.v.tok_zero[:, :, r0:r0 + R] = vz
+            self.stored += R
+        rest = seq_k.shape[2] - nb * R
+        self.tail_k[:, :, :rest] = seq_k[:, :, nb * R:]
+        self.tail_v[:, :, :rest] = seq_v[:, :, nb * R:]
+        self.n_tail = rest
         self.pos += n
 
     def append_recompute_k(self, k: np.ndarray, v: np.ndarray):
@@ -257,5 +315,10 @@ class OracleCache:
         self.stored = n_keep
 
     def dequant(self):
-        """float64 K-hat, V-hat [B,H,stored,D] of the live rows."""
-        return self.k.dequant(self.stored), self.v.dequant(self.stored)
+        """float64 K-hat, V-hat [B,H,stored,D] of the live rows (kivi_block keys: the bulk,
+        then the exact tail, [B,H,stored + n_tail,D])."""
+        kh, vh = self.k.dequant(self.stored), self.v.dequant(self.stored)
+        if self.spec.k_format == "kivi_block":
+            kh = np.concatenate([kh, self.tail_k[:, :, : self.n_tail].astype(np.float64)], axis=2)
+            vh = np.concatenate([vh, self.tail_v[:, :, : self.n_tail].astype(np.float64)], axis=2)
+        return kh, vh

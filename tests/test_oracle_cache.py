@@ -278,3 +278,119 @@ def test_recompute_gate():
     x = np.zeros((1, 1, 2, 16), np.float32)
     with pytest.raises(ValueError):
         c.append_recompute_k(x, x)
+
+
+# ------------------------------------------------------------ KIVI residual buffer
+# MLX memo, section 3: recent tokens stay full precision; keys are quantised
+# per channel in closed blocks once the buffer fills; attention runs over the
+# quantised bulk plus the full-precision tail.
+
+def _residual_spec(R=64, bits=4, D=64, cap=512):
+    return CacheSpec(batch=2, n_kv_heads=2, head_dim=D, capacity=cap, k_format="kivi_block", k_bits=bits,
+                     k_group=R, v_format="affine_token", v_bits=4, v_group=32)
+
+
+def _kv(n, seed, D=64, offsets=True):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((2, 2, n, D)).astype(np.float32)
+    if offsets:
+        k += rng.normal(0, 2, (2, 2, 1, D)).astype(np.float32)   # per-channel K offsets
+    v = rng.standard_normal((2, 2, n, D)).astype(np.float32)
+    return k, v
+
+
+def _live(c):
+    return (c.stored, c.n_tail, c.k.rows[:, :, : c.stored].copy(), c.k.blk_scale[:, :, : c.stored // c.spec.k_group].copy(),
+            c.k.blk_zero[:, :, : c.stored // c.spec.k_group].copy(), c.v.rows[:, :, : c.stored].copy(),
+            c.v.tok_scale[:, :, : c.stored].copy(), c.tail_k[:, :, : c.n_tail].copy(), c.tail_v[:, :, : c.n_tail].copy())
+
+
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 200, 448])
+def test_residual_counts(n):
+    c = OracleCache(_residual_spec())
+    k, v = _kv(n, n)
+    c.append(k, v)
+    assert (c.stored, c.n_tail, c.pos) == ((n // 64) * 64, n % 64, n)
+
+
+def test_residual_call_boundaries_do_not_matter():
+    k, v = _kv(300, 1)
+    one = OracleCache(_residual_spec())
+    one.append(k, v)
+    rng = np.random.default_rng(5)
+    cuts = np.sort(rng.choice(np.arange(1, 300), 17, replace=False))
+    chunked = OracleCache(_residual_spec())
+    for a, b in zip(np.r_[0, cuts], np.r_[cuts, 300]):
+        chunked.append(k[:, :, a:b], v[:, :, a:b])
+    steps = OracleCache(_residual_spec())
+    for i in range(300):
+        steps.append(k[:, :, i:i + 1], v[:, :, i:i + 1])
+    for other in (chunked, steps):
+        for x, y in zip(_live(one), _live(other)):
+            assert np.array_equal(x, y)
+
+
+def test_residual_tail_is_exact_and_attention_without_a_block_is_exact():
+    k, v = _kv(50, 2)
+    c = OracleCache(_residual_spec())
+    c.append(k, v)
+    kh, vh = c.dequant()
+    assert c.stored == 0 and np.array_equal(kh, k.astype(np.float64)) and np.array_equal(vh, v.astype(np.float64))
+    q = np.random.default_rng(3).standard_normal((2, 6, 64))
+    assert np.array_equal(att.decode_attention(q, kh, vh), att.decode_attention(q, k.astype(np.float64), v.astype(np.float64)))
+    k2, v2 = _kv(100, 4)
+    c.append(k2, v2)   # 150 tokens: two closed blocks, 22 in the tail
+    kh, vh = c.dequant()
+    allk = np.concatenate([k, k2], axis=2)
+    assert c.stored == 128 and np.array_equal(kh[:, :, 128:], allk[:, :, 128:].astype(np.float64))
+
+
+def test_residual_blocks_are_closed():
+    k, v = _kv(200, 6)
+    base = OracleCache(_residual_spec())
+    base.append(k, v)
+    for lo, hi in ((64, 128), (128, 192), (192, 200)):   # a later block, the last block, the tail
+        k2 = k.copy()
+        k2[:, :, lo:hi] *= 3.0
+        other = OracleCache(_residual_spec())
+        other.append(k2, v)
+        # every block before the perturbed one keeps its codes and scales
+        nb = lo // 64
+        assert np.array_equal(base.k.rows[:, :, : nb * 64], other.k.rows[:, :, : nb * 64])
+        assert np.array_equal(base.k.blk_scale[:, :, :nb], other.k.blk_scale[:, :, :nb])
+        if hi <= 192:
+            assert not np.array_equal(base.k.blk_scale[:, :, nb], other.k.blk_scale[:, :, nb])
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_residual_block_range_ends_and_error_bound(bits):
+    k, v = _kv(256, 7 + bits)
+    c = OracleCache(_residual_spec(bits=bits))
+    c.append(k, v)
+    L = qz.levels(bits)
+    u = c.k.codes(256).astype(np.int64)
+    kh, _ = c.dequant()
+    for j in range(4):
+        blk = k[:, :, 64 * j:64 * (j + 1)]
+        ub = u[:, :, 64 * j:64 * (j + 1)]
+        # each channel's smallest key of the block sits on code 0, its largest on code L
+        amin = blk.argmin(axis=2)[:, :, None, :]
+        amax = blk.argmax(axis=2)[:, :, None, :]
+        assert np.all(np.take_along_axis(ub, amin, 2) == 0)
+        assert np.all(np.take_along_axis(ub, amax, 2) == L)
+        # reconstruction within half a step of the block's own range, plus the fp16 rounding of
+        # the stored scale and zero
+        step = (blk.max(axis=2) - blk.min(axis=2)).astype(np.float64) / L
+        s16 = c.k.blk_scale[:, :, j].astype(np.float64)
+        z16 = c.k.blk_zero[:, :, j].astype(np.float64)
+        tol = step / 2 * (1 + 1e-6) + L * np.abs(s16 - step) + np.abs(z16 - blk.min(axis=2))
+        err = np.abs(kh[:, :, 64 * j:64 * (j + 1)] - blk)
+        assert np.all(err <= tol[:, :, None, :] + 1e-7)
+
+
+def test_residual_needs_linear_layout_and_affine_values():
+    with pytest.raises(ValueError):
+        OracleCache(CacheSpec(1, 1, 64, 256, layout="compact", sink=4, window=128, k_format="kivi_block",
+                              k_bits=4, k_group=64, v_format="affine_token", v_bits=4, v_group=32))
+    with pytest.raises(ValueError):
+        OracleCache(CacheSpec(1, 1, 64, 256, k_format="kivi_block", k_bits=4, k_group=64))
