@@ -84,12 +84,20 @@ def side_token_bytes(fmt, bits, group, D):
 
 
 def decode_bytes(w, T):
-    """Algorithmic bytes of one decode-attention launch (one layer): codes + metadata + Q + O."""
+    """Algorithmic bytes of one decode-attention launch (one layer): codes + metadata + Q + O.
+    A residual buffer (kivi_block keys) holding T tokens reads its closed blocks as codes plus one
+    fp16 scale and zero per (block, channel), and its T mod R tail rows as fp32 K and V."""
     io = torch.empty((), dtype=synth.torch_dtype(w.io_dtype)).element_size()
+    tail = 0
+    if w.k_format == "kivi_block":
+        tail = T % w.k_group
+        T -= tail
     per_head = T * (side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
                     + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
     if w.k_format == "kivi_chan":
         per_head += 4 * w.head_dim
+    if w.k_format == "kivi_block":
+        per_head += (T // w.k_group) * 4 * w.head_dim + tail * 8 * w.head_dim
     return w.batch * w.n_kv_heads * per_head + 2 * w.batch * w.n_q_heads * w.head_dim * io
 
 
@@ -99,6 +107,10 @@ def append_bytes(w, n):
     rows = w.batch * w.n_kv_heads * n
     wr = (side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
           + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
+    if w.k_format == "kivi_block":
+        # the token enters the fp32 tail; each closed block reads its tail rows back once and
+        # writes codes plus the block's per-channel scale and zero (per token, amortised)
+        wr += 8 * w.head_dim + 8 * w.head_dim + 4 * w.head_dim // w.k_group
     return rows * (2 * w.head_dim * io + wr)
 
 
@@ -381,12 +393,13 @@ class OracleSample:
             self.oc.evict_middle()
         kh, vh = self.oc.dequant()
         self.oatt.decode_attention(self.q, kh, vh)
-        return decode_bytes(self.slice_w, self.oc.stored) + append_bytes(self.slice_w, 1)
+        return decode_bytes(self.slice_w, self.oc.stored + getattr(self.oc, "n_tail", 0)) + append_bytes(self.slice_w, 1)
 
     def describe(self):
         w = self.w
+        held = self.oc.stored + getattr(self.oc, "n_tail", 0)
         return (f"layer 0, batch row 0, kv head 0 of {w.name} ({w.group} query heads, "
-                f"{self.oc.stored} stored tokens): append + evict + float64 attention per step")
+                f"{held} stored tokens): append + evict + float64 attention per step")
 
 
 class SnapKVOracleSample:
@@ -491,7 +504,8 @@ def decode_source_sha(kvq_dir):
 
 def decode_kernel_name(w):
     """The decode kernel the library launches for this workload (tensor-core path for 16-bit io, D 64/128)."""
-    return "decode_tc_kernel" if w.io_dtype != "float32" and w.head_dim in (64, 128) else "decode_kernel"
+    tc = w.io_dtype != "float32" and w.head_dim in (64, 128) and w.k_format != "kivi_block"
+    return "decode_tc_kernel" if tc else "decode_kernel"
 
 
 def decode_traffic(w, kvq_dir):
@@ -804,7 +818,7 @@ def per_config(a, kvq):
     the metric is quoted per config.  Each entry holds that workload's bench
     line essentials; a failure is recorded, not raised."""
     out = {}
-    for name in ("tinygpt", "q4_0_32k", "snapkv", "ring"):
+    for name in ("tinygpt", "q4_0_32k", "snapkv", "ring", "residual"):
         w = synth.get_workload(name)
         sub = argparse.Namespace(**vars(a))
         sub.steps, sub.warmup, sub.no_e2e = (20, 3, True) if w.batch > 1 or w.prompt_len else (50, 5, True)

@@ -36,7 +36,7 @@ lib = ctypes.CDLL(LIB_PATH)
 KVQ_OK = 0
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
                 4: "KVQ_ERR_DEVICE", 5: "KVQ_ERR_CUDA"}
-FORMATS = {"fp16": 0, "kivi_chan": 1, "affine_token": 2, "q4_0": 3}
+FORMATS = {"fp16": 0, "kivi_chan": 1, "affine_token": 2, "q4_0": 3, "kivi_block": 4}
 LAYOUTS = {"linear": 0, "compact": 1, "ring": 2}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 EVICT_MIDDLE = 0
@@ -61,12 +61,14 @@ class kvq_cache_layout(Structure):
                 ("k_codes", c_size_t), ("k_tok_scale", c_size_t), ("k_tok_zero", c_size_t),
                 ("k_ch_scale", c_size_t), ("k_ch_zero", c_size_t), ("k_ch_scale32", c_size_t),
                 ("k_ch_zero32", c_size_t), ("k_bias", c_size_t),
-                ("v_codes", c_size_t), ("v_tok_scale", c_size_t), ("v_tok_zero", c_size_t)]
+                ("v_codes", c_size_t), ("v_tok_scale", c_size_t), ("v_tok_zero", c_size_t),
+                ("k_blk_scale", c_size_t), ("k_blk_zero", c_size_t), ("k_tail", c_size_t), ("v_tail", c_size_t)]
 
 
 class kvq_stats(Structure):
     _fields_ = [("pos", c_int64), ("stored", c_int32), ("capacity", c_int32), ("device_status", c_int32),
-                ("k_calibrated", c_int32), ("cache_bytes", c_size_t), ("live_bytes", c_size_t)]
+                ("k_calibrated", c_int32), ("cache_bytes", c_size_t), ("live_bytes", c_size_t),
+                ("tail", c_int32)]
 
 
 def _proto(name, res, *args):

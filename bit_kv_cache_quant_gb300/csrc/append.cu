@@ -337,6 +337,137 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// KIVI residual buffer (KIVI_BLOCK keys; the format's description in kvq.h).
+// The tail (t rows) followed by the n new tokens is one sequence; each run of
+// R that completes is a closed block.  Grid (nbm + 1, B * Hkv), nbm the most
+// blocks an append of n can close: CTA x < nbm codes block x of its (b, kv
+// head) if that block closes; the new tail is written by CTA 0 after its block
+// has read the old tail, or by CTA nbm when no block closes.  The last CTA to
+// arrive advances the counters, once every CTA has read them.
+template <typename T, int E>
+__global__ void __launch_bounds__(256) residual_append_kernel(CacheView c, const T* __restrict__ k,
+                                                              const T* __restrict__ v, int n, long long hstride) {
+  constexpr int D = 32 * E;
+  constexpr int NW = 8;
+  __shared__ long long s_pos;
+  __shared__ int s_stored, s_tail, s_ok;
+  __shared__ float s_part[2][NW][D];   // per-warp channel min / max
+  __shared__ float s_sc[D], s_zr[D];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int R = c.k.group;
+  const size_t bh = blockIdx.y;
+  const int nbm = gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    s_pos = c.state->pos;
+    s_stored = c.state->stored;
+    s_tail = c.state->tail;
+    const int nb = (s_tail + n) / R;
+    const bool ok = s_stored + nb * R <= (c.cap / R) * R;
+    s_ok = ok ? 1 : 0;
+    if (!ok && blockIdx.x == 0 && blockIdx.y == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
+  }
+  __syncthreads();
+  const int t_old = s_tail;
+  const int nb = (t_old + n) / R;
+  const int j = blockIdx.x;
+  // token i of the sequence (tail, then input), this lane's E channels, as fp32
+  auto load_tok = [&](const float* tail, const T* in, int i, float (&x)[E]) {
+    if (i < t_old) {
+      const float* p = tail + (bh * R + i) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = p[e];
+    } else {
+      load_row_slice<T, E>(in + ((long long)bh * hstride + (i - t_old)) * D + lane * E, x);
+    }
+  };
+  if (s_ok && j < nb) {
+    const float levels = (c.k.bits == 8) ? 255.0f : 15.0f;
+    // keys: each channel's range over the block's R tokens
+    float mn[E], mx[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      mn[e] = __int_as_float(0x7f800000);    // +inf
+      mx[e] = __int_as_float(0xff800000);    // -inf
+    }
+    for (int r = warp; r < R; r += NW) {
+      float x[E];
+      load_tok(c.tail_k, k, j * R + r, x);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        mn[e] = fminf(mn[e], x[e]);
+        mx[e] = fmaxf(mx[e], x[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      s_part[0][warp][lane * E + e] = mn[e];
+      s_part[1][warp][lane * E + e] = mx[e];
+    }
+    __syncthreads();
+    const int blk = s_stored / R + j;
+    for (int ch = threadIdx.x; ch < D; ch += blockDim.x) {
+      float a = s_part[0][0][ch], z = s_part[1][0][ch];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) {
+        a = fminf(a, s_part[0][w][ch]);
+        z = fmaxf(z, s_part[1][w][ch]);
+      }
+      const float sc = affine_scale(a, z, levels);
+      s_sc[ch] = sc;
+      s_zr[ch] = a;
+      const size_t mrow = (bh * (c.cap_alloc / R) + blk) * D + ch;
+      c.k.blk_scale[mrow] = __float2half_rn(sc);
+      c.k.blk_zero[mrow] = __float2half_rn(a);
+    }
+    __syncthreads();
+    for (int r = warp; r < R; r += NW) {
+      const int slot = s_stored + j * R + r;
+      float x[E];
+      load_tok(c.tail_k, k, j * R + r, x);
+      int u[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) u[e] = affine_code(x[e], s_sc[lane * E + e], s_zr[lane * E + e], levels);
+      store_codes<E>(c.k.codes + (bh * c.cap_alloc + slot) * c.k.row_bytes, lane, c.k.bits, u);
+      float y[E];
+      load_tok(c.tail_v, v, j * R + r, y);
+      quantize_row<E>(c.v, nullptr, y, bh, c.cap_alloc, slot, lane);
+    }
+  }
+  // the new tail: sequence tokens [nb R, t_old + n) become tail rows 0 ..
+  if (s_ok && (nb == 0 ? j == nbm : j == 0)) {
+    __syncthreads();   // CTA 0's reads of the old tail are done
+    const int first = nb == 0 ? t_old : 0;               // first tail row written
+    const int count = nb == 0 ? n : t_old + n - nb * R;  // rows written (all from the input)
+    const int in0 = nb == 0 ? 0 : nb * R - t_old;        // their first input token
+    for (int r = warp; r < count; r += NW) {
+      float x[E], y[E];
+      load_row_slice<T, E>(k + ((long long)bh * hstride + in0 + r) * D + lane * E, x);
+      load_row_slice<T, E>(v + ((long long)bh * hstride + in0 + r) * D + lane * E, y);
+      float* pk = c.tail_k + (bh * R + first + r) * D + lane * E;
+      float* pv = c.tail_v + (bh * R + first + r) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        pk[e] = x[e];
+        pv[e] = y[e];
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  __threadfence();
+  if (atomicAdd(&c.state->append_arrive, 1u) == gridDim.x * gridDim.y - 1) {
+    if (s_ok) {
+      c.state->pos = s_pos + n;
+      c.state->stored = s_stored + nb * R;
+      c.state->tail = t_old + n - nb * R;
+    }
+    c.state->append_arrive = 0u;
+    __threadfence();
+  }
+}
+
 // ---------------------------------------------------------------- launch --
 
 template <typename T>
@@ -350,10 +481,22 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
     recompute_kivi_kernel<T><<<c.B * c.Hkv, 256, 0, st>>>(c, static_cast<const T*>(k), n, hstride);
     note_launch();
   }
-  const long long rows = (long long)c.B * c.Hkv * n;
-  const unsigned grid = (unsigned)((rows + kAppendWarps - 1) / kAppendWarps);
   const T* kk = static_cast<const T*>(k);
   const T* vv = static_cast<const T*>(v);
+  if (c.k.fmt == KVQ_FMT_KIVI_BLOCK) {
+    const int R = c.k.group;
+    const dim3 grid((unsigned)((R - 1 + n) / R + 1), (unsigned)(c.B * c.Hkv));
+    switch (c.D) {
+      case 32: residual_append_kernel<T, 1><<<grid, 256, 0, st>>>(c, kk, vv, n, hstride); break;
+      case 64: residual_append_kernel<T, 2><<<grid, 256, 0, st>>>(c, kk, vv, n, hstride); break;
+      case 128: residual_append_kernel<T, 4><<<grid, 256, 0, st>>>(c, kk, vv, n, hstride); break;
+      default: return cudaErrorInvalidValue;
+    }
+    note_launch();
+    return cudaGetLastError();
+  }
+  const long long rows = (long long)c.B * c.Hkv * n;
+  const unsigned grid = (unsigned)((rows + kAppendWarps - 1) / kAppendWarps);
   switch (c.D) {
     case 32: append_kernel<T, 1><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
     case 64: append_kernel<T, 2><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;

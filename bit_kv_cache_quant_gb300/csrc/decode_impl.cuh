@@ -42,7 +42,7 @@ constexpr int kDecodeThreads = 32 * kDecodeWarps;
 constexpr int kTileTokens = 64;       // divides kRowAlign: whole tiles stay inside cap_alloc
 
 template <int F> struct FmtBits {
-  static constexpr int v = (F == F_FP16) ? 16 : ((F == F_KIVI8 || F == F_AFF8) ? 8 : 4);
+  static constexpr int v = (F == F_FP16) ? 16 : ((F == F_KIVI8 || F == F_AFF8 || F == F_KIVIB8) ? 8 : 4);
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -115,7 +115,7 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 
 // Byte offsets of one pipeline stage (one 64-token tile) in shared memory.
 struct TileLayout {
-  int kc, vc, ks, kz, vs, vz, bytes;
+  int kc, vc, ks, kz, vs, vz, kbs, kbz, bytes;
   int tx;   // bytes actually transferred into a stage
 };
 
@@ -134,7 +134,12 @@ __host__ __device__ __forceinline__ TileLayout tile_layout(int kng, int vng) {
   L.kz = off; off += K_AFF ? kTileTokens * kng * 2 : 0;
   L.vs = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
   L.vz = off; off += V_AFF ? kTileTokens * vng * 2 : 0;
-  L.bytes = off;   // every term is a multiple of 128 bytes
+  // KIVI_BLOCK keys: the per-channel scale and zero of the tile's block (a tile
+  // never spans two blocks: the block length is a multiple of 64)
+  constexpr bool K_KIVIB = (KF == F_KIVIB8 || KF == F_KIVIB4);
+  L.kbs = off; off += K_KIVIB ? D * 2 : 0;
+  L.kbz = off; off += K_KIVIB ? D * 2 : 0;
+  L.bytes = off;   // every term is a multiple of 64 bytes
   L.tx = off;
   return L;
 }
@@ -373,6 +378,15 @@ __device__ __forceinline__ void issue_tile(uint8_t* st, const TileLayout& L, con
       cp_async16(st + L.vz + 16 * i, s2 + 16 * i);
     }
   }
+  if constexpr (KF == F_KIVIB8 || KF == F_KIVIB4) {
+    const size_t m = (bh * (c.cap_alloc / c.k.group) + row0 / c.k.group) * D;
+    const uint8_t* s1 = reinterpret_cast<const uint8_t*>(c.k.blk_scale + m);
+    const uint8_t* s2 = reinterpret_cast<const uint8_t*>(c.k.blk_zero + m);
+    for (int i = tid; i < D * 2 / 16; i += kDecodeThreads) {
+      cp_async16(st + L.kbs + 16 * i, s1 + 16 * i);
+      cp_async16(st + L.kbz + 16 * i, s2 + 16 * i);
+    }
+  }
 }
 
 template <int D, int G, int KF, int VF>
@@ -390,8 +404,10 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   constexpr bool K_KIVI = (KF == F_KIVI8 || KF == F_KIVI4);
   constexpr bool K_Q40 = (KF == F_Q40);
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  constexpr bool K_KIVIB = (KF == F_KIVIB8 || KF == F_KIVIB4);
 
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_tail;
   __shared__ float sm_m[kDecodeWarps][G];
   __shared__ float sm_l[kDecodeWarps][G];
   __shared__ __align__(16) float sm_acc[kDecodeWarps][G][D];
@@ -408,13 +424,23 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   const int vng = c.v.n_groups;
   const TileLayout TL = tile_layout<D, KF, VF>(kng, vng);
 
-  if (threadIdx.x == 0) s_T = c.state->stored;
+  if (threadIdx.x == 0) {
+    s_T = c.state->stored;
+    s_tail = K_KIVIB ? c.state->tail : 0;
+  }
   __syncthreads();
   const int T = s_T;
   int t0, t1, nse;
   split_rows(T, a.nsplit, split, t0, t1, nse);
-  if (split >= nse) return;   // no rows for this split
-  const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
+  // KIVI_BLOCK: CTA a.nsplit attends over the full-precision tail and merges as
+  // one more split (partial slot nse, after the bulk's); a cache with no
+  // closed block has no bulk splits.
+  const int TT = s_tail;
+  const bool is_tail = K_KIVIB && split == a.nsplit;
+  if (K_KIVIB && T == 0) nse = TT > 0 ? 0 : 1;
+  const int nse_all = nse + (TT > 0 ? 1 : 0);
+  if (is_tail ? TT == 0 : split >= nse) return;   // no rows for this CTA
+  const int ntiles = is_tail ? 0 : (t1 - t0 + kTileTokens - 1) / kTileTokens;
 
   // Start streaming before anything else.
 #pragma unroll
@@ -481,6 +507,13 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
       load_codes_smem<KB>(kc, st + TL.kc + r * KROW + j * (KROW / NL));
       float x[16];
       unpack<KB>(kc, x);
+      if constexpr (K_KIVIB) {
+        // the block's per-channel scale and zero, in fp32: k = s u + z
+        const __half* bs = reinterpret_cast<const __half*>(st + TL.kbs) + 16 * j;
+        const __half* bz = reinterpret_cast<const __half*>(st + TL.kbz) + 16 * j;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = fmaf(__half2float(bs[i]), x[i], __half2float(bz[i]));
+      }
       float ksc = 0.0f, kzr = 0.0f;
       if constexpr (K_AFF || K_Q40) ksc = __half2float(reinterpret_cast<const __half*>(st + TL.ks)[r * kng + kg]);
       if constexpr (K_AFF) kzr = __half2float(reinterpret_cast<const __half*>(st + TL.kz)[r * kng + kg]);
@@ -561,6 +594,45 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   }
   cp_async_wait<0>();
 
+  if constexpr (K_KIVIB) {
+    if (is_tail) {
+      // The fp32 tail rows [0, TT), one token per lane group per step.
+      const float* tk = c.tail_k + bh * c.k.group * D + 16 * j;
+      const float* tv = c.tail_v + bh * c.k.group * D + 16 * j;
+      for (int base = 0; base < TT; base += TPC) {
+        const int r = base + slot;
+        const bool valid = r < TT;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = valid ? tk[(size_t)r * D + i] : 0.0f;
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float p = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) p = fmaf(qf[h][i], x[i], p);
+#pragma unroll
+          for (int o = NL / 2; o >= 1; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+          sc[h] = valid ? p : neg_inf();
+        }
+        if (!valid) continue;   // uniform over the lane group
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = tv[(size_t)r * D + i];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mn = fmaxf(m[h], sc[h]);
+          const float alpha = exp2f(m[h] - mn);
+          const float pw = exp2f(sc[h] - mn);
+          l[h] = fmaf(l[h], alpha, pw);
+          zacc[h] *= alpha;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[h][i] = fmaf(acc[h][i], alpha, pw * x[i]);
+          m[h] = mn;
+        }
+      }
+    }
+  }
+
   if constexpr (V_AFF) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -601,7 +673,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   }
   __syncthreads();
 
-  merge_store<D, G, 0>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
+  DecodeArgs am = a;
+  if constexpr (K_KIVIB) am.nsplit = a.nsplit + 1;   // partial slots per (b, kv head): the splits and the tail
+  merge_store<D, G, 0>(c, am, b, kvh, is_tail ? nse : split, nse_all, sm_m, sm_l, &sm_acc[0][0][0]);
 }
 
 template <int D, int G, int KF, int VF>
@@ -617,7 +691,8 @@ cudaError_t launch_decode_dg(const CacheView& c, const DecodeArgs& a, cudaStream
     if (e != cudaSuccess) return e;
     configured_for = NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes;
   }
-  const dim3 grid(a.nsplit, c.Hkv, c.B);
+  // KIVI_BLOCK keys: one more CTA per (b, kv head) for the full-precision tail
+  const dim3 grid(a.nsplit + ((KF == F_KIVIB8 || KF == F_KIVIB4) ? 1 : 0), c.Hkv, c.B);
   decode_kernel<D, G, KF, VF><<<grid, kDecodeThreads, smem, st>>>(c, a);
   note_launch();
   return cudaGetLastError();

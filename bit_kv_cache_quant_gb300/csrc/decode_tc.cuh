@@ -676,9 +676,13 @@ cudaError_t launch_decode_tc_d(const CacheView& c, int G, const DecodeArgs& a, c
 
 // Tensor-core path when its preconditions hold (head_dim 64 / 128, 16-bit io,
 // key groups of at least 32 channels, each thread's value channels inside one
-// group); the exact CUDA-core kernel otherwise (fp32 outputs, head_dim 32).
+// group); the exact CUDA-core kernel otherwise (fp32 outputs, head_dim 32,
+// KIVI_BLOCK keys).
 template <int KF, int VF>
 cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st) {
+  if constexpr (KF == F_KIVIB8 || KF == F_KIVIB4) {
+    return launch_decode_cc<KF, VF>(c, G, a, st);   // per-block channel scales and the fp32 tail
+  } else {
   constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   const bool groups_ok = (!K_AFF || c.k.group >= 32) && (!V_AFF || c.v.group >= c.D / 8);
@@ -687,6 +691,7 @@ cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaSt
     return launch_decode_tc_d<64, KF, VF>(c, G, a, st);
   }
   return launch_decode_cc<KF, VF>(c, G, a, st);
+  }
 }
 
 }  // namespace kvq

@@ -81,6 +81,12 @@ kvq_status check_side(int fmt, int bits, int group, int D, bool is_k) {
       if (!is_k) return fail(KVQ_ERR_UNSUPPORTED, "Q4_0 storage is a K-side format");
       if (bits != 4 || (group != 32 && group != 0)) return fail(KVQ_ERR_INVALID_ARG, "Q4_0 needs bits 4, group 32");
       return KVQ_OK;
+    case KVQ_FMT_KIVI_BLOCK:
+      if (!is_k) return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK storage is a K-side format");
+      if (bits != 8 && bits != 4) return fail(KVQ_ERR_INVALID_ARG, "KIVI_BLOCK bits must be 8 or 4");
+      if (group != 64 && group != 128)
+        return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK block length (k_group) must be 64 or 128 tokens");
+      return KVQ_OK;
     default:
       return fail(KVQ_ERR_INVALID_ARG, "unknown format %d", fmt);
   }
@@ -93,6 +99,7 @@ int fmt_code(int fmt, int bits) {
     case KVQ_FMT_KIVI_CHAN: return bits == 8 ? kvq::F_KIVI8 : kvq::F_KIVI4;
     case KVQ_FMT_AFFINE_TOKEN: return bits == 8 ? kvq::F_AFF8 : kvq::F_AFF4;
     case KVQ_FMT_Q4_0: return kvq::F_Q40;
+    case KVQ_FMT_KIVI_BLOCK: return bits == 8 ? kvq::F_KIVIB8 : kvq::F_KIVIB4;
   }
   return -1;
 }
@@ -124,6 +131,10 @@ kvq_status compute_layout(const kvq_config* c, kvq_cache_layout* L) {
   if (s != KVQ_OK) return s;
   if (c->k_bias != nullptr && c->k_format != KVQ_FMT_Q4_0)
     return fail(KVQ_ERR_UNSUPPORTED, "a K mean-centering bias requires Q4_0 keys");
+  if (c->k_format == KVQ_FMT_KIVI_BLOCK &&
+      (c->layout != KVQ_LAYOUT_LINEAR || c->v_format != KVQ_FMT_AFFINE_TOKEN || c->capacity < c->k_group))
+    return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK keys need the LINEAR layout, AFFINE_TOKEN values and capacity >= "
+                                     "the block length");
 
   const size_t B = c->batch, H = c->n_kv_heads, BH = B * H;
   const size_t cap_alloc = align_up((size_t)c->capacity, kvq::kRowAlign);
@@ -153,6 +164,13 @@ kvq_status compute_layout(const kvq_config* c, kvq_cache_layout* L) {
     L->k_ch_zero32 = take(BH * D * 4);
   }
   if (c->k_bias) L->k_bias = take(H * D * 4);
+  if (c->k_format == KVQ_FMT_KIVI_BLOCK) {
+    const size_t R = c->k_group;
+    L->k_blk_scale = take(BH * (cap_alloc / R) * D * 2);
+    L->k_blk_zero = take(BH * (cap_alloc / R) * D * 2);
+    L->k_tail = take(BH * R * D * 4);
+    L->v_tail = take(BH * R * D * 4);
+  }
   L->v_codes = take(BH * cap_alloc * L->v_row_bytes);
   if (L->v_n_groups) L->v_tok_scale = take(BH * cap_alloc * L->v_n_groups * 2);
   if (c->v_format == KVQ_FMT_AFFINE_TOKEN) L->v_tok_zero = take(BH * cap_alloc * L->v_n_groups * 2);
@@ -281,6 +299,7 @@ size_t live_bytes(const kvq_cache_s* c, int stored) {
              (per_token(f.k_format, c->lay.k_row_bytes, c->lay.k_n_groups) +
               per_token(f.v_format, c->lay.v_row_bytes, c->lay.v_n_groups));
   if (f.k_format == KVQ_FMT_KIVI_CHAN) b += BH * f.head_dim * 4;
+  if (f.k_format == KVQ_FMT_KIVI_BLOCK) b += BH * ((size_t)stored / f.k_group) * f.head_dim * 4;   // block scale, zero
   return b;
 }
 
@@ -339,6 +358,10 @@ kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cu
                   lay.k_tok_scale, lay.k_tok_zero, lay.k_ch_scale, lay.k_ch_zero, lay.k_ch_scale32, lay.k_ch_zero32);
   v.v = side_view(b, cfg->v_format, cfg->v_bits, cfg->v_group, lay.v_row_bytes, lay.v_n_groups, lay.v_codes,
                   lay.v_tok_scale, lay.v_tok_zero, 0, 0, 0, 0);
+  v.k.blk_scale = lay.k_blk_scale ? reinterpret_cast<__half*>(b + lay.k_blk_scale) : nullptr;
+  v.k.blk_zero = lay.k_blk_zero ? reinterpret_cast<__half*>(b + lay.k_blk_zero) : nullptr;
+  v.tail_k = lay.k_tail ? reinterpret_cast<float*>(b + lay.k_tail) : nullptr;
+  v.tail_v = lay.v_tail ? reinterpret_cast<float*>(b + lay.v_tail) : nullptr;
   v.B = cfg->batch;
   v.Hkv = cfg->n_kv_heads;
   v.D = cfg->head_dim;
@@ -388,6 +411,8 @@ kvq_status append_rows(kvq_cache c, const void* k, const void* v, int64_t head_s
     return fail(KVQ_ERR_UNSUPPORTED, "KVQ_APPEND_RECOMPUTE_K needs a LINEAR or COMPACT layout");
   if (c->cfg.k_format == KVQ_FMT_KIVI_CHAN && !calibrate && !recompute && !c->k_calibrated)
     return fail(KVQ_ERR_UNSUPPORTED, "per-channel K scales are not calibrated yet (pass KVQ_APPEND_CALIBRATE_K)");
+  if (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK && flags)
+    return fail(KVQ_ERR_INVALID_ARG, "KIVI_BLOCK appends take no flags");
   if (c->cfg.layout != KVQ_LAYOUT_RING && n_tokens > c->cfg.capacity)
     return fail(KVQ_ERR_CAPACITY, "append of %d tokens exceeds capacity %d", n_tokens, c->cfg.capacity);
   cudaError_t e = kvq::launch_append(c->view, k, v, n_tokens, head_stride, in_dtype, calibrate, recompute, stream);
@@ -424,6 +449,8 @@ kvq_status kvq_evict(kvq_cache c, int32_t mode, const int32_t* keep_idx, int32_t
     if (!keep_idx) return fail(KVQ_ERR_INVALID_ARG, "null keep_idx");
     if (n_keep < 1 || n_keep > c->cfg.capacity) return fail(KVQ_ERR_INVALID_ARG, "n_keep out of range");
     if (c->cfg.layout == KVQ_LAYOUT_RING) return fail(KVQ_ERR_UNSUPPORTED, "keep-sets apply to LINEAR or COMPACT caches");
+    if (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK)
+      return fail(KVQ_ERR_UNSUPPORTED, "keep-sets do not apply to KIVI_BLOCK caches (closed blocks share K scales)");
     cudaError_t e = kvq::launch_evict_keepset(c->view, keep_idx, n_keep, stream);
     return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_evict");
   }
@@ -434,7 +461,8 @@ size_t kvq_decode_workspace_bytes(kvq_cache c, int32_t n_q_heads) {
   if (!c || n_q_heads < 1 || n_q_heads % c->cfg.n_kv_heads) return 0;
   const size_t G = n_q_heads / c->cfg.n_kv_heads;
   const DecodePlan p = decode_plan(c, (int)G);
-  const int ns = p.nsplit > p.nsplit_tc ? p.nsplit : p.nsplit_tc;
+  int ns = p.nsplit > p.nsplit_tc ? p.nsplit : p.nsplit_tc;
+  if (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK) ns = p.nsplit + 1;   // the tail's partial
   if (ns == 1) return 0;
   return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + kvq::kPartialPad) * sizeof(float);
 }
@@ -471,6 +499,13 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);
   cudaError_t e;
   using namespace kvq;
+  if (kf == F_KIVIB8 || kf == F_KIVIB4) {
+    if (G > 4) return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode takes up to 4 query heads per kv head");
+    if (kf == F_KIVIB8 && vf == F_AFF8) e = launch_decode<F_KIVIB8, F_AFF8>(c->view, G, a, stream);
+    else if (kf == F_KIVIB4 && vf == F_AFF4) e = launch_decode<F_KIVIB4, F_AFF4>(c->view, G, a, stream);
+    else return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode is built for 8-bit keys with 8-bit values and 4 with 4");
+    return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attn");
+  }
   if (kf == F_FP16 && vf == F_FP16) e = launch_decode<F_FP16, F_FP16>(c->view, G, a, stream);
   else if (kf == F_KIVI8 && vf == F_AFF8) e = launch_decode<F_KIVI8, F_AFF8>(c->view, G, a, stream);
   else if (kf == F_KIVI4 && vf == F_AFF4) e = launch_decode<F_KIVI4, F_AFF4>(c->view, G, a, stream);
@@ -558,6 +593,8 @@ kvq_status kvq_stats_read(kvq_cache c, kvq_stats* out) {
   out->k_calibrated = st.k_calibrated;
   out->cache_bytes = c->lay.total_bytes;
   out->live_bytes = live_bytes(c, st.stored);
+  out->tail = c->cfg.k_format == KVQ_FMT_KIVI_BLOCK ? st.tail : 0;
+  if (out->tail) out->live_bytes += (size_t)c->cfg.batch * c->cfg.n_kv_heads * out->tail * c->cfg.head_dim * 8;
   return st.status ? fail(KVQ_ERR_DEVICE, "device status %d", st.status) : KVQ_OK;
 }
 

@@ -22,7 +22,8 @@ struct DevState {
   unsigned append_arrive;   // CTA arrival counter of the append in flight
   unsigned evict_arrive;    // CTA arrival counter of the eviction in flight
   int k_calibrated;         // per-channel K scales frozen
-  int pad[57];
+  int tail;                 // KIVI_BLOCK: rows in the full-precision tail
+  int pad[56];
 };
 static_assert(sizeof(DevState) == 256, "DevState must be 256 bytes");
 
@@ -34,6 +35,8 @@ enum Fmt : int {
   F_AFF8 = 3,
   F_AFF4 = 4,
   F_Q40 = 5,
+  F_KIVIB8 = 6,   // KIVI_BLOCK keys, 8 / 4 bits
+  F_KIVIB4 = 7,
 };
 
 struct SideView {
@@ -44,6 +47,8 @@ struct SideView {
   __half* ch_zero;       // [B][Hkv][D]
   float* ch_scale32;     // [B][Hkv][D]
   float* ch_zero32;      // [B][Hkv][D]
+  __half* blk_scale;     // [B][Hkv][cap_alloc / R][D] (KIVI_BLOCK)
+  __half* blk_zero;      // [B][Hkv][cap_alloc / R][D] (KIVI_BLOCK)
   int fmt;               // kvq_format
   int bits;
   int group;             // channels per (scale, zero) group
@@ -62,6 +67,8 @@ struct CacheView {
   unsigned* split_sem;   // [B*Hkv]
   const float* k_bias;   // [Hkv][D] or null
   SideView k, v;
+  float* tail_k;         // [B][Hkv][R][D] full-precision tail (KIVI_BLOCK), else null
+  float* tail_v;
   int B, Hkv, D, cap, cap_alloc, layout, sink, window;
   int has_maps;
 };

@@ -76,7 +76,17 @@ typedef enum kvq_format {
   KVQ_FMT_AFFINE_TOKEN = 2,
   /* symmetric 32-channel blocks, one fp16 scale, no zero point ([KMC] "The idea").
      bits 4, group 32.  K side only; the only format that accepts a K bias.        */
-  KVQ_FMT_Q4_0 = 3
+  KVQ_FMT_Q4_0 = 3,
+  /* KIVI residual buffer ([MLX] section 3, "What KIVI and KVQuant found"): the most
+     recent tokens stay at full precision (fp32) in a tail of fewer than `group` = R
+     rows; each time R tokens have gathered, that closed block's keys are coded per
+     (b, kv head, channel) with the block's own asymmetric scale and zero (the KIVI
+     formula over exactly those R tokens) and its values per token with the V
+     format, the codes go to the next R rows of the quantised bulk and the tail
+     empties.  Decode attends over the bulk and then the exact tail.  K side only;
+     bits 8 or 4; R a multiple of 64 (64 or 128); needs an AFFINE_TOKEN V side and
+     the LINEAR layout.                                                              */
+  KVQ_FMT_KIVI_BLOCK = 4
 } kvq_format;
 
 typedef enum kvq_layout {
@@ -141,7 +151,10 @@ typedef struct kvq_config {
      {k,v}_tok_zero     fp16   [B][Hkv][cap_alloc][n_groups] (AFFINE_TOKEN)
      k_ch_scale/zero    fp16   [B][Hkv][D]  stored per-channel metadata (KIVI_CHAN)
      k_ch_scale32/zero32 fp32  [B][Hkv][D]  the values codes are computed from
-     k_bias             fp32   [Hkv][D]     copy of kvq_config.k_bias               */
+     k_bias             fp32   [Hkv][D]     copy of kvq_config.k_bias
+     k_blk_scale/zero   fp16   [B][Hkv][cap_alloc / R][D]  per-block, per-channel K
+                        metadata (KIVI_BLOCK)
+     {k,v}_tail         fp32   [B][Hkv][R][D]  the full-precision tail (KIVI_BLOCK)  */
 typedef struct kvq_cache_layout {
   size_t total_bytes;
   int32_t cap_alloc;
@@ -150,6 +163,7 @@ typedef struct kvq_cache_layout {
   size_t state, split_sem;
   size_t k_codes, k_tok_scale, k_tok_zero, k_ch_scale, k_ch_zero, k_ch_scale32, k_ch_zero32, k_bias;
   size_t v_codes, v_tok_scale, v_tok_zero;
+  size_t k_blk_scale, k_blk_zero, k_tail, v_tail;
 } kvq_cache_layout;
 
 typedef struct kvq_stats {
@@ -160,7 +174,10 @@ typedef struct kvq_stats {
   int32_t device_status;  /* KVQ_DEV_* */
   int32_t k_calibrated;   /* KIVI_CHAN: per-channel scales frozen */
   size_t cache_bytes;     /* size of the cache buffer */
-  size_t live_bytes;      /* bytes of codes + metadata of the stored rows */
+  size_t live_bytes;      /* bytes of codes + metadata of the stored rows (and, for
+                             KIVI_BLOCK, of the full-precision tail) */
+  int32_t tail;           /* KIVI_BLOCK: tokens in the full-precision tail (stored counts
+                             the quantised bulk only); 0 otherwise */
 } kvq_stats;
 
 typedef struct kvq_cache_s* kvq_cache;
@@ -190,7 +207,12 @@ void kvq_cache_release(kvq_cache cache);
    scale = max(1e-5, (max - min) / (qMax - qMin)), zero = min, and
    u = clamp(rint((x - zero) / scale), 0, qMax - qMin) ([SLK] "Affine quantisation
    formula"); Q4_0 uses d = max|x - kbar| / 7, u = clamp(rint((x - kbar) / d), -8, 7) + 8
-   (u = 8 when d == 0).  Stored scales and zeros are fp16. */
+   (u = 8 when d == 0).  Stored scales and zeros are fp16.
+   KIVI_BLOCK keys ([MLX] section 3): the tail (t rows) followed by the n new tokens
+   is taken in order; each complete run of R is a closed block, coded (keys per
+   channel over its R tokens, values per token) into bulk rows stored .. stored + R - 1,
+   and the rest becomes the tail; the split into calls does not change the result.
+   Device overflow of the bulk -> KVQ_DEV_OVERFLOW, nothing written; flags must be 0. */
 kvq_status kvq_append(kvq_cache cache, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype,
                       int32_t flags, cudaStream_t stream);
 
@@ -229,7 +251,11 @@ size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
    codes and fp16 metadata; softmax_scale <= 0 means 1/sqrt(D).  The rows are
    split across CTAs and merged with the online-softmax rule.  workspace: device,
    >= kvq_decode_workspace_bytes bytes (may be NULL when that is 0).  Calls on the
-   same cache must not overlap on the GPU.  Hq / Hkv in {1, 2, 3, 4}. */
+   same cache must not overlap on the GPU.  KIVI_BLOCK caches attend over the
+   quantised bulk and then the exact fp32 tail ([MLX] section 3), on the fp32
+   CUDA-core path with one more CTA per (b, kv head) for the tail.  Hq / Hkv from
+   1 to 8 on the tensor-core path (16-bit io, head_dim 64 / 128), 1 to 4 on the
+   CUDA-core path (fp32 io, head_dim 32, KIVI_BLOCK keys). */
 kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                            float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream);
 

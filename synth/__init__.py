@@ -18,7 +18,9 @@ Workloads follow the five shapes the pages discuss:
   mean-centering bias and int8 per-token V at 32K context, batch 8,
 * a SnapKV prefill eviction (16K prompt to a 512-token budget) followed by
   fp16 decode appends,
-* a long streaming decode with KIVI int4 and a 4 + 4096 ring.
+* a long streaming decode with KIVI int4 and a 4 + 4096 ring,
+* a KIVI residual buffer (full-precision tail, int4 keys per channel in
+  closed blocks of 128 tokens) on the Llama-3.2-3B attention shape at 8K.
 """
 from __future__ import annotations
 
@@ -50,7 +52,7 @@ class Workload:
     n_kv_heads: int
     head_dim: int
     context: int                 # tokens held by the cache when decode starts
-    k_format: str                # "fp16" | "kivi_chan" | "affine_token" | "q4_0"
+    k_format: str                # "fp16" | "kivi_chan" | "affine_token" | "q4_0" | "kivi_block"
     k_bits: int
     k_group: int
     v_format: str                # "fp16" | "affine_token"
@@ -143,6 +145,15 @@ WORKLOADS = {
             seed=1005, k_channel_offset_sigma=2.0, rope_theta=10000.0,
             generated_steps=40000,
         ),
+        # KIVI residual buffer: fp32 tail, int4 K per channel in closed blocks of 128, V g32.
+        Workload(
+            name="kivi4_residual_r128_ctx8k",
+            batch=1, layers=28, n_q_heads=24, n_kv_heads=8, head_dim=128,
+            context=8192 + 100,
+            k_format="kivi_block", k_bits=4, k_group=128,
+            v_format="affine_token", v_bits=4, v_group=32,
+            io_dtype="bfloat16", seed=1006, k_channel_offset_sigma=2.0,
+        ),
     ]
 }
 
@@ -153,6 +164,7 @@ ALIASES = {
     "q4_0_32k": "q4_0_centered_k_int8_v_ctx32k_b8",
     "snapkv": "snapkv_s16k_budget512_fp16",
     "ring": "kivi4_ring_sink4_win4096_b64",
+    "residual": "kivi4_residual_r128_ctx8k",
 }
 
 

@@ -39,7 +39,7 @@ def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = "") -
 def oracle_spec(cache, bias: np.ndarray | None = None) -> CacheSpec:
     """The oracle CacheSpec of a KVCache (from its kvq_config)."""
     c = cache.cfg
-    inv_fmt = {0: "fp16", 1: "kivi_chan", 2: "affine_token", 3: "q4_0"}
+    inv_fmt = {0: "fp16", 1: "kivi_chan", 2: "affine_token", 3: "q4_0", 4: "kivi_block"}
     inv_lay = {0: "linear", 1: "compact", 2: "ring"}
     return CacheSpec(batch=c.batch, n_kv_heads=c.n_kv_heads, head_dim=c.head_dim, capacity=c.capacity,
                      layout=inv_lay[c.layout], sink=c.sink, window=c.window,
@@ -74,10 +74,19 @@ def gpu_planes(cache) -> dict:
         off = getattr(L, f"k_{name}")
         if off:
             out[f"k_{name}"] = _plane(buf, off, B * H * D * sz).view(dt).reshape(B, H, D)
-    st = _plane(buf, L.state, 16)
+    if L.k_blk_scale:   # KIVI residual buffer: per-block channel metadata and the fp32 tails
+        R = c.k_group
+        for name in ("blk_scale", "blk_zero"):
+            out[f"k_{name}"] = _plane(buf, getattr(L, f"k_{name}"), B * H * (ca // R) * D * 2).view(
+                np.float16).reshape(B, H, ca // R, D)
+        for side in ("k", "v"):
+            out[f"{side}_tail"] = _plane(buf, getattr(L, f"{side}_tail"), B * H * R * D * 4).view(
+                np.float32).reshape(B, H, R, D)
+    st = _plane(buf, L.state, 32)
     out["pos"] = int(st[:8].view(np.int64)[0])
     out["stored"] = int(st[8:12].view(np.int32)[0])
     out["status"] = int(st[12:16].view(np.int32)[0])
+    out["tail"] = int(st[28:32].view(np.int32)[0])
     return out
 
 
@@ -110,6 +119,16 @@ def assert_cache_equal(cache, oc: OracleCache, what: str = "", sel=None, planes=
         if o.tok_zero is not None:
             np.testing.assert_array_equal(_bits(g[f"{side}_tok_zero"][:, :, :n]), _bits(o.tok_zero[:, :, :n]),
                                           err_msg=f"{what}: {side} token zeros")
+    if oc.spec.k_format == "kivi_block":
+        R, nb, nt = oc.spec.k_group, oc.stored // oc.spec.k_group, oc.n_tail
+        assert g["tail"] == nt, f"{what}: tail {g['tail']} vs oracle {nt}"
+        for name in ("blk_scale", "blk_zero"):
+            np.testing.assert_array_equal(_bits(g[f"k_{name}"][:, :, :nb]), _bits(getattr(oc.k, name)[:, :, :nb]),
+                                          err_msg=f"{what}: k {name}")
+        np.testing.assert_array_equal(_bits(g["k_tail"][:, :, :nt]), _bits(oc.tail_k[:, :, :nt]),
+                                      err_msg=f"{what}: k tail")
+        np.testing.assert_array_equal(_bits(g["v_tail"][:, :, :nt]), _bits(oc.tail_v[:, :, :nt]),
+                                      err_msg=f"{what}: v tail")
     if oc.k.ch_scale32 is not None:
         for name, arr in (("ch_scale", oc.k.ch_scale), ("ch_zero", oc.k.ch_zero),
                           ("ch_scale32", oc.k.ch_scale32), ("ch_zero32", oc.k.ch_zero32)):

@@ -121,3 +121,35 @@ def test_null_handles(kvq):
     assert kvq.lib.kvq_append(None, None, None, 1, 1, 0, None) == 1
     assert kvq.lib.kvq_decode_attn(None, None, None, 1, 1, 0.0, None, 0, None) == 1
     assert kvq.lib.kvq_decode_workspace_bytes(None, 8) == 0
+
+
+def test_residual_buffer_layout(kvq):
+    # KIVI_BLOCK keys: per-block channel metadata [B][Hkv][cap_alloc / R][D] fp16 and fp32 tails [B][Hkv][R][D]
+    cfg = _cfg(kvq, capacity=300, k_format="kivi_block", k_bits=4, k_group=128, v_format="affine_token", v_bits=4,
+               v_group=32)
+    st, lay = _status(kvq, cfg)
+    assert st == 0, kvq.lib.kvq_last_error()
+    assert lay.cap_alloc == 320 and lay.k_n_groups == 0 and lay.k_tok_scale == 0
+    BH, D = 2 * 4, 128
+    offs = [lay.k_codes, lay.k_blk_scale, lay.k_blk_zero, lay.k_tail, lay.v_tail]
+    assert all(o and o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.k_blk_zero - lay.k_blk_scale >= BH * (320 // 128) * D * 2
+    assert lay.v_tail - lay.k_tail >= BH * 128 * D * 4 and lay.total_bytes >= lay.v_tail + BH * 128 * D * 4
+    st, lay = _status(kvq, _cfg(kvq))
+    assert lay.k_blk_scale == 0 and lay.k_tail == 0 and lay.v_tail == 0
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(k_group=32), 2),                                           # block length not 64 or 128
+    (dict(k_bits=2), 1),
+    (dict(layout="compact", sink=4, window=64, capacity=200), 2),   # residual buffers are LINEAR
+    (dict(v_format="fp16", v_bits=16, v_group=0), 2),                # values must be AFFINE_TOKEN
+    (dict(capacity=100), 2),                                         # capacity below one block
+    (dict(v_format="kivi_block", v_bits=4, v_group=64), 2),          # a K-side format
+])
+def test_residual_buffer_invalid_configs(kvq, bad, code):
+    base = dict(capacity=256, k_format="kivi_block", k_bits=4, k_group=128, v_format="affine_token", v_bits=4,
+                v_group=32)
+    base.update(bad)
+    st, _ = _status(kvq, _cfg(kvq, **base))
+    assert st == code, kvq.lib.kvq_last_error()

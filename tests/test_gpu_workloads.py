@@ -74,6 +74,27 @@ def test_mlx_affine4_ctx8k_one_layer_full(kvq):
     assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), "mlx g64 layer")
 
 
+def test_residual_buffer_ctx8k_one_layer_full(kvq):
+    # the residual workload at full context (64 closed blocks of 128 and a 100-token tail), then
+    # 30 decode-step appends: the 28th closes a block mid-decode
+    w = synth.get_workload("residual")
+    cache = _cache_for(kvq, w, capacity=w.context + 64)
+    oc = OracleCache(oracle_spec(cache))
+    k, v = synth.layer_inputs(w, 1, 0, w.context, device="cuda")
+    cache.append(k, v)
+    oc.append(host(k), host(v))
+    assert (oc.stored, oc.n_tail) == (8192, 100)
+    for step in range(30):
+        q, k1, v1 = synth.decode_token_inputs(w, 1, step, w.context + step, device="cuda")
+        cache.append(k1, v1)
+        oc.append(host(k1), host(v1))
+    out = cache.decode_attn(q)
+    assert (oc.stored, oc.n_tail) == (8320, 2)
+    assert_cache_equal(cache, oc, "residual layer")
+    kh, vh = oc.dequant()
+    assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), "residual layer")
+
+
 @pytest.mark.parametrize("name,samples", [("q4_0_32k", [(0, 0), (3, 5), (7, 7)]),
                                           ("ring", [(0, 0), (17, 3), (63, 7)])])
 def test_large_batch_workloads_sampled(kvq, name, samples):
