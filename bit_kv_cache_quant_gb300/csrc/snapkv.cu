@@ -20,6 +20,8 @@
 // largest score exactly, followed by one ordered pass that keeps every larger
 // score and the lowest-indexed equal ones, emitting positions in ascending
 // order with a block scan.
+#include <cooperative_groups.h>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -478,6 +480,123 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
   }
 }
 
+// The same selection with a cluster of kTopkCluster CTAs per (b, kv head), so
+// that a long prompt's scores are worked by that many SMs instead of one.
+// CTA rank r holds positions [r * chunk, (r + 1) * chunk) in shared memory.
+// Each radix pass builds the CTA's histogram (double-buffered by pass), and
+// after one cluster barrier every CTA sums the cluster's histograms through
+// distributed shared memory and picks the same bin.  The positions kept come
+// out in ascending order: rank r writes after the kept positions of the lower
+// ranks (sinks, larger keys and the ties they keep, lowest positions first),
+// which each CTA counts from the lower ranks' (larger, tie) counts.
+constexpr int kTopkCluster = 8;
+constexpr int kTopkClusterThreads = 512;
+constexpr int kTopkClusterMaxChunk = 8192;   // positions per CTA (32 KB of shared memory)
+
+__global__ void __launch_bounds__(kTopkClusterThreads) topk_cluster_kernel(const float* __restrict__ scores, int S,
+                                                                           int budget, int n_sink,
+                                                                           int* __restrict__ idx_out) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ float sm_sc[];
+  __shared__ unsigned hist[2][256];
+  __shared__ unsigned tot[256];
+  __shared__ unsigned s_bin, s_need;
+  __shared__ int warp_sums[33];
+  __shared__ int s_cnt[2];   // this CTA's positions kept outright (sinks, larger keys) and ties
+  const int rank = (int)cluster.block_rank();
+  const size_t bh = blockIdx.y;
+  const float* sc = scores + bh * S;
+  int* out = idx_out + bh * budget;   // budget < S (the host takes the other case)
+  const int chunk = (S + kTopkCluster - 1) / kTopkCluster;
+  const int c0 = min(S, rank * chunk), c1 = min(S, c0 + chunk);
+  for (int i = threadIdx.x; i < c1 - c0; i += blockDim.x) sm_sc[i] = __ldg(sc + c0 + i);
+  __syncthreads();
+  const int ns = min(n_sink, S);
+  const int k = budget - ns;
+  unsigned prefix = 0u, mask = 0u, need = (unsigned)k;
+  if (k > 0) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      unsigned* h = hist[pass & 1];
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+      __syncthreads();
+      for (int j = max(c0, ns) + threadIdx.x; j < c1; j += blockDim.x) {
+        const unsigned key = order_key(sm_sc[j - c0]);
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1u);
+      }
+      // every CTA's histogram of this pass is complete; the buffer of the
+      // previous pass is free (each CTA finished reading it before arriving)
+      cluster.sync();
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        unsigned t = 0u;
+#pragma unroll
+        for (int r = 0; r < kTopkCluster; ++r) t += cluster.map_shared_rank(h, r)[i];
+        tot[i] = t;
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) pick_bin(tot, need, &s_bin, &s_need);
+      __syncthreads();
+      prefix |= s_bin << shift;
+      mask |= 0xFFu << shift;
+      need = s_need;
+      __syncthreads();
+    }
+  }
+  // This thread's positions, their counts, and the CTA's totals.
+  const int seg = (c1 - c0 + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int j0 = min(c1, c0 + (int)threadIdx.x * seg), j1 = min(c1, j0 + seg);
+  int n_big = 0, n_tie = 0;
+  for (int j = j0; j < j1; ++j) {
+    if (j < ns) {
+      ++n_big;
+    } else if (k > 0) {
+      const unsigned key = order_key(sm_sc[j - c0]);
+      n_big += key > prefix;
+      n_tie += key == prefix;
+    }
+  }
+  int big_total, tie_total;
+  const int big_before = block_excl_count_n(n_big, &big_total, warp_sums);
+  const int tie_before = block_excl_count_n(n_tie, &tie_total, warp_sums);
+  if (threadIdx.x == 0) {
+    s_cnt[0] = big_total;
+    s_cnt[1] = tie_total;
+  }
+  cluster.sync();
+  // positions the lower ranks keep, and the ties they take
+  int out_before = 0, ties_before_cta = 0;
+  for (int r = 0; r < rank; ++r) {
+    const int* rc = cluster.map_shared_rank(s_cnt, r);
+    const int kept = max(0, min(rc[1], (int)need - ties_before_cta));
+    out_before += rc[0] + kept;
+    ties_before_cta += rc[1];
+  }
+  cluster.sync();   // no CTA leaves while another may still read its counts
+  const int ties_cta = max(0, min(tie_total, (int)need - ties_before_cta));
+  const int ties_kept = max(0, min(n_tie, ties_cta - tie_before));
+  // the CTA's kept ties come from its lowest positions: threads before this
+  // one keep min(tie_before, ties_cta) of them
+  int pos = out_before + big_before + min(tie_before, ties_cta);
+  int ties_left = ties_kept;
+  for (int j = j0; j < j1; ++j) {
+    bool sel;
+    if (j < ns) {
+      sel = true;
+    } else if (k > 0) {
+      const unsigned key = order_key(sm_sc[j - c0]);
+      sel = key > prefix;
+      if (key == prefix && ties_left > 0) {
+        sel = true;
+        --ties_left;
+      }
+    } else {
+      sel = false;
+    }
+    if (sel) out[pos++] = j;
+  }
+}
+
 // ------------------------------------------------------------ smoothing --
 // The SnapKV paper's max-pool smoothing of the scores (the page leaves it out,
 // "Proxy limitation"): out[j] = max of in[j - r .. j + r] clipped to [0, S),
@@ -545,6 +664,23 @@ static cudaError_t launch_snapkv_d(const void* k, long long hs, int B, int Hkv, 
 
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
                         cudaStream_t st) {
+  if (budget < S && S >= 4096 && (S + kTopkCluster - 1) / kTopkCluster <= kTopkClusterMaxChunk) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kTopkCluster, B * Hkv);
+    cfg.blockDim = dim3(kTopkClusterThreads);
+    cfg.dynamicSmemBytes = ((S + kTopkCluster - 1) / kTopkCluster) * sizeof(float);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kTopkCluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, S, budget, n_sink, idx);
+    note_launch();
+    return e;
+  }
   const int smem = S <= kTopkSmemKeys ? S * (int)sizeof(float) : 0;
   static int configured = 0;
   if (!configured) {

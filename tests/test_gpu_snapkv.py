@@ -53,6 +53,28 @@ def test_topk_bit_exact_on_identical_scores(kvq, S, budget, n_sink):
             np.testing.assert_array_equal(got[b, h], ref, err_msg=f"b{b} h{h}")
 
 
+# Prompts of 4096 positions and more run the selection on a cluster of CTAs per
+# head (each a contiguous slice of the positions): ties and kept positions
+# cross the slice boundaries.
+@pytest.mark.parametrize("S,budget,n_sink", [(16384, 512, 4), (65536, 4096, 0), (8192, 4, 4), (4096, 4095, 1),
+                                             (4097, 2000, 7)])
+def test_topk_cluster_sizes(kvq, S, budget, n_sink):
+    rng = np.random.default_rng(S + 3 * budget)
+    scores = (rng.random((1, 2, S)).astype(np.float32) * 1e-3)
+    scores[0, 0, rng.integers(0, S, size=200)] = scores[0, 0, S // 3]   # ties around the cutoff
+    got = _topk_gpu(kvq, scores, budget, n_sink)
+    for h in range(2):
+        np.testing.assert_array_equal(got[0, h], osk.select_indices(scores[0, h], budget, n_sink), err_msg=f"h{h}")
+
+
+def test_topk_cluster_all_equal(kvq):
+    # every score equal: the lowest positions are kept, across all slices
+    S, budget, n_sink = 20000, 9000, 4
+    scores = np.full((1, 1, S), 0.25, np.float32)
+    got = _topk_gpu(kvq, scores, budget, n_sink)
+    assert got[0, 0].tolist() == list(range(budget)) == osk.select_indices(scores[0, 0], budget, n_sink).tolist()
+
+
 def test_topk_negative_scores_order(kvq):
     scores = np.array([[[-3.0, -1.0, -2.0, 5.0, -0.5, 0.0]]], np.float32)
     got = _topk_gpu(kvq, scores, 3, 1)
