@@ -250,10 +250,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const int hg = (warp >> 2) % HG;
   const int grp = (warp >> 2) / HG;
   const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
-  // Thread 0 reads the stored length and requests each tile group's first
-  // tile (alone, so that it reaches the SM ahead of the rest of the split,
-  // which every CTA would otherwise ask for at the same moment) while the
-  // query fragments are built.
+  // Thread 0 reads the stored length and requests the whole initial ring
+  // of tiles while the query fragments are built (requesting each group's
+  // first tile alone, ahead of the rest, measured slower once the request
+  // moved before the fragment build).
   // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
   // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
   // columns and q enters exactly.  Thread (g, t) builds column g at the key
@@ -265,12 +265,9 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     split_rows(T0, a.nsplit, split, a0, a1, ns0);
     if (split < ns0) {
       const int nt0 = (a1 - a0 + kTileTokens - 1) / kTileTokens;
-#pragma unroll
-      for (int gp = 0; gp < NGRP; ++gp) {
-        if (gp < nt0) {
-          issue_tile_tma<D, KF, VF>(smem + gp * TL.bytes, TL, c, bh, a0 + gp * kTileTokens, &mbar[gp]);
-          s_last_tile[gp] = gp;
-        }
+      for (int s0 = 0; s0 < NSTAGE && s0 < nt0; ++s0) {
+        issue_tile_tma<D, KF, VF>(smem + s0 * TL.bytes, TL, c, bh, a0 + s0 * kTileTokens, &mbar[s0]);
+        s_last_tile[s0] = s0;
       }
     }
   }
@@ -323,9 +320,6 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   split_rows(T, a.nsplit, split, t0, t1, nse);
   if (split >= nse) return;   // no rows for this split (no copy was issued)
   const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
-  // The group's first warp requests the group's other initial tiles once
-  // its first tile has landed.
-  const bool leader = (warp % TW) == 0 && lane == 0;
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 
@@ -365,12 +359,6 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar[stg], (it / NSTAGE) & 1))) {
       s_fail = 1;
       break;
-    }
-    if (it == grp && leader) {
-      for (int s = grp + NGRP; s < NSTAGE && s < ntiles; s += NGRP) {
-        issue_tile_tma<D, KF, VF>(smem + s * TL.bytes, TL, c, bh, t0 + s * kTileTokens, &mbar[s]);
-        s_last_tile[s] = s;
-      }
     }
     const uint8_t* st = smem + stg * TL.bytes;
     const int tok0 = t0 + it * kTileTokens + blk;
