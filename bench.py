@@ -504,7 +504,7 @@ def decode_source_sha(kvq_dir):
 
 def decode_kernel_name(w):
     """The decode kernel the library launches for this workload (tensor-core path for 16-bit io, D 64/128)."""
-    tc = w.io_dtype != "float32" and w.head_dim in (64, 128) and w.k_format != "kivi_block"
+    tc = w.io_dtype != "float32" and w.head_dim in (64, 128)
     return "decode_tc_kernel" if tc else "decode_kernel"
 
 

@@ -673,9 +673,13 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(CacheView c, Dec
   }
   __syncthreads();
 
-  DecodeArgs am = a;
-  if constexpr (K_KIVIB) am.nsplit = a.nsplit + 1;   // partial slots per (b, kv head): the splits and the tail
-  merge_store<D, G, 0>(c, am, b, kvh, is_tail ? nse : split, nse_all, sm_m, sm_l, &sm_acc[0][0][0]);
+  if constexpr (K_KIVIB) {
+    DecodeArgs am = a;
+    am.nsplit = a.nsplit + 1;   // partial slots per (b, kv head): the splits and the tail
+    merge_store<D, G, 0>(c, am, b, kvh, is_tail ? nse : split, nse_all, sm_m, sm_l, &sm_acc[0][0][0]);
+  } else {
+    merge_store<D, G, 0>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
+  }
 }
 
 template <int D, int G, int KF, int VF>

@@ -159,7 +159,8 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
   static constexpr int vng_max = 8;
   static constexpr int stage = ((64 * D * FmtBits<KF>::v / 8 + 64 * D * FmtBits<VF>::v / 8 +
                                  ((KF == F_AFF8 || KF == F_AFF4) ? 2 : (KF == F_Q40 ? 1 : 0)) * 64 * kng_max * 2 +
-                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * vng_max * 2) +
+                                 ((VF == F_AFF8 || VF == F_AFF4) ? 2 : 0) * 64 * vng_max * 2 +
+                                 ((KF == F_KIVIB8 || KF == F_KIVIB4) ? 2 * D * 2 : 0)) +
                                 1023) / 1024 * 1024;
   using Shape = TcShape<NGRP, TcHeads<G>::hg>;
   static constexpr int warps = Shape::warps;
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   constexpr bool K_Q40 = (KF == F_Q40);
   constexpr bool KG = K_AFF || K_Q40;
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  constexpr bool K_KIVIB = (KF == F_KIVIB8 || KF == F_KIVIB4);
   constexpr int NACC = KG ? NB : 1;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per kv head");
   static_assert(NSTAGE % NGRP == 0, "each stage serves one tile group");
@@ -210,6 +212,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   __shared__ int s_T;
   __shared__ volatile int s_fail;
   __shared__ float sm_qsum[NB][8];        // sum of q of each head over each 32-channel key block
+  // KIVI_BLOCK keys: the query in fp32 (the fragments are folded with each
+  // block's channel scales as the tiles reach a new block) and the tail length
+  __shared__ float sm_qraw[K_KIVIB ? G : 1][K_KIVIB ? D : 1];
+  __shared__ int s_tail;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int lane = threadIdx.x & 31;
@@ -261,6 +267,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   if (threadIdx.x == 0) {
     const int T0 = c.state->stored;
     s_T = T0;
+    if constexpr (K_KIVIB) s_tail = c.state->tail;
     int a0, a1, ns0;
     split_rows(T0, a.nsplit, split, a0, a1, ns0);
     if (split < ns0) {
@@ -314,12 +321,27 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       }
     }
   }
+  if constexpr (K_KIVIB) {
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+      sm_qraw[i / D][i % D] = load_io(a.q, ((size_t)b * a.Hq + (size_t)kvh * G + i / D) * D + i % D, a.io_dtype);
+  }
   __syncthreads();
   const int T = s_T;
   int t0, t1, nse;
   split_rows(T, a.nsplit, split, t0, t1, nse);
-  if (split >= nse) return;   // no rows for this split (no copy was issued)
-  const int ntiles = (t1 - t0 + kTileTokens - 1) / kTileTokens;
+  // KIVI_BLOCK: CTA a.nsplit attends over the fp32 tail and merges as one
+  // more split (partial slot nse, after the bulk's); a cache with no closed
+  // block has no bulk splits.
+  int nse_all = nse, TT = 0;
+  bool is_tail = false;
+  if constexpr (K_KIVIB) {
+    TT = s_tail;
+    is_tail = split == a.nsplit;
+    if (T == 0) nse = TT > 0 ? 0 : 1;
+    nse_all = nse + (TT > 0 ? 1 : 0);
+  }
+  if (is_tail ? TT == 0 : split >= nse) return;   // no rows for this CTA (no copy was issued)
+  const int ntiles = is_tail ? 0 : (t1 - t0 + kTileTokens - 1) / kTileTokens;
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
 
@@ -353,6 +375,11 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const int rk[2] = {blk + tau<VROW>(g), blk + tau<VROW>(g + 8)};
   const int rr[4] = {blk + tau<VROW>(2 * t), blk + tau<VROW>(2 * t + 1), blk + tau<VROW>(2 * t + 8),
                      blk + tau<VROW>(2 * t + 9)};
+  // KIVI_BLOCK keys: k = s u + z with a (scale, zero) per (block, channel), so
+  // the score is sum((q s) u) + sum(q z); the fragments hold q s of the block
+  // of the warp's current tile and zt = sum(q z) of head hd.
+  int cur_blk = -1;
+  float zt = 0.0f;
 
   for (int it = grp; it < ntiles; it += NGRP) {
     const int stg = it % NSTAGE;
@@ -362,6 +389,44 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     }
     const uint8_t* st = smem + stg * TL.bytes;
     const int tok0 = t0 + it * kTileTokens + blk;
+    if constexpr (K_KIVIB) {
+      const int bk = (t0 + it * kTileTokens) / c.k.group;
+      if (bk != cur_blk && tok0 < t1) {   // warp-uniform
+        cur_blk = bk;
+        const __half* bs = reinterpret_cast<const __half*>(st + TL.kbs);
+        const __half* bz = reinterpret_cast<const __half*>(st + TL.kbz);
+        const int hq = 4 * hg + (g >> 1);
+        const float* qr = sm_qraw[hq < G ? hq : 0];
+        const bool live = hq < G;
+        float zp = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          int ch[4];
+          key_channels<KB>(ks, t, ch);
+          float x[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float q = live ? qr[ch[i]] : 0.0f;
+            zp = fmaf(q, __half2float(bz[ch[i]]), zp);
+            x[i] = q * __half2float(bs[ch[i]]);
+          }
+          const __half2 h01 = __floats2half2_rn(x[0], x[1]);
+          const __half2 h23 = __floats2half2_rn(x[2], x[3]);
+          qf[ks][0] = h2u(h01);
+          qf[ks][1] = h2u(h23);
+          if (g & 1) {
+            const float2 f01 = __half22float2(h01);
+            const float2 f23 = __half22float2(h23);
+            qf[ks][0] = h2u(__floats2half2_rn(x[0] - f01.x, x[1] - f01.y));
+            qf[ks][1] = h2u(__floats2half2_rn(x[2] - f23.x, x[3] - f23.y));
+          }
+        }
+        // quad g holds head 4 hg + g / 2 (both of its columns carry the same sum)
+        zp += __shfl_xor_sync(0xffffffffu, zp, 1);
+        zp += __shfl_xor_sync(0xffffffffu, zp, 2);
+        zt = __shfl_sync(0xffffffffu, zp, 8 * t);
+      }
+    }
     // Blocks wholly inside the split skip the row masks; the last block of
     // the split (rows past its end) takes them.
     auto block = [&](auto masked) {
@@ -444,6 +509,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
           }
         } else {
           v = acc[0][2 * e] + acc[0][2 * e + 1];
+          if constexpr (K_KIVIB) v += zt;
         }
         sc[e] = vk[e] ? v * a.qscale : neg_inf();
       }
@@ -585,24 +651,89 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   // landed and been read).  Thread (g, t) holds head hd at its value channels
   // d = g * VCH + 2 mt + e, stored at (d % VCH) * 8 + d / VCH.
   float(*sm_acc)[G][D + 8] = reinterpret_cast<float(*)[G][D + 8]>(smem);
+  if (is_tail) {
+    if constexpr (K_KIVIB) {
+      // The fp32 tail rows [0, TT): the head group's 4 NGRP warps take rows in
+      // turn, each for the group's heads, lane l for channels [l C, l C + C).
+      constexpr int C = D / 32;
+      const int wi = (warp & 3) + 4 * grp;
+      const float* tk = c.tail_k + (bh * c.k.group) * D + lane * C;
+      const float* tv = c.tail_v + (bh * c.k.group) * D + lane * C;
+      float tm[4], tl[4], ta[4][C];
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
-    zacc += __shfl_xor_sync(0xffffffffu, zacc, o);
-  }
-  if (hd < G) {
+      for (int j = 0; j < 4; ++j) {
+        tm[j] = neg_inf();
+        tl[j] = 0.0f;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      sm_acc[warp][hd][(2 * mt) * 8 + g] = (oacc[mt][0] + oacc[mt][1]) + zacc;
-      sm_acc[warp][hd][(2 * mt + 1) * 8 + g] = (oacc[mt][2] + oacc[mt][3]) + zacc;
+        for (int i = 0; i < C; ++i) ta[j][i] = 0.0f;
+      }
+      for (int r = wi; r < TT; r += 4 * NGRP) {
+        float x[C], y[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+          x[i] = tk[(size_t)r * D + i];
+          y[i] = tv[(size_t)r * D + i];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int h = 4 * hg + j;
+          if (h >= G) break;   // warp-uniform
+          float p = 0.0f;
+#pragma unroll
+          for (int i = 0; i < C; ++i) p = fmaf(sm_qraw[h][lane * C + i], x[i], p);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+          const float sc = p * a.qscale;
+          const float mn = fmaxf(tm[j], sc);
+          const float alpha = fast_exp2(tm[j] - mn);
+          const float pw = fast_exp2(sc - mn);
+          tl[j] = fmaf(tl[j], alpha, pw);
+#pragma unroll
+          for (int i = 0; i < C; ++i) ta[j][i] = fmaf(ta[j][i], alpha, pw * y[i]);
+          tm[j] = mn;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int h = 4 * hg + j;
+        if (h >= G) break;
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+          const int d = lane * C + i;
+          sm_acc[warp][h][(d % VCH) * 8 + d / VCH] = ta[j][i];
+        }
+        if (lane == 0) {
+          sm_m[warp][h] = tm[j];
+          sm_l[warp][h] = tl[j];
+        }
+      }
     }
-    if (g == 0) {
-      sm_m[warp][hd] = m_run;
-      sm_l[warp][hd] = l_part;
+  } else {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+      zacc += __shfl_xor_sync(0xffffffffu, zacc, o);
+    }
+    if (hd < G) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        sm_acc[warp][hd][(2 * mt) * 8 + g] = (oacc[mt][0] + oacc[mt][1]) + zacc;
+        sm_acc[warp][hd][(2 * mt + 1) * 8 + g] = (oacc[mt][2] + oacc[mt][3]) + zacc;
+      }
+      if (g == 0) {
+        sm_m[warp][hd] = m_run;
+        sm_l[warp][hd] = l_part;
+      }
     }
   }
   __syncthreads();
-  merge_store<D, G, 8, NWARP, HG>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
+  if constexpr (K_KIVIB) {
+    DecodeArgs am = a;
+    am.nsplit = a.nsplit + 1;   // partial slots per (b, kv head): the splits and the tail
+    merge_store<D, G, 8, NWARP, HG>(c, am, b, kvh, is_tail ? nse : split, nse_all, sm_m, sm_l, &sm_acc[0][0][0]);
+  } else {
+    merge_store<D, G, 8, NWARP, HG>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
+  }
 }
 
 template <int D, int G, int KF, int VF, int NGRP>
@@ -625,7 +756,8 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   // (this kernel triggers after its main loop) and wait in the kernel for it
   // to complete before reading anything.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.nsplit, c.Hkv, c.B);
+  // KIVI_BLOCK keys: one more CTA per (b, kv head) for the full-precision tail
+  cfg.gridDim = dim3(a.nsplit + ((KF == F_KIVIB8 || KF == F_KIVIB4) ? 1 : 0), c.Hkv, c.B);
   cfg.blockDim = dim3(Shape::threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -664,13 +796,10 @@ cudaError_t launch_decode_tc_d(const CacheView& c, int G, const DecodeArgs& a, c
 
 // Tensor-core path when its preconditions hold (head_dim 64 / 128, 16-bit io,
 // key groups of at least 32 channels, each thread's value channels inside one
-// group); the exact CUDA-core kernel otherwise (fp32 outputs, head_dim 32,
-// KIVI_BLOCK keys).
+// group); the exact CUDA-core kernel otherwise (fp32 outputs, head_dim 32).
 template <int KF, int VF>
 cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st) {
-  if constexpr (KF == F_KIVIB8 || KF == F_KIVIB4) {
-    return launch_decode_cc<KF, VF>(c, G, a, st);   // per-block channel scales and the fp32 tail
-  } else {
+  {
   constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   const bool groups_ok = (!K_AFF || c.k.group >= 32) && (!V_AFF || c.v.group >= c.D / 8);

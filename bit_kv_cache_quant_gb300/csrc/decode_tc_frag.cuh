@@ -213,6 +213,12 @@ __device__ __forceinline__ void issue_tile_tma(uint8_t* st, const TileLayout& L,
     bulk_copy(st + L.vs, reinterpret_cast<const uint8_t*>(c.v.tok_scale) + row * mb, kTileTokens * mb, m);
     bulk_copy(st + L.vz, reinterpret_cast<const uint8_t*>(c.v.tok_zero) + row * mb, kTileTokens * mb, m);
   }
+  if constexpr (KF == F_KIVIB8 || KF == F_KIVIB4) {
+    // the per-channel scale and zero of the tile's block (a tile never spans two)
+    const size_t mr = (bh * (c.cap_alloc / c.k.group) + row0 / c.k.group) * D;
+    bulk_copy(st + L.kbs, c.k.blk_scale + mr, D * 2, m);
+    bulk_copy(st + L.kbz, c.k.blk_zero + mr, D * 2, m);
+  }
 }
 
 // Stage layout: the planes placed for the largest group counts the kernel

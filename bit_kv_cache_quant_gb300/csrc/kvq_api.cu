@@ -462,7 +462,7 @@ size_t kvq_decode_workspace_bytes(kvq_cache c, int32_t n_q_heads) {
   const size_t G = n_q_heads / c->cfg.n_kv_heads;
   const DecodePlan p = decode_plan(c, (int)G);
   int ns = p.nsplit > p.nsplit_tc ? p.nsplit : p.nsplit_tc;
-  if (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK) ns = p.nsplit + 1;   // the tail's partial
+  if (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK) ns += 1;   // the tail's partial
   if (ns == 1) return 0;
   return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + kvq::kPartialPad) * sizeof(float);
 }
@@ -500,7 +500,8 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   cudaError_t e;
   using namespace kvq;
   if (kf == F_KIVIB8 || kf == F_KIVIB4) {
-    if (G > 4) return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode takes up to 4 query heads per kv head");
+    if (G > 4 && (io_dtype == KVQ_DTYPE_F32 || c->cfg.head_dim == 32 || !c->view.has_maps))
+      return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode on the fp32 CUDA-core path takes up to 4 query heads per kv head");
     if (kf == F_KIVIB8 && vf == F_AFF8) e = launch_decode<F_KIVIB8, F_AFF8>(c->view, G, a, stream);
     else if (kf == F_KIVIB4 && vf == F_AFF4) e = launch_decode<F_KIVIB4, F_AFF4>(c->view, G, a, stream);
     else return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode is built for 8-bit keys with 8-bit values and 4 with 4");

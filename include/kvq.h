@@ -252,10 +252,10 @@ size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
    split across CTAs and merged with the online-softmax rule.  workspace: device,
    >= kvq_decode_workspace_bytes bytes (may be NULL when that is 0).  Calls on the
    same cache must not overlap on the GPU.  KIVI_BLOCK caches attend over the
-   quantised bulk and then the exact fp32 tail ([MLX] section 3), on the fp32
-   CUDA-core path with one more CTA per (b, kv head) for the tail.  Hq / Hkv from
-   1 to 8 on the tensor-core path (16-bit io, head_dim 64 / 128), 1 to 4 on the
-   CUDA-core path (fp32 io, head_dim 32, KIVI_BLOCK keys). */
+   quantised bulk and then the exact fp32 tail ([MLX] section 3), with one more
+   CTA per (b, kv head) for the tail.  Hq / Hkv from 1 to 8 on the tensor-core
+   path (16-bit io, head_dim 64 / 128), 1 to 4 on the CUDA-core path (fp32 io,
+   head_dim 32). */
 kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                            float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream);
 

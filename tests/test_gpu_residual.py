@@ -1,5 +1,8 @@
 """GPU parity: the KIVI residual buffer (full-precision tail, per-channel K in closed blocks).
 
+bf16 decodes run the tensor-core kernel (fragments folded with each block's
+channel scales, one CTA for the tail); fp32 decodes the CUDA-core kernel.
+
 MLX memo, section 3: recent tokens stay full precision, keys are quantised per
 channel in closed blocks once the buffer fills, and attention runs over the
 quantised bulk plus the full-precision tail.  Codes, block scales, value planes
@@ -136,5 +139,19 @@ def test_overflow_and_unsupported_calls(kvq):
         cache.evict_keepset(torch.zeros((B, H, 4), dtype=torch.int32).cuda())
     with pytest.raises(kvq.KvqError):
         cache.append(k.cuda(), k.cuda(), calibrate_k=True)
-    with pytest.raises(kvq.KvqError):
-        cache.decode_attn(torch.zeros((B, 5 * H, D), dtype=torch.bfloat16).cuda())
+    with pytest.raises(kvq.KvqError):   # over four heads per kv head: tensor-core path only (16-bit io)
+        cache.decode_attn(torch.zeros((B, 5 * H, D), dtype=torch.float32).cuda())
+
+
+@pytest.mark.parametrize("G", [5, 8])
+@pytest.mark.parametrize("n", [100, 400])
+def test_decode_up_to_eight_heads_per_kv_head(kvq, G, n):
+    B, H, D = 1, 2, 128
+    cache, oc = _pair(kvq, B, H, D, 512, (4, 64, 4, 32))
+    k = _inputs((B, H, n, D), 3 * n + G, torch.bfloat16)
+    v = _inputs((B, H, n, D), 3 * n + G + 1, torch.bfloat16, 0.0)
+    cache.append(k.cuda(), v.cuda())
+    oc.append(host(k), host(v))
+    kh, vh = oc.dequant()
+    q = _inputs((B, H * G, 1, D), 11 * n + G, torch.bfloat16, 0.0).reshape(B, H * G, D)
+    assert_attention_close(cache.decode_attn(q.cuda()), oatt.decode_attention(host(q), kh, vh), f"G={G} n={n}")
