@@ -655,7 +655,12 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     if constexpr (K_KIVIB) {
       // The fp32 tail rows [0, TT): the head group's 4 NGRP warps take rows in
       // turn, each for the group's heads, lane l for channels [l C, l C + C).
+      // A warp loads U of its rows before using any, so that the tail costs
+      // about TT / (4 NGRP U) memory round trips rather than one per row; the
+      // rows are still folded in one at a time, in order.
       constexpr int C = D / 32;
+      constexpr int U = 8;
+      constexpr int RS = 4 * NGRP;   // row stride between a warp's rows
       const int wi = (warp & 3) + 4 * grp;
       const float* tk = c.tail_k + (bh * c.k.group) * D + lane * C;
       const float* tv = c.tail_v + (bh * c.k.group) * D + lane * C;
@@ -667,30 +672,38 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
 #pragma unroll
         for (int i = 0; i < C; ++i) ta[j][i] = 0.0f;
       }
-      for (int r = wi; r < TT; r += 4 * NGRP) {
-        float x[C], y[C];
+      for (int r0 = wi; r0 < TT; r0 += RS * U) {
+        float x[U][C], y[U][C];
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-          x[i] = tk[(size_t)r * D + i];
-          y[i] = tv[(size_t)r * D + i];
+        for (int u = 0; u < U; ++u) {
+          const int r = r0 + u * RS;
+#pragma unroll
+          for (int i = 0; i < C; ++i) {
+            x[u][i] = r < TT ? tk[(size_t)r * D + i] : 0.0f;
+            y[u][i] = r < TT ? tv[(size_t)r * D + i] : 0.0f;
+          }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int h = 4 * hg + j;
-          if (h >= G) break;   // warp-uniform
-          float p = 0.0f;
+        for (int u = 0; u < U; ++u) {
+          if (r0 + u * RS >= TT) break;   // warp-uniform
 #pragma unroll
-          for (int i = 0; i < C; ++i) p = fmaf(sm_qraw[h][lane * C + i], x[i], p);
+          for (int j = 0; j < 4; ++j) {
+            const int h = 4 * hg + j;
+            if (h >= G) break;   // warp-uniform
+            float p = 0.0f;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-          const float sc = p * a.qscale;
-          const float mn = fmaxf(tm[j], sc);
-          const float alpha = fast_exp2(tm[j] - mn);
-          const float pw = fast_exp2(sc - mn);
-          tl[j] = fmaf(tl[j], alpha, pw);
+            for (int i = 0; i < C; ++i) p = fmaf(sm_qraw[h][lane * C + i], x[u][i], p);
 #pragma unroll
-          for (int i = 0; i < C; ++i) ta[j][i] = fmaf(ta[j][i], alpha, pw * y[i]);
-          tm[j] = mn;
+            for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+            const float sc = p * a.qscale;
+            const float mn = fmaxf(tm[j], sc);
+            const float alpha = fast_exp2(tm[j] - mn);
+            const float pw = fast_exp2(sc - mn);
+            tl[j] = fmaf(tl[j], alpha, pw);
+#pragma unroll
+            for (int i = 0; i < C; ++i) ta[j][i] = fmaf(ta[j][i], alpha, pw * y[u][i]);
+            tm[j] = mn;
+          }
         }
       }
 #pragma unroll
