@@ -258,6 +258,11 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        return self.summarize(out)
+
+    @staticmethod
+    def summarize(out):
+        """Median SM clock under load, max clock and the throttle reasons seen, from the sampler's CSV."""
         rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 7]
         if not rows:
             return None
@@ -284,9 +289,11 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest x over the ranks (the slowest rank's time); NCCL reduces a device tensor, gloo a host one."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 

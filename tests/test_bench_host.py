@@ -1,0 +1,114 @@
+"""Host-side logic of bench.py that needs no GPU: the algorithmic-byte model behind
+the roofline's numerator, and the clock record that decides whether a run stands.
+
+The per-layer byte counts are written out from the workloads' shapes (batch,
+kv heads, stored tokens, head_dim) and the storage formats: 4-bit codes are
+D/2 bytes a token, 8-bit codes D bytes, an fp16 scale and zero 4 bytes per
+group, a Q4_0 block one fp16 scale per 32 channels, KIVI per-channel keys one
+fp16 scale and zero per channel, and Q plus O one row per query head.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+from oracle import accounting  # noqa: E402
+
+
+def _io_bytes(w):
+    return {"float32": 4, "bfloat16": 2, "float16": 2}[w.io_dtype]
+
+
+# (workload, stored tokens T, per-layer bytes written out by hand from the shapes)
+PER_LAYER = [
+    # tinygpt: B1, 8 heads, D32, T = 4 + 256. int8 K and V codes; K per-channel fp16 scale+zero;
+    # V per-token fp16 scale+zero; fp32 Q and O.
+    ("tinygpt", 260, 8 * 260 * 32 * 2 + 8 * 32 * 4 + 8 * 260 * 4 + 2 * 8 * 32 * 4),
+    # mlx g64 4-bit: B1, Hkv 8, Hq 24, D128, T 8192. K and V: 64 code bytes + 2 groups x 4 B a token.
+    ("mlx8k", 8192, 2 * 8 * 8192 * (64 + 8) + 2 * 24 * 128 * 2),
+    # Q4_0 K + int8 V: B8, Hkv 8, Hq 32, T 32768. K: 64 code bytes + 4 fp16 block scales;
+    # V: 128 code bytes + one fp16 scale and zero a token.
+    ("q4_0_32k", 32768, 8 * 8 * 32768 * (64 + 8 + 128 + 4) + 2 * 8 * 32 * 128 * 2),
+    # KIVI int4 ring 4 + 4096: B64, Hkv 8, Hq 32. K: 64 code bytes a token + per-channel 128 x 4 B;
+    # V g32: 64 code bytes + 4 groups x 4 B a token.
+    ("ring", 4100, 64 * 8 * (4100 * (64 + 64 + 16) + 128 * 4) + 2 * 64 * 32 * 128 * 2),
+]
+
+
+@pytest.mark.parametrize("name,T,expected", PER_LAYER)
+def test_decode_bytes_closed_form(name, T, expected):
+    w = synth.get_workload(name)
+    assert bench.decode_bytes(w, T) == expected
+
+
+def test_decode_bytes_per_step_totals():
+    """Whole-step figures (every layer) of the 8K, 32K and streaming workloads."""
+    totals = {name: synth.get_workload(name).layers * expected for name, _, expected in PER_LAYER}
+    assert totals["tinygpt"] == 144_512
+    assert totals["mlx8k"] == 264_585_216
+    assert totals["q4_0_32k"] == 13_694_402_560
+    assert totals["ring"] == 9_715_056_640
+
+
+@pytest.mark.parametrize("name,T,expected", PER_LAYER)
+def test_decode_bytes_agrees_with_oracle_accounting(name, T, expected):
+    w = synth.get_workload(name)
+    got = accounting.decode_read_bytes(w.batch, w.n_kv_heads, w.n_q_heads, w.head_dim, T,
+                                       w.k_format, w.k_bits, w.k_group,
+                                       w.v_format, w.v_bits, w.v_group if w.v_group < w.head_dim else w.head_dim,
+                                       _io_bytes(w))
+    assert got == bench.decode_bytes(w, T) == expected
+
+
+def test_residual_buffer_bytes():
+    """Residual buffer of 128-token K blocks: closed blocks as 4-bit codes plus a per-(block, channel)
+    fp16 scale and zero; the T mod 128 tail as fp32 K and V rows; V g32 as in the ring workload."""
+    w = synth.get_workload("residual")
+    T = 8292                     # 64 closed blocks + a 100-row tail
+    closed, tail = 64 * 128, 100
+    per_head = closed * (64 + 64 + 16) + 64 * 128 * 4 + tail * 128 * 8
+    assert bench.decode_bytes(w, T) == 8 * per_head + 2 * 24 * 128 * 2
+
+
+def test_stored_after_streaming_cap():
+    ring = synth.get_workload("ring")
+    for t in (1, 4100, 4101, 40_000 + 4100):
+        assert bench.stored_after(ring, t) == min(t, 4100)
+    lin = synth.get_workload("mlx8k")
+    assert bench.stored_after(lin, 8193) == 8193
+
+
+FAKE_SMI = """\
+2070, 2070, 120.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active
+1965, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active
+1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active
+2010, 2070, 1310.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active
+malformed line
+"""
+
+
+def test_clock_summary_reads_reasons_and_loaded_median():
+    s = bench.ClockSampler.summarize(FAKE_SMI)
+    assert s["samples"] == 4
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["sm_mhz"] == 1980.0       # median of the three samples drawing > 30% of the peak power
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_flags_thermal_slowdown_and_empty_log():
+    hot = "1500, 2070, 1300.0, 0x20, Not Active, Active, Not Active, Not Active\n"
+    assert bench.ClockSampler.summarize(hot)["reasons"] == ["hw_thermal_slowdown"]
+    assert bench.ClockSampler.summarize("") is None
+
+
+def test_peaks_come_from_the_measured_file():
+    peak, kind = bench.read_peaks()
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured" and peak > 1000.0
+    else:
+        assert (peak, kind) == (6800.0, "fallback")
