@@ -394,3 +394,44 @@ def test_residual_needs_linear_layout_and_affine_values():
                               k_bits=4, k_group=64, v_format="affine_token", v_bits=4, v_group=32))
     with pytest.raises(ValueError):
         OracleCache(CacheSpec(1, 1, 64, 256, k_format="kivi_block", k_bits=4, k_group=64))
+
+
+def test_keepset_moves_per_token_scales_with_their_codes():
+    # "SnapKV", "How it works", step 4 on a quantised cache: each kept row
+    # carries its own per-token scales, so the dequantised cache after the
+    # keep-set is the dequantised cache before it, read at the kept rows.
+    rng = np.random.default_rng(18)
+    S, D = 48, 64
+    spec = CacheSpec(batch=2, n_kv_heads=2, head_dim=D, capacity=S, k_format="q4_0", k_bits=4, k_group=32,
+                     v_format="affine_token", v_bits=4, v_group=32)
+    c = OracleCache(spec)
+    k = (rng.standard_normal((2, 2, S, D)) * rng.uniform(0.1, 9, size=(2, 2, S, 1))).astype(np.float32)
+    v = (rng.standard_normal((2, 2, S, D)) * rng.uniform(0.1, 9, size=(2, 2, S, 1))).astype(np.float32)
+    c.append(k, v)
+    kh0, vh0 = c.dequant()
+    idx = np.stack([np.stack([np.sort(rng.choice(S, 12, replace=False)) for _ in range(2)])
+                    for _ in range(2)]).astype(np.int32)
+    c.evict_keepset(idx)
+    kh1, vh1 = c.dequant()
+    for b in range(2):
+        for h in range(2):
+            np.testing.assert_array_equal(kh1[b, h], kh0[b, h, idx[b, h]])
+            np.testing.assert_array_equal(vh1[b, h], vh0[b, h, idx[b, h]])
+
+
+def test_cache_planes_are_the_page_layout():
+    # "StreamingLLM + KIVI", "Storage layout" and "Cache-bytes table": int8
+    # codes, fp16 per-channel K scale and zero, fp16 per-token V scale and
+    # zero.  The oracle's planes hold exactly the bytes the page's accounting
+    # counts (pinned above to the page's printed totals), in fp16.
+    B, H, T, D = 1, 8, 100, 32
+    spec = CacheSpec(batch=B, n_kv_heads=H, head_dim=D, capacity=T, k_format="kivi_chan", k_bits=8,
+                     v_format="affine_token", v_bits=8, v_group=D)
+    c = OracleCache(spec)
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((B, H, T, D)).astype(np.float32)
+    c.calibrate_k(x)
+    c.append(x, x)
+    planes = [c.k.rows, c.k.ch_scale, c.k.ch_zero, c.v.rows, c.v.tok_scale, c.v.tok_zero]
+    assert all(p.dtype == np.float16 for p in planes[1:3] + planes[4:])
+    assert sum(p.nbytes for p in planes) == acc.kivi_cache_bytes(1, H, T, D, 8, batch=B)

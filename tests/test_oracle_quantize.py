@@ -220,3 +220,67 @@ def test_centering_reduces_q4_0_error_on_biased_channels():
     u1, d1 = qz.q4_0_quantize(kc)
     err1 = np.abs(qz.dequant_q4_0(u1, qz.to_fp16(d1)) + kbar[None, :, None, :] - k).mean()
     assert err1 < 0.8 * err0
+
+
+def test_exact_ties_round_to_even():
+    # Reading of "round" in the affine formula and in Q4_0: IEEE round to
+    # nearest, ties to even (the fp32 hardware rounding).  With a group
+    # spanning exactly 0..L the scale is exactly 1 and zero is 0, so every
+    # x + 0.5 sits on a tie that half-away rounding would send up.
+    x4 = np.array([[[[0, 15, 0.5, 1.5, 2.5, 3.5, 13.5, 14.5]]]], np.float32)
+    u4, s4, z4 = qz.affine_token_quantize(x4, 4, 8)
+    assert s4.ravel()[0] == 1.0 and z4.ravel()[0] == 0.0
+    assert u4.ravel().tolist() == [0, 15, 0, 2, 2, 4, 14, 14]
+    x8 = np.array([[[[0, 255, 0.5, 1.5, 126.5, 127.5, 253.5, 254.5]]]], np.float32)
+    u8, s8, _ = qz.affine_token_quantize(x8, 8, 8)
+    assert s8.ravel()[0] == 1.0
+    assert u8.ravel().tolist() == [0, 255, 0, 2, 126, 128, 254, 254]
+    # Q4_0: max|x| = 7 gives d = 1; signed ties go to the even level
+    xq = np.zeros((1, 1, 1, 32), np.float32)
+    xq[0, 0, 0, :7] = [7, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5]
+    uq, dq = qz.q4_0_quantize(xq)
+    assert dq.ravel()[0] == 1.0
+    assert (uq.ravel()[:7].astype(int) - 8).tolist() == [7, 0, 2, 2, 0, -2, -2]
+
+
+def test_q4_0_blocks_are_per_token_runs_of_32_channels():
+    # "32-element blocks with one fp16 scale" along the head vector: a token's
+    # codes and scales do not depend on the other tokens, and a spike in one
+    # channel moves only the scale of its own 32-channel block of that token.
+    rng = _rng(31)
+    x = rng.standard_normal((1, 2, 32, 128)).astype(np.float32)
+    u, d = qz.q4_0_quantize(x)
+    for t in (0, 7, 31):
+        ut, dt = qz.q4_0_quantize(x[:, :, t:t + 1])
+        np.testing.assert_array_equal(ut[:, :, 0], u[:, :, t])
+        np.testing.assert_array_equal(dt[:, :, 0], d[:, :, t])
+    y = x.copy()
+    y[0, 1, 5, 70] = 50.0
+    uy, dy = qz.q4_0_quantize(y)
+    changed = np.argwhere(dy != d)
+    assert changed.tolist() == [[0, 1, 5, 2]]
+    assert dy[0, 1, 5, 2] == np.float32(50.0) / np.float32(7.0)
+    same = np.ones(u.shape, bool)
+    same[0, 1, 5, 64:96] = False
+    np.testing.assert_array_equal(uy[same], u[same])
+
+
+def test_q4_0_stored_roundtrip():
+    # the stored path: nibbles and the fp16 scale, dequantised by the oracle's
+    # own routine, land within half a step of x plus the fp16 rounding of the
+    # scale times the largest level (7); an all-zero block reads back as zeros.
+    rng = _rng(33)
+    x = (rng.standard_normal((2, 2, 9, 64)) * rng.uniform(0.05, 20, size=(2, 2, 9, 1))).astype(np.float32)
+    x[1, 1, 3, 32:] = 0.0
+    u, d = qz.q4_0_quantize(x)
+    d16 = qz.to_fp16(d)
+    xh = qz.dequant_q4_0(u, d16)
+    rep = lambda a: np.repeat(a.astype(np.float64), 32, axis=-1)
+    bound = 0.5 * rep(d) * (1 + 1e-6) + 7 * np.abs(rep(d16) - rep(d))
+    assert np.all(np.abs(x.astype(np.float64) - xh) <= bound)
+    assert np.all(xh[1, 1, 3, 32:] == 0.0)
+    # the extreme element of every nonzero block comes back as +-7 d16
+    blk = xh.reshape(2, 2, 9, 2, 32)
+    amax = np.abs(blk).max(-1)
+    nz = d > 0
+    np.testing.assert_array_equal(amax[nz], 7 * d16.astype(np.float64)[nz])
