@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
   if (threadIdx.x == 0) {
     s_pos = c.state->pos;
     s_stored = c.state->stored;
-    const bool ok = (c.layout == KVQ_LAYOUT_RING) || (s_stored + n <= c.cap);
+    const bool ok = (c.layout == KVQ_LAYOUT_RING) || ((long long)s_stored + n <= c.cap);
     s_ok = ok ? 1 : 0;
     if (!ok && blockIdx.x == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
   }
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(256) residual_append_kernel(CacheView c, const
     s_pos = c.state->pos;
     s_stored = c.state->stored;
     s_tail = c.state->tail;
-    const int nb = (s_tail + n) / R;
-    const bool ok = s_stored + nb * R <= (c.cap / R) * R;
+    const long long nb = ((long long)s_tail + n) / R;
+    const bool ok = (long long)s_stored + nb * R <= (c.cap / R) * R;
     s_ok = ok ? 1 : 0;
     if (!ok && blockIdx.x == 0 && blockIdx.y == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
   }

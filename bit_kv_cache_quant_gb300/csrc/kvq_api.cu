@@ -138,6 +138,13 @@ kvq_status compute_layout(const kvq_config* c, kvq_cache_layout* L) {
 
   const size_t B = c->batch, H = c->n_kv_heads, BH = B * H;
   const size_t cap_alloc = align_up((size_t)c->capacity, kvq::kRowAlign);
+  // The decode kernels address a code plane as one tensor of B * Hkv * cap_alloc
+  // rows whose row coordinate is a signed 32-bit integer; keep every row and the
+  // 64-row tile after it below 2^31.
+  if (BH * cap_alloc > (size_t)INT32_MAX - kvq::kRowAlign)
+    return fail(KVQ_ERR_UNSUPPORTED,
+                "batch * n_kv_heads * capacity (rounded up to a multiple of %d rows) must stay below 2^31 - %d rows",
+                kvq::kRowAlign, kvq::kRowAlign);
   const size_t A = kvq::kPlaneAlign;
   *L = kvq_cache_layout{};
   L->cap_alloc = (int32_t)cap_alloc;

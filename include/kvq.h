@@ -183,7 +183,10 @@ typedef struct kvq_stats {
 typedef struct kvq_cache_s* kvq_cache;
 
 /* Computes the plane layout for `cfg` (no device work).  Returns INVALID_ARG or
-   UNSUPPORTED for configurations the library rejects. */
+   UNSUPPORTED for configurations the library rejects, among them caches of
+   2^31 - 64 rows or more (batch * n_kv_heads * capacity, with capacity rounded
+   up to a multiple of 64): the decode kernels address each code plane with a
+   signed 32-bit row coordinate. */
 kvq_status kvq_cache_layout_query(const kvq_config* cfg, kvq_cache_layout* out);
 
 /* Creates a cache over the caller's device buffer `dev_mem` of `bytes` bytes

@@ -153,3 +153,16 @@ def test_residual_buffer_invalid_configs(kvq, bad, code):
     base.update(bad)
     st, _ = _status(kvq, _cfg(kvq, **base))
     assert st == code, kvq.lib.kvq_last_error()
+
+
+def test_row_count_limit(kvq):
+    # each code plane is one tensor of B * Hkv * cap_alloc rows addressed with a
+    # signed 32-bit row coordinate: 2^31 - 64 rows or more are refused up front
+    st, _ = _status(kvq, _cfg(kvq, batch=1 << 16, n_kv_heads=8, capacity=4096))
+    assert st == 2 and b"2^31" in kvq.lib.kvq_last_error()
+    st, _ = _status(kvq, _cfg(kvq, batch=1, n_kv_heads=1, capacity=(1 << 31) - 1))
+    assert st == 2
+    st, lay = _status(kvq, _cfg(kvq, batch=8, n_kv_heads=8, capacity=(1 << 25) - 64))
+    assert st == 0, kvq.lib.kvq_last_error()
+    assert lay.cap_alloc == (1 << 25) - 64
+    assert lay.total_bytes > 64 * ((1 << 25) - 64) * 64 * 2      # ~256 GB of 4-bit K and V codes
