@@ -254,8 +254,23 @@ class KVCache:
         self.handle = None
         self.handle = kvq_cache_init(self.cfg, self.buf, stream)
 
+    def _check_rows(self, k: torch.Tensor, v: torch.Tensor) -> None:
+        """k, v: one shape [B, Hkv, n, D] of this cache and one dtype: the C call gets raw pointers and
+        reads both with k's dtype.  One short-circuit test on the common path (eager decode calls it
+        once per layer)."""
+        s = k.shape
+        if (s != v.shape or k.dtype is not v.dtype or len(s) != 4 or s[0] != self.batch
+                or s[1] != self.n_kv_heads or s[3] != self.head_dim):
+            if s != v.shape or k.dtype is not v.dtype:
+                raise ValueError(f"k {tuple(s)} {k.dtype} and v {tuple(v.shape)} {v.dtype} must match")
+            raise ValueError(f"k and v must be [{self.batch}, {self.n_kv_heads}, n, {self.head_dim}], "
+                             f"got {tuple(s)}")
+        if k.dtype not in DTYPES:
+            raise ValueError(f"unsupported input dtype {k.dtype}")
+
     def append(self, k: torch.Tensor, v: torch.Tensor, calibrate_k: bool = False, recompute_k: bool = False,
                stream=None) -> None:
+        self._check_rows(k, v)
         n = k.shape[2]
         flags = (APPEND_CALIBRATE_K if calibrate_k else 0) | (APPEND_RECOMPUTE_K if recompute_k else 0)
         kvq_append(self.handle, k, v, n, DTYPES[k.dtype], flags, stream)
@@ -267,6 +282,9 @@ class KVCache:
         rows contiguous) into this cache."""
         if k.shape != v.shape or k.dim() != 4 or not k.is_contiguous() or not v.is_contiguous():
             raise ValueError("k and v must be contiguous [B, Hkv, C, D] tensors of one shape")
+        self._check_rows(k, v)
+        if not 1 <= n_tokens <= k.shape[2]:
+            raise ValueError(f"n_tokens must be in 1..{k.shape[2]}")
         kvq_convert(self.handle, k, v, k.shape[2], n_tokens, DTYPES[k.dtype],
                     APPEND_CALIBRATE_K if calibrate_k else 0, stream)
         self.launches += kvq_last_launch_count()
@@ -287,8 +305,14 @@ class KVCache:
 
     def decode_attn(self, q: torch.Tensor, out: Optional[torch.Tensor] = None, softmax_scale: float = 0.0,
                     stream=None) -> torch.Tensor:
+        s = q.shape
+        if len(s) != 3 or s[0] != self.batch or s[2] != self.head_dim or q.dtype not in DTYPES:
+            raise ValueError(f"q must be [{self.batch}, Hq, {self.head_dim}] fp32 / bf16 / fp16, "
+                             f"got {tuple(q.shape)} {q.dtype}")
         if out is None:
             out = torch.empty_like(q)
+        elif out.shape != q.shape or out.dtype != q.dtype:
+            raise ValueError("out must have q's shape and dtype")
         hq = q.shape[1]
         kvq_decode_attn(self.handle, q, out, hq, DTYPES[q.dtype], softmax_scale, self.workspace(hq), stream)
         self.launches += kvq_last_launch_count()

@@ -166,3 +166,30 @@ def test_row_count_limit(kvq):
     assert st == 0, kvq.lib.kvq_last_error()
     assert lay.cap_alloc == (1 << 25) - 64
     assert lay.total_bytes > 64 * ((1 << 25) - 64) * 64 * 2      # ~256 GB of 4-bit K and V codes
+
+
+def test_binding_checks_shapes_before_any_call(kvq):
+    # the C entry points get raw pointers and cannot see shapes or dtypes; the
+    # binding refuses mismatched tensors before calling them
+    import torch
+
+    c = object.__new__(kvq.KVCache)
+    c.batch, c.n_kv_heads, c.head_dim, c.handle, c.launches, c._ws = 2, 4, 64, None, 0, {}
+    k = torch.zeros((2, 4, 3, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="must match"):
+        c.append(k, k.float())
+    with pytest.raises(ValueError, match="must match"):
+        c.append(k, k[:, :, :2])
+    with pytest.raises(ValueError, match=r"\[2, 4, n, 64\]"):
+        c.append(k[:, :3].contiguous(), k[:, :3].contiguous())
+    with pytest.raises(ValueError, match="unsupported input dtype"):
+        c.append(k.to(torch.int8), k.to(torch.int8))
+    with pytest.raises(ValueError, match="n_tokens"):
+        c.convert(k, k, 4)
+    with pytest.raises(ValueError, match="q must be"):
+        c.decode_attn(torch.zeros((2, 8, 32), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out must"):
+        q = torch.zeros((2, 8, 64), dtype=torch.bfloat16)
+        c.decode_attn(q, out=torch.zeros((2, 8, 64), dtype=torch.float32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        c.append(k, k)
