@@ -435,3 +435,51 @@ def test_cache_planes_are_the_page_layout():
     planes = [c.k.rows, c.k.ch_scale, c.k.ch_zero, c.v.rows, c.v.tok_scale, c.v.tok_zero]
     assert all(p.dtype == np.float16 for p in planes[1:3] + planes[4:])
     assert sum(p.nbytes for p in planes) == acc.kivi_cache_bytes(1, H, T, D, 8, batch=B)
+
+
+@pytest.mark.parametrize("k_fmt,k_bits,k_group,v_bits,v_group", [
+    ("affine_token", 4, 64, 4, 64), ("affine_token", 8, 32, 8, 128), ("q4_0", 4, 32, 8, 128),
+    ("q4_0", 4, 32, 4, 32), ("kivi_chan", 4, 0, 4, 32), ("kivi_chan", 8, 0, 8, 64)])
+def test_cache_round_trip_within_the_per_group_bound(k_fmt, k_bits, k_group, v_bits, v_group):
+    # "StreamingLLM + KIVI", "Affine quantisation formula" (and Q4_0's
+    # symmetric blocks): every stored element reads back within half a step
+    # of its own group's true range, plus the fp16 rounding of the stored
+    # scale (up to L steps) and zero.  The bound is computed here from the
+    # inputs alone, per group, independently of the oracle's planes.
+    rng = np.random.default_rng(23)
+    B, H, T, D = 2, 2, 40, 128
+    k = (rng.standard_normal((B, H, T, D)) * rng.uniform(0.2, 6, size=(B, H, T, 1))
+         + rng.standard_normal((B, H, 1, D))).astype(np.float32)
+    v = (rng.standard_normal((B, H, T, D)) * rng.uniform(0.2, 6, size=(B, H, T, 1))).astype(np.float32)
+    c = OracleCache(CacheSpec(batch=B, n_kv_heads=H, head_dim=D, capacity=T, k_format=k_fmt, k_bits=k_bits,
+                              k_group=k_group, v_format="affine_token", v_bits=v_bits, v_group=v_group))
+    if k_fmt == "kivi_chan":
+        c.calibrate_k(k)
+    c.append(k, v)
+    kh, vh = c.dequant()
+    u16 = 2.0 ** -11
+
+    def affine_bound(x, bits, axis_groups):
+        L = (1 << bits) - 1
+        g = axis_groups(x)
+        lo, hi = g.min(axis=-1, keepdims=True), g.max(axis=-1, keepdims=True)
+        s = np.maximum(1e-5, (hi - lo) / L)
+        b = 0.5 * s + L * s * u16 + np.abs(lo) * u16 + 2.0 ** -20 * (np.abs(g) + L * s)
+        return np.broadcast_to(b, g.shape)
+
+    # values: per token, groups of v_group channels
+    vb = affine_bound(v.astype(np.float64), v_bits, lambda x: x.reshape(B, H, T, D // v_group, v_group))
+    assert np.all(np.abs(vh - v).reshape(vb.shape) <= vb)
+    if k_fmt == "affine_token":
+        kb = affine_bound(k.astype(np.float64), k_bits, lambda x: x.reshape(B, H, T, D // k_group, k_group))
+        assert np.all(np.abs(kh - k).reshape(kb.shape) <= kb)
+    elif k_fmt == "kivi_chan":
+        # per channel over the tokens: move the token axis last
+        kt = np.swapaxes(k.astype(np.float64), 2, 3)
+        kb = affine_bound(kt, k_bits, lambda x: x)
+        assert np.all(np.abs(np.swapaxes(kh, 2, 3) - kt) <= kb)
+    else:
+        blk = k.astype(np.float64).reshape(B, H, T, D // 32, 32)
+        d = np.abs(blk).max(axis=-1, keepdims=True) / 7
+        kb = 0.5 * d * (1 + 1e-6) + 7 * d * u16
+        assert np.all(np.abs(kh.reshape(blk.shape) - blk) <= kb)

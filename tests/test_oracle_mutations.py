@@ -591,6 +591,103 @@ def _m():
     return [(oc.OracleCache, "append_recompute_k", f)]
 
 
+@mutant("ring bulk append lets an earlier token win a shared slot", ["cache"])
+def _m():
+    orig_slot = oc.ring_slot
+    orig = oc.OracleCache.append
+
+    def f(self, k, v):
+        spec = self.spec
+        if spec.layout != "ring" or spec.k_format == "kivi_block":
+            return orig(self, k, v)
+        k = np.asarray(k, np.float32)
+        v = np.asarray(v, np.float32)
+        n = k.shape[2]
+        kr, ks, kz = self.k.encode(k, spec.k_bias)
+        vr, vs, vz = self.v.encode(v, None)
+        dst = [(i, orig_slot(self.pos + i, spec.sink, spec.window)) for i in reversed(range(n))]
+        self.stored = min(self.pos + n, spec.sink + spec.window)
+        for i, slot in dst:
+            for side, rows, sc, zr in ((self.k, kr, ks, kz), (self.v, vr, vs, vz)):
+                side.rows[:, :, slot] = rows[:, :, i]
+                if sc is not None:
+                    side.tok_scale[:, :, slot] = sc[:, :, i]
+                if zr is not None:
+                    side.tok_zero[:, :, slot] = zr[:, :, i]
+        self.pos += n
+    return [(oc.OracleCache, "append", f)]
+
+
+@mutant("per-token group scales indexed by channel modulo the group count", ["cache", "quantize"])
+def _m():
+    orig = oc._Side.dequant
+
+    def f(self, n):
+        if self.fmt != "affine_token" or self.D // self.group == 1:
+            return orig(self, n)
+        B, H = self.rows.shape[:2]
+        D, g = self.D, self.group
+        ng = D // g
+        u = self.codes(n).astype(np.float64)
+        gi = np.arange(D) % ng                      # should be channel // g
+        s = self.tok_scale[:, :, :n][..., gi].astype(np.float64)
+        z = self.tok_zero[:, :, :n][..., gi].astype(np.float64)
+        return u * s + z
+    return [(oc._Side, "dequant", f)]
+
+
+@mutant("residual bulk read with the first block's scales for every block", ["cache"])
+def _m():
+    orig = oc._Side.dequant
+
+    def f(self, n):
+        if self.fmt != "kivi_block":
+            return orig(self, n)
+        u = self.codes(n)
+        return qz.dequant_affine(u, self.blk_scale[:, :, :1, :], self.blk_zero[:, :, :1, :])
+    return [(oc._Side, "dequant", f)]
+
+
+@mutant("recompute takes the range over the new keys only", ["cache"])
+def _m():
+    def f(self, k, v):
+        spec = self.spec
+        if spec.k_format != "kivi_chan" or spec.layout == "ring":
+            raise ValueError("recompute-on-append needs kivi_chan keys and a linear or compact layout")
+        k = np.asarray(k, np.float32)
+        n_old = self.stored
+        if n_old > 0:
+            u = self.k.codes(n_old).astype(np.float32)
+            s16 = self.k.ch_scale.astype(np.float32)[:, :, None, :]
+            z16 = self.k.ch_zero.astype(np.float32)[:, :, None, :]
+            x_old = (u * s16).astype(np.float32) + z16
+        self.k.calibrate(k)
+        if n_old > 0:
+            self.k.rows[:, :, :n_old] = self.k._pack(
+                qz.kivi_channel_codes(x_old, self.k.ch_scale32, self.k.ch_zero32, self.k.bits))
+        self.append(k, v)
+    return [(oc.OracleCache, "append_recompute_k", f)]
+
+
+@mutant("compact eviction drops [sink, len - window] one past the end", ["cache"])
+def _m():
+    def f(self):
+        spec = self.spec
+        if spec.layout == "ring":
+            return
+        if spec.layout != "compact":
+            raise ValueError("evict_middle needs a streaming layout")
+        L = self.stored
+        if L <= spec.sink + spec.window:
+            return
+        keep = list(range(spec.sink)) + list(range(L - spec.window + 1, L))
+        for side in (self.k, self.v):
+            for plane in side.token_planes():
+                plane[:, :, : len(keep)] = plane[:, :, keep].copy()
+        self.stored = len(keep)
+    return [(oc.OracleCache, "evict_middle", f)]
+
+
 # byte accounting ---------------------------------------------------------------
 
 @mutant("bits per element count one fp16 word per group", ["cache"])
