@@ -213,3 +213,22 @@ def test_coverage_and_random_baseline():
     sc[[50, 90, 300]] = 0.3
     idx = sk.select_indices(sc, 20, 4)
     assert sk.coverage(sc, idx) > sk.random_coverage(sc, 20, 4) + 0.5
+
+
+@pytest.mark.parametrize("scale", [0.5, 0.02, 1.7])
+def test_explicit_softmax_scale(scale):
+    # a caller-given scale replaces 1/sqrt(D): equal to torch SDPA (float64)
+    # with that scale, and to the default-scale result for q * scale * sqrt(D)
+    rng = np.random.default_rng(41)
+    B, Hkv, G, T, D = 2, 2, 2, 33, 64
+    q = rng.standard_normal((B, Hkv * G, D))
+    k = rng.standard_normal((B, Hkv, T, D))
+    v = rng.standard_normal((B, Hkv, T, D))
+    o = att.decode_attention(q, k, v, scale)
+    tq = torch.from_numpy(q)[:, :, None, :]
+    tk = torch.from_numpy(np.repeat(k, G, axis=1))
+    tv = torch.from_numpy(np.repeat(v, G, axis=1))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)[:, :, 0, :].numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(o, att.decode_attention(q * scale * math.sqrt(D), k, v), rtol=1e-12, atol=1e-13)
+    assert not np.allclose(o, att.decode_attention(q, k, v), atol=1e-3)

@@ -363,6 +363,12 @@ def _m():
     return [(att, "decode_attention", _attention_variant(values_from_keys=True))]
 
 
+@mutant("attention ignores a caller-given softmax scale", ["attention"])
+def _m():
+    orig = att.decode_attention
+    return [(att, "decode_attention", lambda q, khat, vhat, scale=None: orig(q, khat, vhat))]
+
+
 # SnapKV ----------------------------------------------------------------------
 
 def _scores_variant(rows="last", axis=1, reduce="mean", scale_of=None):
@@ -465,6 +471,18 @@ def _m():
         scores = np.asarray(scores, np.float64)
         return float(scores[np.asarray(idx)].sum() / len(idx))
     return [(sk, "coverage", f)]
+
+
+@mutant("random-coverage baseline leaves out the forced sinks", ["attention"])
+def _m():
+    def f(scores, budget, n_sink):
+        scores = np.asarray(scores, np.float64)
+        S = scores.shape[0]
+        if budget >= S:
+            return 1.0
+        ns = min(n_sink, S)
+        return float(((budget - ns) / (S - ns) * scores[ns:].sum()) / scores.sum())
+    return [(sk, "random_coverage", f)]
 
 
 # cache model -----------------------------------------------------------------
