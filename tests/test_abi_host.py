@@ -193,3 +193,28 @@ def test_binding_checks_shapes_before_any_call(kvq):
         c.decode_attn(q, out=torch.zeros((2, 8, 64), dtype=torch.float32))
     with pytest.raises(ValueError, match="CUDA tensor"):
         c.append(k, k)
+
+
+def test_readme_c_example_compiles_and_links(kvq, tmp_path):
+    # the README's C example is written against this header and this library
+    import re
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    with open(os.path.join(ROOT, "README.md")) as f:
+        code = re.search(r"```c\n(.*?)```", f.read(), re.S).group(1)
+    src = tmp_path / "example.c"
+    src.write_text(code)
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+    obj = tmp_path / "example.o"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fPIC", "-c", str(src), "-o", str(obj),
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([gcc, "-shared", "-Wl,--no-undefined", "-o", str(tmp_path / "example.so"), str(obj),
+                        "-L", os.path.dirname(kvq.LIB_PATH), "-lkvq", "-L", cuda_lib, "-lcudart"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
