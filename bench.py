@@ -714,6 +714,22 @@ def bench_recompute(kvq, w, device, warmup):
             "what": "append of one token per (batch row, kv head) recoding every stored key"}
 
 
+def coverage_stats(scores, idx, budget, n_sink):
+    """Mean over (batch row, kv head) of the kept rows' share of the score mass, and of the
+    expected share of the sinks plus (budget - n_sink) uniformly random other rows.
+    scores [B, H, S] and idx [B, H, n] tensors on any device; float64 sums."""
+    sc = scores.double()
+    tot = sc.sum(-1)
+    kept = torch.gather(sc, 2, idx.long()).sum(-1) / tot
+    S = sc.shape[-1]
+    if budget >= S:
+        rnd = torch.ones_like(tot)
+    else:
+        ns = min(n_sink, S)
+        rnd = (sc[..., :ns].sum(-1) + (budget - ns) / (S - ns) * sc[..., ns:].sum(-1)) / tot
+    return float(kept.mean()), float(rnd.mean())
+
+
 def bench_snapkv(a, kvq, w, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
     ep = SnapKVEpisode(kvq, w, device)
@@ -751,11 +767,7 @@ def bench_snapkv(a, kvq, w, rank, world):
     t_sel = sum(s_.elapsed_time(e_) for s_, e_ in sel_ev) / 1e3 / a.steps
     peak, peak_kind = read_peaks()
     achieved = sel_b / t_sel / 1e9
-    from oracle import snapkv as osk   # host arithmetic on the device's scores and indices
-
-    sc, ix = ep.scores.double().cpu().numpy(), ep.idx.cpu().numpy()
-    cov = [osk.coverage(sc[b, h], ix[b, h]) for b in range(ep.B) for h in range(ep.H)]
-    rnd = [osk.random_coverage(sc[b, h], w.budget, w.n_sink) for b in range(ep.B) for h in range(ep.H)]
+    cov_kept, cov_rnd = coverage_stats(ep.scores, ep.idx, w.budget, w.n_sink)
     line = {"metric": METRIC, "value": world * total_b * a.steps / t / 1e9, "unit": "GB/s", "n_gpus": world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": t * 1e3 / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
@@ -767,7 +779,7 @@ def bench_snapkv(a, kvq, w, rank, world):
                        "l2": "flushed (256 MiB write) after the prompt fill, before each timed episode",
                        "parallelism": f"replicas x{world}"},
             "snapkv_select_us": t_sel * 1e6,
-            "coverage": {"kept": sum(cov) / len(cov), "random_same_size": sum(rnd) / len(rnd),
+            "coverage": {"kept": cov_kept, "random_same_size": cov_rnd,
                          "what": "share of the observation-window score mass held by the kept rows, mean over "
                                  "heads, against sinks plus a uniformly random set of the same size"},
             "decode_steps_per_s": world * w.decode_steps * a.steps / t,

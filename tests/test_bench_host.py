@@ -112,3 +112,26 @@ def test_peaks_come_from_the_measured_file():
         assert kind == "measured" and peak > 1000.0
     else:
         assert (peak, kind) == (6800.0, "fallback")
+
+
+@pytest.mark.parametrize("S,budget,n_sink", [(200, 24, 4), (64, 64, 4), (64, 100, 0), (300, 17, 0)])
+def test_coverage_stats_match_the_oracle(S, budget, n_sink):
+    # the bench reports SnapKV coverage with its own torch arithmetic on the
+    # device's scores and indices; it must agree with the oracle's definitions
+    import numpy as np
+    import torch
+
+    from oracle import snapkv as osk
+
+    rng = np.random.default_rng(S + budget)
+    sc = rng.random((2, 3, S)) ** 4
+    idx = np.stack([np.stack([osk.select_indices(sc[b, h], budget, n_sink) for h in range(3)]) for b in range(2)])
+    kept, rnd = bench.coverage_stats(torch.from_numpy(sc).float(), torch.from_numpy(idx), budget, n_sink)
+    sc32 = sc.astype(np.float32).astype(np.float64)          # the bench sees fp32 scores
+    ref_kept = np.mean([osk.coverage(sc32[b, h], idx[b, h]) for b in range(2) for h in range(3)])
+    ref_rnd = np.mean([osk.random_coverage(sc32[b, h], budget, n_sink) for b in range(2) for h in range(3)])
+    assert kept == pytest.approx(ref_kept, rel=1e-12) and rnd == pytest.approx(ref_rnd, rel=1e-12)
+    if budget >= S:
+        assert kept == pytest.approx(1.0) and rnd == 1.0
+    else:
+        assert kept > rnd
