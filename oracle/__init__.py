@@ -28,6 +28,8 @@ Every function is pinned by ``tests/test_oracle_quantize.py``,
 ``tests/test_oracle_cache.py`` and ``tests/test_oracle_attention_snapkv.py``
 against closed forms, brute force, special cases that reduce to library routines and the
 pages' printed numbers (``tests/golden/``).  No function here is "parity
-unpinned".
+unpinned".  ``tests/test_oracle_mutations.py`` checks the pins in turn: each
+of its cases plants one plausible slip in a function here (on the CPU, for
+that case only) and requires a pin to fail.
 """
 from . import quantize, cache, attention, snapkv, accounting  # noqa: F401
