@@ -85,6 +85,8 @@ _proto("kvq_append", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_
 _proto("kvq_convert", c_int32, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32, c_void_p)
 _proto("kvq_evict", c_int32, c_void_p, c_int32, c_void_p, c_int32, c_void_p)
 _proto("kvq_decode_workspace_bytes", c_size_t, c_void_p, c_int32)
+_proto("kvq_decode_plan_query", c_int32, POINTER(kvq_config), c_int32, c_int32, POINTER(c_int32), POINTER(c_int32),
+       POINTER(c_int32))
 _proto("kvq_decode_attn", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p, c_size_t,
        c_void_p)
 _proto("snapkv_workspace_bytes", c_size_t, c_int32, c_int32, c_int32, c_int32, c_int32)
@@ -174,6 +176,13 @@ def kvq_evict(cache, mode: int, keep_idx: Optional[torch.Tensor] = None, n_keep:
 
 def kvq_decode_workspace_bytes(cache, n_q_heads: int) -> int:
     return lib.kvq_decode_workspace_bytes(cache, n_q_heads)
+
+
+def kvq_decode_plan_query(cfg: kvq_config, n_q_heads: int, sms: int):
+    """(splits, tensor-core splits, wide) of the decode launch for this configuration and SM count."""
+    ns, ntc, wide = c_int32(), c_int32(), c_int32()
+    _check(lib.kvq_decode_plan_query(byref(cfg), n_q_heads, sms, byref(ns), byref(ntc), byref(wide)))
+    return ns.value, ntc.value, wide.value
 
 
 def kvq_decode_attn(cache, q: torch.Tensor, out: torch.Tensor, n_q_heads: int, io_dtype: int,

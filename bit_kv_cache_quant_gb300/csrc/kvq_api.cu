@@ -474,6 +474,26 @@ size_t kvq_decode_workspace_bytes(kvq_cache c, int32_t n_q_heads) {
   return (size_t)c->cfg.batch * c->cfg.n_kv_heads * ns * G * (c->cfg.head_dim + kvq::kPartialPad) * sizeof(float);
 }
 
+kvq_status kvq_decode_plan_query(const kvq_config* cfg, int32_t n_q_heads, int32_t sms, int32_t* nsplit,
+                                 int32_t* nsplit_tc, int32_t* wide) {
+  begin_call();
+  kvq_cache_layout lay;
+  const kvq_status s = compute_layout(cfg, &lay);
+  if (s != KVQ_OK) return s;
+  if (n_q_heads < 1 || n_q_heads % cfg->n_kv_heads)
+    return fail(KVQ_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (sms < 1) return fail(KVQ_ERR_INVALID_ARG, "sms must be >= 1");
+  if (!nsplit || !nsplit_tc || !wide) return fail(KVQ_ERR_INVALID_ARG, "null output");
+  kvq_cache_s c{};   // only the configuration and the SM count enter the plan
+  c.cfg = *cfg;
+  c.sms = sms;
+  const DecodePlan p = decode_plan(&c, n_q_heads / cfg->n_kv_heads);
+  *nsplit = p.nsplit;
+  *nsplit_tc = p.nsplit_tc;
+  *wide = p.wide;
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                            float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   begin_call();

@@ -246,6 +246,22 @@ kvq_status kvq_evict(kvq_cache cache, int32_t mode, const int32_t* keep_idx, int
    the call needs none).  Depends on the cache's capacity and the SM count. */
 size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
 
+/* The launch plan kvq_decode_attn uses for a cache of configuration `cfg` with
+   n_q_heads query heads on a GPU of `sms` SMs (no device work; for tests and
+   tuning).  *nsplit: splits per (b, kv head) sized from the capacity (about
+   eight CTAs per SM in all, at least 64 rows per split, 256 from 4096 rows on,
+   at most 128); the CUDA-core kernel (fp32 io, head_dim 32) uses it.
+   *nsplit_tc: the tensor-core kernel's splits; *wide: 1 when that grid runs
+   eight-warp CTAs in a single wave (two per SM, one for over four query heads
+   per kv head) with *nsplit_tc == *nsplit, 0 when it runs smaller CTAs (four
+   warps, four per SM; eight warps, two per SM, for over four query heads per
+   kv head) over as many splits as fill two whole waves without starting a
+   third.  The kernels spread the rows actually stored over at most that many
+   splits.  Configuration errors as kvq_cache_layout_query; a bad n_q_heads or
+   sms, or a null output, is INVALID_ARG. */
+kvq_status kvq_decode_plan_query(const kvq_config* cfg, int32_t n_q_heads, int32_t sms, int32_t* nsplit,
+                                 int32_t* nsplit_tc, int32_t* wide);
+
 /* Fused decode attention over the stored rows, reading the packed codes and
    dequantising in registers ([MLX] section 5: decode reads the cache; [SLK]
    "Affine quantisation formula": attention over the dequantised K, V).

@@ -218,3 +218,58 @@ def test_readme_c_example_compiles_and_links(kvq, tmp_path):
                         "-L", os.path.dirname(kvq.LIB_PATH), "-lkvq", "-L", cuda_lib, "-lcudart"],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+# GB300: 152 SMs.  Tensor-core decode: eight-warp CTAs, two per SM (one with
+# over four query heads per kv head), when the grid fits one wave; otherwise
+# four-warp CTAs, four per SM (eight-warp, two per SM, over four heads), over
+# two whole waves.  At most 128 splits per (b, kv head).
+SMS = 152
+
+
+def _plan(kvq, n_q_heads, sms=SMS, **cfg):
+    return kvq.kvq_decode_plan_query(_cfg(kvq, **cfg), n_q_heads, sms)
+
+
+def test_decode_plan_of_the_workloads(kvq):
+    # 8K mlx layer (B1, 8 kv heads, G 3): 32 splits of 256 rows, 256 eight-warp CTAs in one wave
+    assert _plan(kvq, 24, batch=1, n_kv_heads=8, capacity=8192 + 64) == (32, 32, 1)
+    # 32K Q4_0 layer (B8, 8 kv heads, G 4): 19 splits, 1216 four-warp CTAs = two whole waves of 4 per SM
+    ns, ntc, wide = _plan(kvq, 32, batch=8, n_kv_heads=8, capacity=32768 + 64, k_format="q4_0", k_group=32,
+                          v_bits=8, v_group=128)
+    assert (ntc, wide) == (19, 0) and 64 * ntc == 2 * 4 * SMS
+    # ring 4 + 4096 (B64, 8 kv heads, G 4): 2 splits, 1024 CTAs inside two waves
+    ns, ntc, wide = _plan(kvq, 32, batch=64, n_kv_heads=8, capacity=4100, layout="ring", sink=4, window=4096,
+                          k_format="kivi_chan", k_bits=4, k_group=0, v_group=32)
+    assert (ntc, wide) == (2, 0)
+    # tinygpt (D 32, fp32: the CUDA-core kernel): 261 rows over 4 splits of at least 64
+    ns, _, _ = _plan(kvq, 8, batch=1, n_kv_heads=8, head_dim=32, capacity=261, layout="compact", sink=4,
+                     window=256, k_format="kivi_chan", k_bits=8, k_group=0, v_bits=8, v_group=32)
+    assert ns == 4
+
+
+@pytest.mark.parametrize("sms", [SMS, 148, 132])
+def test_decode_plan_invariants(kvq, sms):
+    for B, H, cap, G in [(1, 8, 8256, 3), (1, 8, 8256, 8), (2, 4, 1000, 2), (8, 8, 32832, 4), (64, 8, 4100, 4),
+                         (1, 1, 64, 1), (1, 2, 300000, 6), (16, 8, 131072, 5), (4, 8, 5000, 7)]:
+        ns, ntc, wide = _plan(kvq, G * H, sms=sms, batch=B, n_kv_heads=H, capacity=cap)
+        units = B * H
+        min_rows = 256 if cap >= 4096 else 64
+        for n in (ns, ntc):
+            assert 1 <= n <= 128
+            assert n == 1 or cap // n >= min_rows
+        if wide:
+            assert ntc == ns and units * ns <= (1 if G > 4 else 2) * sms
+        else:
+            assert units * ntc <= 2 * (2 if G > 4 else 4) * sms or ntc == 1   # never a third wave
+            assert units * ns > (1 if G > 4 else 2) * sms                    # did not fit one wide wave
+
+
+def test_decode_plan_argument_checks(kvq):
+    assert kvq.lib.kvq_decode_plan_query(None, 8, SMS, None, None, None) == 1
+    with pytest.raises(kvq.KvqError):
+        _plan(kvq, 6, batch=1, n_kv_heads=4, capacity=100)          # 6 query heads over 4 kv heads
+    with pytest.raises(kvq.KvqError):
+        _plan(kvq, 8, sms=0, batch=1, n_kv_heads=4, capacity=100)
+    with pytest.raises(kvq.KvqError):
+        _plan(kvq, 8, batch=1, n_kv_heads=4, capacity=100, head_dim=96)
