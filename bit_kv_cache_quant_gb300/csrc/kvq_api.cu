@@ -141,7 +141,7 @@ kvq_status compute_layout(const kvq_config* c, kvq_cache_layout* L) {
   // The decode kernels address a code plane as one tensor of B * Hkv * cap_alloc
   // rows whose row coordinate is a signed 32-bit integer; keep every row and the
   // 64-row tile after it below 2^31.
-  if (BH * cap_alloc > (size_t)INT32_MAX - kvq::kRowAlign)
+  if (BH > (size_t)INT32_MAX || BH * cap_alloc > (size_t)INT32_MAX - kvq::kRowAlign)
     return fail(KVQ_ERR_UNSUPPORTED,
                 "batch * n_kv_heads * capacity (rounded up to a multiple of %d rows) must stay below 2^31 - %d rows",
                 kvq::kRowAlign, kvq::kRowAlign);

@@ -162,6 +162,9 @@ def test_row_count_limit(kvq):
     assert st == 2 and b"2^31" in kvq.lib.kvq_last_error()
     st, _ = _status(kvq, _cfg(kvq, batch=1, n_kv_heads=1, capacity=(1 << 31) - 1))
     assert st == 2
+    # batch * n_kv_heads * capacity near 2^93 must not wrap around into an accepted size
+    st, _ = _status(kvq, _cfg(kvq, batch=(1 << 31) - 1, n_kv_heads=(1 << 31) - 1, capacity=(1 << 31) - 64))
+    assert st == 2
     st, lay = _status(kvq, _cfg(kvq, batch=8, n_kv_heads=8, capacity=(1 << 25) - 64))
     assert st == 0, kvq.lib.kvq_last_error()
     assert lay.cap_alloc == (1 << 25) - 64
