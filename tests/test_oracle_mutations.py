@@ -319,6 +319,31 @@ def _m():
     return [(qz, "to_fp16", f)]
 
 
+@mutant("nibbles unpacked high nibble first", ["quantize", "cache"])
+def _m():
+    def f(b):
+        b = np.asarray(b, np.uint8)
+        out = np.empty(b.shape[:-1] + (b.shape[-1] * 2,), dtype=np.uint8)
+        out[..., 0::2] = b >> 4
+        out[..., 1::2] = b & 0x0F
+        return out
+    return [(qz, "unpack_nibbles", f)]
+
+
+@mutant("signed 8-bit level read back with offset 127", ["quantize", "cache"])
+def _m():
+    return [(qz, "int8_to_codes", lambda q: (np.asarray(q).astype(np.int16) + 127).astype(np.uint8))]
+
+
+@mutant("new keys coded against the scale and zero of the previous channel", ["quantize", "cache"])
+def _m():
+    orig = qz.affine_codes
+
+    def f(k, scale, zero, bits):
+        return orig(k, np.roll(scale, 1, axis=-1)[:, :, None, :], np.roll(zero, 1, axis=-1)[:, :, None, :], bits)
+    return [(qz, "kivi_channel_codes", f)]
+
+
 # attention -------------------------------------------------------------------
 
 def _attention_variant(kv_head=None, scale_of=None, normalise=True, values_from_keys=False):
