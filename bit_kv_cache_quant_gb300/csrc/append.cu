@@ -6,7 +6,8 @@
 // "Low-bit KV caches on MLX", section 1: the same affine rule per token and
 // per 64-channel group.  "kv-cache: optional per-channel K-cache
 // mean-centering for Q4_0": subtract the per-(kv head, channel) bias, then
-// quantise symmetric 32-channel blocks.
+// code symmetric blocks (32 channels, one fp16 scale: the Q4_0 layout, which
+// the page does not spell out).
 #include "kvq_internal.cuh"
 
 namespace kvq {

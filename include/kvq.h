@@ -74,8 +74,11 @@ typedef enum kvq_format {
      QuantizedKVCache with group = 64 ([MLX] section 1).  bits 8 or 4; group a
      multiple of 16 dividing D.                                                      */
   KVQ_FMT_AFFINE_TOKEN = 2,
-  /* symmetric 32-channel blocks, one fp16 scale, no zero point ([KMC] "The idea").
-     bits 4, group 32.  K side only; the only format that accepts a K bias.        */
+  /* symmetric blocks of 32 channels, one fp16 scale each, no zero point.  [KMC]
+     "The idea" calls Q4_0 a symmetric block quantiser without a zero point; the
+     32-channel block and its fp16 scale are the Q4_0 layout, which the page does
+     not spell out.  bits 4, group 32.  K side only; the only format that accepts
+     a K bias.                                                                       */
   KVQ_FMT_Q4_0 = 3,
   /* KIVI residual buffer ([MLX] section 3, "What KIVI and KVQuant found"): the most
      recent tokens stay at full precision (fp32) in a tail of fewer than `group` = R
@@ -199,7 +202,8 @@ kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cu
 void kvq_cache_release(kvq_cache cache);
 
 /* Quantise-on-append ([SLK] "Implementation": after each per-layer append;
-   [KMC] "Why this is safe": one subtract at the point of cache write).
+   [KMC] "Why this is safe": the bias costs a single subtraction when K is
+   written).
    k, v: device [B, Hkv, n, D] of `in_dtype` (kvq_dtype).  Tokens take absolute
    positions pos .. pos + n - 1.  LINEAR / COMPACT write rows stored .. stored + n - 1
    (device overflow -> KVQ_DEV_OVERFLOW, nothing written); RING writes each

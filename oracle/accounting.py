@@ -2,8 +2,8 @@
 
 "StreamingLLM + KIVI", "Storage layout" and "Cache-bytes table": per layer,
 codes [B, H, T, D] plus fp16 kScales/kZeros [B, H, D] and vScales/vZeros
-[B, H, T].  "Low-bit KV caches on MLX", section 4: a 64-element group's
-fp16 scale and bias add half a bit per element.
+[B, H, T].  "Low-bit KV caches on MLX", section 4: with groups of 64
+elements, the two fp16 values of each group cost an extra 0.5 bit per element.
 """
 from __future__ import annotations
 

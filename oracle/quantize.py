@@ -10,15 +10,17 @@ from __future__ import annotations
 import numpy as np
 
 # "StreamingLLM + KIVI" page, section "Affine quantisation formula":
-# eps = 1e-5 guards the scale, and (qMin, qMax) is (-128, 127) for int8 and
-# (-8, 7) for int4 (the "clamped to +-7" remark under "Storage layout" is
-# read as this same (-8, 7) range).
+# the scale never falls below eps = 1e-5; the level range is -128..127 at
+# 8 bits and -8..7 at 4 bits (the "clamped to +-7" remark under "Storage
+# layout" is read as this same 4-bit range).
 EPS = np.float32(1e-5)
 QRANGE = {8: (-128, 127), 4: (-8, 7)}
 
-# Symmetric Q4_0: 32-element blocks, one fp16 scale, no zero point ("kv-cache:
-# optional per-channel K-cache mean-centering for Q4_0", section "The idea").
-# The page gives no arithmetic; the reading used is d = max|x| / 7 and
+# Symmetric Q4_0: the page ("kv-cache: optional per-channel K-cache
+# mean-centering for Q4_0", section "The idea") calls it a symmetric block
+# quantiser without a zero point, and gives neither block size nor
+# arithmetic.  The layout used is that of the Q4_0 K-cache workload, blocks of
+# 32 elements with one fp16 scale; the reading is d = max|x| / 7 and
 # q = clamp(rint(x / d), -8, 7), stored as the nibble q + 8.
 Q4_0_BLOCK = 32
 Q4_0_QMAX = np.float32(7.0)
@@ -61,8 +63,8 @@ def affine_codes(x: np.ndarray, scale: np.ndarray, zero: np.ndarray, bits: int) 
 def kivi_channel_calibrate(k: np.ndarray, bits: int):
     """Per-(b, kv-head, channel) scale and zero over the token axis of k [B,H,T,D].
 
-    KIVI keys are quantised per channel: one (scale, zero) per (batch, head,
-    channel) shared by all stored tokens ("StreamingLLM + KIVI", "KIVI --
+    KIVI codes keys channel by channel: every stored token of a (batch row,
+    head) uses that channel's single (scale, zero) ("StreamingLLM + KIVI", "KIVI --
     int8/int4 KV cache").  Here the scales are computed once from the tokens
     given and then frozen (the group-boundary freezing the page's caveats
     attribute to the KIVI paper); returns fp32 [B,H,D] scale and zero.

@@ -3,9 +3,9 @@
 bf16 decodes run the tensor-core kernel (fragments folded with each block's
 channel scales, one CTA for the tail); fp32 decodes the CUDA-core kernel.
 
-MLX memo, section 3: recent tokens stay full precision, keys are quantised per
-channel in closed blocks once the buffer fills, and attention runs over the
-quantised bulk plus the full-precision tail.  Codes, block scales, value planes
+MLX memo, section 3: the newest tokens are kept unquantised; when the buffer is
+full, its keys are quantised per channel as one closed block; attention reads the
+quantised bulk and then the unquantised tail.  Codes, block scales, value planes
 and the fp32 tail are compared bit-exactly with the oracle; attention within
 the decode tolerance of the io dtype.
 """
