@@ -124,9 +124,9 @@ def mean_center(k: np.ndarray, kbar: np.ndarray) -> np.ndarray:
     """k - kbar[kv-head, channel] in fp32, the subtraction made right before K is quantised.
 
     "kv-cache: optional per-channel K-cache mean-centering for Q4_0",
-    sections "Summary" and "Why this is safe": a fixed per-(kv-head,
-    channel) bias is subtracted at cache-write time and nothing is added
-    back at decode.
+    sections "Summary" and "Why this is safe": one precomputed value per
+    (kv head, channel) comes off K as it is written to the cache, and decode
+    adds nothing back.
     """
     k = np.asarray(k, dtype=np.float32)
     kbar = np.asarray(kbar, dtype=np.float32)

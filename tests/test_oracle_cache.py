@@ -281,9 +281,9 @@ def test_recompute_gate():
 
 
 # ------------------------------------------------------------ KIVI residual buffer
-# MLX memo, section 3: recent tokens stay full precision; keys are quantised
-# per channel in closed blocks once the buffer fills; attention runs over the
-# quantised bulk plus the full-precision tail.
+# MLX memo, section 3: the newest tokens are kept unquantised; a full buffer's
+# keys are quantised per channel as one closed block; attention reads the
+# quantised bulk and then the unquantised tail.
 
 def _residual_spec(R=64, bits=4, D=64, cap=512):
     return CacheSpec(batch=2, n_kv_heads=2, head_dim=D, capacity=cap, k_format="kivi_block", k_bits=bits,
