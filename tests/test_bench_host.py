@@ -135,3 +135,25 @@ def test_coverage_stats_match_the_oracle(S, budget, n_sink):
         assert kept == pytest.approx(1.0) and rnd == 1.0
     else:
         assert kept > rnd
+
+
+@pytest.mark.parametrize("name", ["tinygpt", "mlx8k", "q4_0_32k", "snapkv", "ring", "residual"])
+def test_reference_arm_line(name, capsys):
+    # `bench.py --impl reference`: the oracle on a bounded sample of the workload, one JSON line
+    import json
+
+    a = bench.parse_args(["--impl", "reference", "--workload", name, "--steps", "1", "--warmup", "1"])
+    assert a.warmup == 3                                   # at least three warm-up steps, always
+    bench.run_reference(a, 0, 1)
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    w = synth.get_workload(name)
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["config"]["workload"] == w.name
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["scaling"], d["data"]) == (1, 1, 3, "weak", "synthetic")
+    assert d["vs_baseline"] is None and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["value"] == d["value"] and cb["unit"] == "GB/s" and cb["kind"] == "oracle" and cb["cores"] == 1
+    assert cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
