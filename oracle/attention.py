@@ -38,3 +38,41 @@ def decode_attention(q: np.ndarray, khat: np.ndarray, vhat: np.ndarray, scale: f
             p /= p.sum()
             out[b, h] = p @ vhat[b, kv]
     return out
+
+
+def split_partials(q: np.ndarray, khat: np.ndarray, vhat: np.ndarray, bounds, scale: float | None = None):
+    """Per-split online-softmax state of one query against rows [t0, t1) of its kv head.
+
+    q [D]; khat, vhat [T, D]; bounds a list of (t0, t1).  For each split:
+    m = max of its scores, l = sum of exp(s - m), acc = sum of exp(s - m) v
+    (float64).  An empty split has m = -inf, l = 0, acc = 0.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    khat = np.asarray(khat, dtype=np.float64)
+    vhat = np.asarray(vhat, dtype=np.float64)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    parts = []
+    for t0, t1 in bounds:
+        if t1 <= t0:
+            parts.append((-math.inf, 0.0, np.zeros(q.shape[-1])))
+            continue
+        s = (khat[t0:t1] @ q) * scale
+        m = float(s.max())
+        p = np.exp(s - m)
+        parts.append((m, float(p.sum()), p @ vhat[t0:t1]))
+    return parts
+
+
+def merge_partials(parts) -> np.ndarray:
+    """Output of the splits' states merged by the online-softmax rule.
+
+    m* = max_i m_i;  l* = sum_i l_i exp(m_i - m*);  o = sum_i acc_i exp(m_i - m*) / l*.
+    Empty splits (m = -inf) contribute nothing.  Exact up to rounding: the
+    result is the softmax-weighted sum over the union of the splits' rows.
+    """
+    live = [(m, l, a) for m, l, a in parts if m != -math.inf]
+    m_star = max(m for m, _, _ in live)
+    l_star = sum(l * math.exp(m - m_star) for m, l, _ in live)
+    acc = sum(a * math.exp(m - m_star) for m, _, a in live)
+    return acc / l_star

@@ -232,3 +232,44 @@ def test_explicit_softmax_scale(scale):
     np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(o, att.decode_attention(q * scale * math.sqrt(D), k, v), rtol=1e-12, atol=1e-13)
     assert not np.allclose(o, att.decode_attention(q, k, v), atol=1e-3)
+
+
+def _random_bounds(rng, T, n):
+    cuts = np.sort(rng.integers(0, T + 1, size=n - 1))
+    edges = [0, *cuts.tolist(), T]
+    return [(edges[i], edges[i + 1]) for i in range(n)]
+
+
+@pytest.mark.parametrize("T,n", [(1, 1), (7, 3), (64, 1), (300, 5), (300, 32), (1000, 128)])
+def test_split_merge_equals_unsplit_attention(T, n):
+    # the split-KV merge rule: any partition of the rows into splits, empty ones
+    # included and in any order, merges to the same output as one softmax over all rows
+    rng = np.random.default_rng(T * 131 + n)
+    D = 64
+    q = rng.standard_normal(D) * 2
+    k = rng.standard_normal((T, D)) * 1.5
+    v = rng.standard_normal((T, D))
+    ref = att.decode_attention(q[None, None], k[None, None], v[None, None])[0, 0]
+    bounds = _random_bounds(rng, T, n)
+    parts = att.split_partials(q, k, v, bounds)
+    np.testing.assert_allclose(att.merge_partials(parts), ref, rtol=1e-12, atol=1e-13)
+    order = rng.permutation(len(parts))
+    np.testing.assert_allclose(att.merge_partials([parts[i] for i in order]), ref, rtol=1e-12, atol=1e-13)
+    # one split per row: each split's l is 1 and acc its own value row
+    singles = att.split_partials(q, k, v, [(t, t + 1) for t in range(T)])
+    assert all(l == 1.0 for _, l, _ in singles)
+    np.testing.assert_allclose(att.merge_partials(singles), ref, rtol=1e-12, atol=1e-13)
+
+
+def test_split_merge_with_far_apart_maxima():
+    # splits whose maxima differ by hundreds: exp(m_i - m*) underflows to 0 for
+    # the low split without producing NaN, and the high split decides the output
+    D = 16
+    q = np.ones(D)
+    k = np.zeros((4, D))
+    k[2:] = 100.0
+    v = np.arange(4 * D, dtype=np.float64).reshape(4, D)
+    parts = att.split_partials(q, k, v, [(0, 2), (2, 4)], scale=1.0)
+    out = att.merge_partials(parts)
+    np.testing.assert_allclose(out, v[2:].mean(axis=0), rtol=1e-12)
+    assert np.all(np.isfinite(out))

@@ -394,6 +394,33 @@ def _m():
     return [(att, "decode_attention", lambda q, khat, vhat, scale=None: orig(q, khat, vhat))]
 
 
+@mutant("split merge sums the l terms without rescaling them", ["attention"])
+def _m():
+    def f(parts):
+        live = [(m, l, a) for m, l, a in parts if m != -math.inf]
+        ms = max(m for m, _, _ in live)
+        return sum(a * math.exp(m - ms) for m, _, a in live) / sum(l for _, l, _ in live)
+    return [(att, "merge_partials", f)]
+
+
+@mutant("split merge rescales by exp(m* - m_i)", ["attention"])
+def _m():
+    def f(parts):
+        live = [(m, l, a) for m, l, a in parts if m != -math.inf]
+        ms = max(m for m, _, _ in live)
+        return (sum(a * math.exp(ms - m) for m, _, a in live)
+                / sum(l * math.exp(ms - m) for m, l, _ in live))
+    return [(att, "merge_partials", f)]
+
+
+@mutant("split merge averages the splits' outputs", ["attention"])
+def _m():
+    def f(parts):
+        live = [(m, l, a) for m, l, a in parts if m != -math.inf]
+        return sum(a / l for _, l, a in live) / len(live)
+    return [(att, "merge_partials", f)]
+
+
 # SnapKV ----------------------------------------------------------------------
 
 def _scores_variant(rows="last", axis=1, reduce="mean", scale_of=None):
