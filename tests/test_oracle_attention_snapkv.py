@@ -273,3 +273,19 @@ def test_split_merge_with_far_apart_maxima():
     out = att.merge_partials(parts)
     np.testing.assert_allclose(out, v[2:].mean(axis=0), rtol=1e-12)
     assert np.all(np.isfinite(out))
+
+
+def test_softmax_shift_invariance():
+    # adding one vector c_h to every key of kv head h adds q . c_h to every score
+    # of each query on that head, the same constant across its row: the output
+    # must not move (a per-token shift, by contrast, must)
+    rng = np.random.default_rng(43)
+    B, Hkv, G, T, D = 2, 3, 2, 50, 32
+    q = rng.standard_normal((B, Hkv * G, D))
+    k = rng.standard_normal((B, Hkv, T, D))
+    v = rng.standard_normal((B, Hkv, T, D))
+    c = rng.standard_normal((B, Hkv, 1, D)) * 5
+    o = att.decode_attention(q, k, v)
+    np.testing.assert_allclose(att.decode_attention(q, k + c, v), o, rtol=1e-10, atol=1e-12)
+    per_token = rng.standard_normal((B, Hkv, T, 1)) * c
+    assert not np.allclose(att.decode_attention(q, k + per_token, v), o, atol=1e-3)
