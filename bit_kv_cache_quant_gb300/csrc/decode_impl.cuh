@@ -188,28 +188,48 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   constexpr int PROW = D + kPartialPad;
   constexpr int AROW = D + ACCPAD;
   constexpr int NTHR = 32 * NWARP;
+  static_assert(NWARP <= 32, "one lane per warp in the per-head reduction");
   __shared__ float sm_w[kMaxSplits][G];
   __shared__ float sm_lsum[kMaxSplits][G];
   __shared__ float sm_inv[G];
+  __shared__ float sm_we[NWARP][G];   // weight of warp w's state in head h's CTA merge
+  __shared__ float sm_hm[G];          // CTA max and sum of each head
+  __shared__ float sm_hl[G];
   __shared__ int s_last;
   const size_t bh = (size_t)b * c.Hkv + kvh;
-  // Merge the warps; write the output (one split) or this split's partial.
+  // Merge the warps.  One warp per head first finds the CTA's max over the
+  // warps holding that head, each warp's weight 2^(m_w - M) and the weighted
+  // sum, so that every (head, channel) output then takes one multiply-add per
+  // warp; then write the output (one split) or this split's partial.
+  {
+    const int lane = threadIdx.x & 31;
+    for (int h = threadIdx.x >> 5; h < G; h += NWARP) {
+      const bool mine = lane < NWARP && (HG == 1 || ((lane >> 2) % HG) == (h >> 2));
+      const float mw = mine ? sm_m[lane][h] : neg_inf();
+      float M = mw;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float e = (mw == neg_inf()) ? 0.0f : exp2f(mw - M);
+      float L = mine ? sm_l[lane][h] * e : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane < NWARP) sm_we[lane][h] = e;
+      if (lane == 0) {
+        sm_hm[h] = M;
+        sm_hl[h] = L;
+      }
+    }
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += NTHR) {
     const int h = idx / D, d = idx % D;
     const int pos = h * AROW + (ACCPAD ? (d % (D / 8)) * 8 + d / (D / 8) : d);
-    float M = neg_inf();
+    const float M = sm_hm[h], L = sm_hl[h];
+    float A = 0.0f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w)
-      if (HG == 1 || ((w >> 2) % HG) == (h >> 2)) M = fmaxf(M, sm_m[w][h]);
-    float A = 0.0f, L = 0.0f;
-    if (M != neg_inf()) {
-#pragma unroll
-      for (int w = 0; w < NWARP; ++w) {
-        if (HG > 1 && ((w >> 2) % HG) != (h >> 2)) continue;
-        const float e = (sm_m[w][h] == neg_inf()) ? 0.0f : exp2f(sm_m[w][h] - M);
-        A = fmaf(sm_acc[w * G * AROW + pos], e, A);
-        L = fmaf(sm_l[w][h], e, L);
-      }
+    for (int w = 0; w < NWARP; ++w) {
+      if (HG > 1 && ((w >> 2) % HG) != (h >> 2)) continue;
+      A = fmaf(sm_acc[w * G * AROW + pos], sm_we[w][h], A);
     }
     if (nse == 1) {
       const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;

@@ -137,7 +137,8 @@ __device__ __forceinline__ void pvt_mma(float (&oacc)[MT][4], const uint32_t (&p
 // heads 4 j .. 4 j + 3 over the same stages (HG = 2 for five to eight heads per
 // kv head).  Four-warp CTAs (four per SM) suit grids of several waves;
 // eight-warp tile pairs (two per SM) halve the time per split when the whole
-// grid fits in one wave.
+// grid fits in one wave; sixteen-warp CTAs of four tile groups (one per SM)
+// give a one-wave grid of few (b, kv head) units the most warps per tile.
 template <int NGRP, int HG> struct TcShape {
   static constexpr int warps = 4 * NGRP * HG;
   static constexpr int threads = 32 * warps;
@@ -150,7 +151,7 @@ template <int G> struct TcHeads {
 
 // Pipeline depth.  Four-warp CTAs (four per SM, several waves) use two
 // stages: deeper rings measured slower on the 32K and ring workloads, whose
-// time is instruction issue, not latency.  Eight-warp CTAs (one wave) take as
+// time is instruction issue, not latency.  Larger CTAs (one wave) take as
 // many stages (a multiple of NGRP, up to 8) as fit next to the static shared
 // memory, so that a short split is requested in one go.
 template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
@@ -200,6 +201,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   constexpr bool K_KIVIB = (KF == F_KIVIB8 || KF == F_KIVIB4);
   constexpr int NACC = KG ? NB : 1;
+  // tiles of the split requested into L2 before the dependency wait: the
+  // whole initial ring of a one-wave grid, four tiles for a CTA of several
+  // waves (whose later tiles would only crowd L2)
+  constexpr int PF_TILES = NGRP == 1 ? 4 : NSTAGE;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per kv head");
   static_assert(NSTAGE % NGRP == 0, "each stage serves one tile group");
 
@@ -229,17 +234,43 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
 
   // Before the grids this launch depends on have finished (programmatic
-  // dependent launch), touch only what they cannot change: the tensor maps,
-  // this CTA's barriers, and L2 / address-translation hints for the first
-  // rows this split would read at full capacity.
+  // dependent launch), touch only what they cannot change: the tensor maps
+  // and this CTA's barriers.  Besides, request into L2 the first rows of the
+  // split this CTA would read if the stored length were what the counter
+  // holds now.  That read races with a producer still running, so it is only
+  // a hint: the rows are clamped to this (b, kv head)'s allocation, and a
+  // prefetch into L2 (the point of coherence) never serves stale data.
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
-    const size_t row0 = bh * c.cap_alloc + (size_t)split * ((c.cap + a.nsplit - 1) / a.nsplit);
-    prefetch_l2(c.k.codes + row0 * KROW);
-    prefetch_l2(c.v.codes + row0 * VROW);
-    if constexpr (KG) prefetch_l2(c.k.tok_scale + row0 * c.k.n_groups);
-    if constexpr (V_AFF) prefetch_l2(c.v.tok_scale + row0 * c.v.n_groups);
+    if constexpr (!K_KIVIB) {
+      const int Th = min(max(*reinterpret_cast<volatile const int*>(&c.state->stored), 0), c.cap_alloc);
+      int h0, h1, hn;
+      split_rows(Th, a.nsplit, split, h0, h1, hn);
+      if (split < hn && h1 > h0) {
+        // whole tiles (every plane offset of a 64-row boundary is 16-byte
+        // aligned), at most PF_TILES of them
+        const int r1 = min(min((h1 + kTileTokens - 1) / kTileTokens * kTileTokens, c.cap_alloc),
+                           h0 + PF_TILES * kTileTokens);
+        const size_t row0 = bh * c.cap_alloc + h0;
+        const uint32_t nr = (uint32_t)(r1 - h0);
+        prefetch_l2_bulk(c.k.codes + row0 * KROW, nr * KROW);
+        prefetch_l2_bulk(c.v.codes + row0 * VROW, nr * VROW);
+        if constexpr (KG) prefetch_l2_bulk(c.k.tok_scale + row0 * c.k.n_groups, nr * 2 * c.k.n_groups);
+        if constexpr (K_AFF) prefetch_l2_bulk(c.k.tok_zero + row0 * c.k.n_groups, nr * 2 * c.k.n_groups);
+        if constexpr (V_AFF) {
+          prefetch_l2_bulk(c.v.tok_scale + row0 * c.v.n_groups, nr * 2 * c.v.n_groups);
+          prefetch_l2_bulk(c.v.tok_zero + row0 * c.v.n_groups, nr * 2 * c.v.n_groups);
+        }
+      }
+    }
+    // the query rows of this kv head (the producer may still write them, so
+    // they are only requested into L2)
+    {
+      const int es = a.io_dtype == KVQ_DTYPE_F32 ? 4 : 2;
+      const uint8_t* q0 = reinterpret_cast<const uint8_t*>(a.q) + ((size_t)b * a.Hq + (size_t)kvh * G) * D * es;
+      for (int off = 0; off < G * D * es; off += 128) prefetch_l2(q0 + off);
+    }
     s_fail = 0;
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) {
@@ -251,30 +282,37 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     fence_async_smem();   // the initialised barriers are visible to the copy engine
   }
   grid_dependency_wait();
+  // Every CTA of this grid is resident: the next launch may start its own
+  // prologue (and L2 requests) while this one runs.
+  grid_launch_dependents();
   // Warp roles: 16-row block of each tile, head group, tile group.
   const int blk = (warp & 3) * 16;
   const int hg = (warp >> 2) % HG;
   const int grp = (warp >> 2) / HG;
   const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
-  // Thread 0 reads the stored length and requests the whole initial ring
-  // of tiles while the query fragments are built (requesting each group's
-  // first tile alone, ahead of the rest, measured slower once the request
-  // moved before the fragment build).
+  // Warp 0 reads the stored length and requests the whole initial ring of
+  // tiles, lane s the tile of stage s (one thread issuing the whole ring
+  // serialises the requests), while the other warps build their query
+  // fragments.
   // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
   // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
   // columns and q enters exactly.  Thread (g, t) builds column g at the key
   // channels of its fragment slots.
-  if (threadIdx.x == 0) {
-    const int T0 = c.state->stored;
-    s_T = T0;
-    if constexpr (K_KIVIB) s_tail = c.state->tail;
+  if (warp == 0) {
+    int T0 = 0;
+    if (lane == 0) {
+      T0 = c.state->stored;
+      s_T = T0;
+      if constexpr (K_KIVIB) s_tail = c.state->tail;
+    }
+    T0 = __shfl_sync(0xffffffffu, T0, 0);
     int a0, a1, ns0;
     split_rows(T0, a.nsplit, split, a0, a1, ns0);
     if (split < ns0) {
       const int nt0 = (a1 - a0 + kTileTokens - 1) / kTileTokens;
-      for (int s0 = 0; s0 < NSTAGE && s0 < nt0; ++s0) {
-        issue_tile_tma<D, KF, VF>(smem + s0 * TL.bytes, TL, c, bh, a0 + s0 * kTileTokens, &mbar[s0]);
-        s_last_tile[s0] = s0;
+      if (lane < NSTAGE && lane < nt0) {
+        issue_tile_tma<D, KF, VF>(smem + lane * TL.bytes, TL, c, bh, a0 + lane * kTileTokens, &mbar[lane]);
+        s_last_tile[lane] = lane;
       }
     }
   }
@@ -283,6 +321,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     const int hq = 4 * hg + (g >> 1);
     const bool live = hq < G;
     const size_t qo = ((size_t)b * a.Hq + (size_t)kvh * G + (live ? hq : 0)) * D;
+    // the thread's query values at its fragment channels (key_channels), in
+    // 16-byte (4-bit keys) or 8-byte loads when the row is 16-byte aligned
+    float xq[KS][4];
+    load_query_channels<D, KB>(a.q, qo, a.io_dtype, t, live, xq);
     float qb[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i) qb[i] = 0.0f;
@@ -293,7 +335,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       float x[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float v = live ? load_io(a.q, qo + ch[i], a.io_dtype) : 0.0f;
+        float v = xq[ks][i];
         if constexpr (K_KIVI) v *= __half2float(c.k.ch_scale[bh * D + ch[i]]);
         x[i] = v;
       }
@@ -635,7 +677,6 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     }
   }
   __syncthreads();
-  grid_launch_dependents();   // the next launch may start its prologue during this merge
   if (s_fail) {
     // A stage never arrived: report it, wait (bounded) for the copies still
     // in flight into this CTA's shared memory, and leave the outputs alone.
@@ -754,20 +795,19 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   using S = TcStages<D, G, KF, VF, NGRP>;
   using Shape = typename S::Shape;
+  auto kern = decode_tc_kernel<D, G, KF, VF, NGRP>;
   const int smem = S::dyn_bytes(L.bytes);
   static_assert(S::dyn_bytes(S::stage) + S::static_smem <= 227 * 1024, "shared memory per CTA");
-  static int configured = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, KF, VF, NGRP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::dyn_bytes(tc_layout<D, KF, VF>(S::kng_max, S::vng_max).bytes));
-    if (e != cudaSuccess) return e;
-    configured = 1;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = once_per_device(configured, [&]() {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                S::dyn_bytes(tc_layout<D, KF, VF>(S::kng_max, S::vng_max).bytes));
+  });
+  if (e != cudaSuccess) return e;
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: its CTAs may start once that kernel's CTAs have all triggered
-  // (this kernel triggers after its main loop) and wait in the kernel for it
-  // to complete before reading anything.
+  // (this kernel triggers right after its own dependency wait) and wait in
+  // the kernel for it to complete before reading anything.
   cudaLaunchConfig_t cfg = {};
   // KIVI_BLOCK keys: one more CTA per (b, kv head) for the full-precision tail
   cfg.gridDim = dim3(a.nsplit + ((KF == F_KIVIB8 || KF == F_KIVIB4) ? 1 : 0), c.Hkv, c.B);
@@ -779,7 +819,7 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, G, KF, VF, NGRP>, c, a);
+  e = cudaLaunchKernelEx(&cfg, kern, c, a);
   note_launch();
   return e;
 }
@@ -789,6 +829,10 @@ cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStr
   DecodeArgs at = a;
   at.nsplit = a.nsplit_tc;
   if (at.nsplit < 1 || at.nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  if constexpr (G <= 4) {
+    if (a.wide == 2) return launch_decode_tc_shape<D, G, KF, VF, 4>(c, at, st);
+  }
+  if (a.wide == 2) return cudaErrorInvalidValue;   // the plan gives sixteen-warp CTAs up to four heads only
   return a.wide ? launch_decode_tc_shape<D, G, KF, VF, 2>(c, at, st) : launch_decode_tc_shape<D, G, KF, VF, 1>(c, at, st);
 }
 

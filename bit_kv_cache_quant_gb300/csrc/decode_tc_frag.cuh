@@ -258,6 +258,14 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
 }
 
+// A hint: bring `bytes` bytes at p into L2 with one bulk request (p 16-byte
+// aligned, bytes a multiple of 16).  L2 is the GPU's point of coherence, so
+// a prefetch issued before a producer kernel has finished writing cannot
+// leave a stale copy behind; it only wastes bandwidth if the data changes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Key channel order: k-step ks, mma k index 2t + jj (jj in {0, 1}) and
 // 2t + 8 + jj of quad thread t.  4-bit codes: thread t reads word t of chunk
 // ks / 2 (channels 32 (ks / 2) + 8 t + 0..7), nibble pairs (c0, c4), (c2, c6)
@@ -272,6 +280,52 @@ __device__ __forceinline__ void key_channels(int ks, int t, int (&ch)[4]) {
   } else {
     const int base = 16 * ks + 4 * t;
     ch[0] = base; ch[1] = base + 1; ch[2] = base + 2; ch[3] = base + 3;
+  }
+}
+
+// Query values of quad thread t at the channels key_channels gives for every
+// k-step, as fp32, from a 16-bit (bf16 / fp16) query row starting at element
+// qo; zeros when !live.  A 16-byte aligned row is read with one 16-byte load
+// per 32-channel block (4-bit keys: k-steps 2p, 2p + 1 take channels 32 p +
+// 8 t + 0..7) or one 8-byte load per k-step (channels 16 ks + 4 t + 0..3);
+// any other row element by element.
+template <int D, int KB>
+__device__ __forceinline__ void load_query_channels(const void* q, size_t qo, int io_dtype, int t, bool live,
+                                                    float (&x)[D / 16][4]) {
+  constexpr int KS = D / 16;
+  const uint16_t* row = static_cast<const uint16_t*>(q) + qo;
+  const bool bf = io_dtype == KVQ_DTYPE_BF16;
+  auto f = [bf](uint32_t h16) {
+    return bf ? __uint_as_float(h16 << 16) : __half2float(__ushort_as_half((unsigned short)h16));
+  };
+  if (!live) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) x[ks][0] = x[ks][1] = x[ks][2] = x[ks][3] = 0.0f;
+  } else if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    if constexpr (KB == 4) {
+#pragma unroll
+      for (int p = 0; p < KS / 2; ++p) {
+        const uint4 w = *reinterpret_cast<const uint4*>(row + 32 * p + 8 * t);
+        const float c0 = f(w.x & 0xffffu), c1 = f(w.x >> 16), c2 = f(w.y & 0xffffu), c3 = f(w.y >> 16);
+        const float c4 = f(w.z & 0xffffu), c5 = f(w.z >> 16), c6 = f(w.w & 0xffffu), c7 = f(w.w >> 16);
+        x[2 * p][0] = c0; x[2 * p][1] = c4; x[2 * p][2] = c2; x[2 * p][3] = c6;
+        x[2 * p + 1][0] = c1; x[2 * p + 1][1] = c5; x[2 * p + 1][2] = c3; x[2 * p + 1][3] = c7;
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t);
+        x[ks][0] = f(w.x & 0xffffu); x[ks][1] = f(w.x >> 16); x[ks][2] = f(w.y & 0xffffu); x[ks][3] = f(w.y >> 16);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      int ch[4];
+      key_channels<KB>(ks, t, ch);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[ks][i] = load_io(q, qo + ch[i], io_dtype);
+    }
   }
 }
 

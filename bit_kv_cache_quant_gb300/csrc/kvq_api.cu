@@ -270,7 +270,10 @@ int decode_nsplit(const kvq_cache_s* c) {
 // kernel's shape: eight-warp CTAs when that grid fits in one wave (wide), with
 // the same splits; otherwise four-warp CTAs (kTcCtasPerSm per SM; eight-warp,
 // two per SM, over four heads per kv head) with as many splits as fill two
-// whole waves without starting a third.
+// whole waves without starting a third.  A one-wave grid of up to four heads
+// per kv head whose (b, kv head) units can each take at least two splits of
+// four tiles of the capacity at one CTA per SM runs sixteen-warp CTAs instead
+// (wide == 2): SMs / units splits (one fewer with a KIVI_BLOCK tail CTA).
 struct DecodePlan {
   int nsplit;
   int nsplit_tc;
@@ -283,6 +286,17 @@ DecodePlan decode_plan(const kvq_cache_s* c, int G) {
   const long long units = (long long)c->cfg.batch * c->cfg.n_kv_heads;
   p.wide = units * p.nsplit <= (G > 4 ? 1LL : 2LL) * c->sms;
   p.nsplit_tc = p.nsplit;
+  if (p.wide && G <= 4) {
+    int rows = c->cfg.capacity;
+    if (c->cfg.layout != KVQ_LAYOUT_LINEAR) rows = c->cfg.sink + c->cfg.window + (c->cfg.layout == KVQ_LAYOUT_COMPACT);
+    long long ns = c->sms / units - (c->cfg.k_format == KVQ_FMT_KIVI_BLOCK ? 1 : 0);
+    if (ns > rows / (4 * kvq::kTmaRows)) ns = rows / (4 * kvq::kTmaRows);
+    if (ns > kvq::kMaxSplits) ns = kvq::kMaxSplits;
+    if (ns >= 2) {
+      p.wide = 2;
+      p.nsplit_tc = (int)ns;
+    }
+  }
   if (!p.wide) {
     const long long slots = (long long)kvq::kTcWaves * (G > 4 ? 2 : kvq::kTcCtasPerSm) * c->sms;
     int rows = c->cfg.capacity;

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -130,6 +132,23 @@ __device__ __forceinline__ int q40_code(float x, float d) {
   return (int)q + 8;
 }
 
+// Runs fn (a cudaError_t() callable that must be idempotent) unless it has
+// already succeeded for the current device at this call site; `done` holds one
+// bit per device ordinal below 64 (higher ordinals run fn every time).  A
+// function attribute set with cudaFuncSetAttribute applies to the current
+// device only, hence per device.  Concurrent first calls may both run fn.
+template <typename F>
+cudaError_t once_per_device(std::atomic<unsigned long long>& done, F fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // Counts kernels enqueued by the current API call (host side, per thread).
 void note_launch(int n = 1);
 
@@ -153,8 +172,9 @@ struct DecodeArgs {
   float* partials;   // [B*Hkv][nsplit][G][D + kPartialPad] or null when nsplit == 1
   int nsplit;        // splits per (b, kv head): the CUDA-core kernel's grid x extent
   int nsplit_tc;     // the same for the tensor-core kernel
-  int wide;          // tensor-core kernel: two tile groups of warps per CTA (the grid fits in
-                     // one wave at the CTAs per SM of that shape) instead of one
+  int wide;          // tensor-core kernel: 1 = two tile groups of warps per CTA (the grid fits
+                     // in one wave at the CTAs per SM of that shape) instead of one; 2 = four
+                     // tile groups, one CTA per SM
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
 // an (D, G) outside the instantiated set.

@@ -257,11 +257,15 @@ size_t kvq_decode_workspace_bytes(kvq_cache cache, int32_t n_q_heads);
    at most 128); the CUDA-core kernel (fp32 io, head_dim 32) uses it.
    *nsplit_tc: the tensor-core kernel's splits; *wide: 1 when that grid runs
    eight-warp CTAs in a single wave (two per SM, one for over four query heads
-   per kv head) with *nsplit_tc == *nsplit, 0 when it runs smaller CTAs (four
-   warps, four per SM; eight warps, two per SM, for over four query heads per
-   kv head) over as many splits as fill two whole waves without starting a
-   third.  The kernels spread the rows actually stored over at most that many
-   splits.  Configuration errors as kvq_cache_layout_query; a bad n_q_heads or
+   per kv head) with *nsplit_tc == *nsplit; 2 when that single wave instead
+   runs one sixteen-warp CTA per SM, *nsplit_tc = SMs / (B * Hkv) splits (one
+   fewer for KIVI_BLOCK keys, whose tail takes one more CTA), chosen for up
+   to four query heads per kv head when every split keeps at least four
+   64-row tiles of the capacity and there are at least two; 0 when it runs
+   smaller CTAs (four warps, four per SM; eight warps, two per SM, for over
+   four query heads per kv head) over as many splits as fill two whole waves
+   without starting a third.  The kernels spread the rows actually stored
+   over at most that many splits.  Configuration errors as kvq_cache_layout_query; a bad n_q_heads or
    sms, or a null output, is INVALID_ARG. */
 kvq_status kvq_decode_plan_query(const kvq_config* cfg, int32_t n_q_heads, int32_t sms, int32_t* nsplit,
                                  int32_t* nsplit_tc, int32_t* wide);

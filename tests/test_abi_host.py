@@ -224,9 +224,11 @@ def test_readme_c_example_compiles_and_links(kvq, tmp_path):
 
 
 # GB300: 152 SMs.  Tensor-core decode: eight-warp CTAs, two per SM (one with
-# over four query heads per kv head), when the grid fits one wave; otherwise
-# four-warp CTAs, four per SM (eight-warp, two per SM, over four heads), over
-# two whole waves.  At most 128 splits per (b, kv head).
+# over four query heads per kv head), when the grid fits one wave, or one
+# sixteen-warp CTA per SM (wide 2) when up to four heads per kv head leave
+# every (b, kv head) at least two splits of four tiles; otherwise four-warp
+# CTAs, four per SM (eight-warp, two per SM, over four heads), over two whole
+# waves.  At most 128 splits per (b, kv head).
 SMS = 152
 
 
@@ -235,8 +237,18 @@ def _plan(kvq, n_q_heads, sms=SMS, **cfg):
 
 
 def test_decode_plan_of_the_workloads(kvq):
-    # 8K mlx layer (B1, 8 kv heads, G 3): 32 splits of 256 rows, 256 eight-warp CTAs in one wave
-    assert _plan(kvq, 24, batch=1, n_kv_heads=8, capacity=8192 + 64) == (32, 32, 1)
+    # 8K mlx layer (B1, 8 kv heads, G 3): 19 splits, 152 sixteen-warp CTAs, one per SM
+    assert _plan(kvq, 24, batch=1, n_kv_heads=8, capacity=8192 + 64) == (32, 19, 2)
+    # the same layer with a KIVI residual buffer: one split fewer for the tail CTA (160 - 8 = 152 CTAs)
+    assert _plan(kvq, 24, batch=1, n_kv_heads=8, capacity=8192 + 128, k_format="kivi_block", k_bits=4,
+                 k_group=128, v_group=32) == (32, 18, 2)
+    # over four heads per kv head: eight-warp CTAs over two head groups, one per SM, in two waves
+    assert _plan(kvq, 48, batch=1, n_kv_heads=8, capacity=8192 + 64)[2] == 0
+    # SnapKV's kept cache (768 rows): three splits of four tiles, sixteen-warp CTAs
+    assert _plan(kvq, 24, batch=1, n_kv_heads=8, capacity=768, k_format="fp16", k_bits=16, k_group=0,
+                 v_format="fp16", v_bits=16, v_group=0) == (12, 3, 2)
+    # a 300-row cache has no two splits of four tiles: eight-warp CTAs, four splits
+    assert _plan(kvq, 24, batch=2, n_kv_heads=4, capacity=300) == (4, 4, 1)
     # 32K Q4_0 layer (B8, 8 kv heads, G 4): 19 splits, 1216 four-warp CTAs = two whole waves of 4 per SM
     ns, ntc, wide = _plan(kvq, 32, batch=8, n_kv_heads=8, capacity=32768 + 64, k_format="q4_0", k_group=32,
                           v_bits=8, v_group=128)
@@ -261,7 +273,10 @@ def test_decode_plan_invariants(kvq, sms):
         for n in (ns, ntc):
             assert 1 <= n <= 128
             assert n == 1 or cap // n >= min_rows
-        if wide:
+        if wide == 2:
+            assert G <= 4 and 2 <= ntc <= sms // units and cap // ntc >= 256
+            assert units * ns <= 2 * sms
+        elif wide:
             assert ntc == ns and units * ns <= (1 if G > 4 else 2) * sms
         else:
             assert units * ntc <= 2 * (2 if G > 4 else 4) * sms or ntc == 1   # never a third wave

@@ -137,13 +137,15 @@ def test_repeated_calls_are_identical(kvq):
 
 # The tensor-core decode picks its launch shape from the number of (batch row,
 # kv head) pairs and the cache length.  On a 152-SM GB300 these cases land on
-# each shape: eight-warp CTAs with a global split merge (the grid fits one
-# wave at two CTAs per SM), with one or many splits; four-warp CTAs (larger
-# grids).  Over four query heads per kv head (G = 8 here) every CTA carries a
-# second head group of warps over the same tiles, and the one-wave shape
-# holds one CTA per SM.  Whatever the shape, the result must match the oracle.
+# each shape: one sixteen-warp CTA per SM (few pairs, long caches: 19 or 9
+# splits per pair); eight-warp CTAs, two per SM, when the grid fits one wave
+# otherwise, with one or many splits; four-warp CTAs (larger grids).  Over
+# four query heads per kv head (G = 8 here) every CTA carries a second head
+# group of warps over the same tiles, and the one-wave shape holds one CTA
+# per SM.  Whatever the shape, the result must match the oracle.
 LAUNCH_SHAPES = [
-    ("eight_warps_32_splits", 1, 8, 8192 + 37, None),
+    ("sixteen_warps_19_splits", 1, 8, 8192 + 37, None),
+    ("sixteen_warps_9_splits", 1, 16, 3000, None),
     ("eight_warps_4_splits", 2, 4, 300, None),
     ("eight_warps_2_splits", 13, 8, 150, 150),
     ("four_warps", 16, 8, 2000, None),
