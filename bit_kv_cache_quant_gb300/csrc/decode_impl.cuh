@@ -221,9 +221,13 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     }
   }
   __syncthreads();
+  // Consecutive threads read consecutive accumulator words (no bank
+  // conflicts): with ACCPAD > 0 word p of a row holds channel
+  // (p % 8) * (D / 8) + p / 8.
   for (int idx = threadIdx.x; idx < G * D; idx += NTHR) {
-    const int h = idx / D, d = idx % D;
-    const int pos = h * AROW + (ACCPAD ? (d % (D / 8)) * 8 + d / (D / 8) : d);
+    const int h = idx / D, p = idx % D;
+    const int d = ACCPAD ? (p % 8) * (D / 8) + p / 8 : p;
+    const int pos = h * AROW + p;
     const float M = sm_hm[h], L = sm_hl[h];
     float A = 0.0f;
 #pragma unroll

@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   __shared__ float sm_m[NWARP][G];
   __shared__ float sm_l[NWARP][G];
   __shared__ __align__(8) uint64_t mbar[NSTAGE];
+  __shared__ __align__(8) uint64_t mbar_meta;   // metadata of the initial ring (one use)
+  __shared__ int s_ninit;                       // tiles of the initial ring
   __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (TW per tile)
   __shared__ int s_last_tile[NSTAGE];     // last tile copied into a stage, -1 if none
   __shared__ int s_T;
@@ -231,7 +233,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const size_t bh = (size_t)b * c.Hkv + kvh;
   const int kng = c.k.n_groups;
   const int vng = c.v.n_groups;
-  const TileLayout TL = tc_layout<D, KF, VF>(kng, vng);
+  // plane-major ring for the one-wave shapes, stage-major for four-warp CTAs
+  using Ring = TcRing<D, KF, VF, NSTAGE, (NGRP > 1)>;
+  static_assert(Ring::bytes <= NSTAGE * TcStages<D, G, KF, VF, NGRP>::stage, "the ring fits its stages");
+  const Ring R(kng, vng);
 
   // Before the grids this launch depends on have finished (programmatic
   // dependent launch), touch only what they cannot change: the tensor maps
@@ -272,6 +277,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       for (int off = 0; off < G * D * es; off += 128) prefetch_l2(q0 + off);
     }
     s_fail = 0;
+    s_ninit = 0;
+    mbar_init(&mbar_meta, 1);
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&mbar[s], 1);
@@ -291,9 +298,10 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const int grp = (warp >> 2) / HG;
   const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
   // Warp 0 reads the stored length and requests the whole initial ring of
-  // tiles, lane s the tile of stage s (one thread issuing the whole ring
-  // serialises the requests), while the other warps build their query
-  // fragments.
+  // tiles: lane s the code planes of stage s, lane NSTAGE the metadata of
+  // all of them (one copy per plane; every copy request costs the issuing
+  // SM's copy engine time, so a ring of many small copies arrives late),
+  // while the other warps build their query fragments.
   // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
   // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
   // columns and q enters exactly.  Thread (g, t) builds column g at the key
@@ -309,11 +317,24 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     int a0, a1, ns0;
     split_rows(T0, a.nsplit, split, a0, a1, ns0);
     if (split < ns0) {
-      const int nt0 = (a1 - a0 + kTileTokens - 1) / kTileTokens;
-      if (lane < NSTAGE && lane < nt0) {
-        issue_tile_tma<D, KF, VF>(smem + lane * TL.bytes, TL, c, bh, a0 + lane * kTileTokens, &mbar[lane]);
+      const int nt0 = min((a1 - a0 + kTileTokens - 1) / kTileTokens, NSTAGE);
+      __syncwarp();   // lane 0's barrier initialisation is visible to the warp
+      if (lane < nt0) {
+        const int r0 = a0 + lane * kTileTokens;
+        if constexpr (NGRP > 1) {
+          mbar_expect_tx(&mbar[lane], (uint32_t)R.tx_codes);
+          issue_codes<D, KF, VF>(smem, R, lane, c, bh, r0, &mbar[lane]);
+        } else {
+          mbar_expect_tx(&mbar[lane], (uint32_t)(R.tx_codes + R.tx_meta));
+          issue_codes<D, KF, VF>(smem, R, lane, c, bh, r0, &mbar[lane]);
+          if (R.tx_meta > 0) issue_meta(smem, R, lane, 1, c, bh, r0, &mbar[lane]);
+        }
         s_last_tile[lane] = lane;
+      } else if (NGRP > 1 && lane == NSTAGE && R.tx_meta > 0) {
+        mbar_expect_tx(&mbar_meta, (uint32_t)(nt0 * R.tx_meta));
+        issue_meta(smem, R, 0, nt0, c, bh, a0, &mbar_meta);
       }
+      if (lane == 0) s_ninit = nt0;
     }
   }
   uint32_t qf[KS][2];
@@ -423,20 +444,32 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   int cur_blk = -1;
   float zt = 0.0f;
 
+  const int ninit = s_ninit;
+  // the plane-major initial ring's metadata has landed (seen by this warp)
+  bool meta_in = NGRP == 1 || R.tx_meta == 0;
   for (int it = grp; it < ntiles; it += NGRP) {
     const int stg = it % NSTAGE;
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar[stg], (it / NSTAGE) & 1))) {
       s_fail = 1;
       break;
     }
-    const uint8_t* st = smem + stg * TL.bytes;
+    if (it < ninit && !meta_in) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&mbar_meta, 0))) {
+        s_fail = 1;
+        break;
+      }
+      meta_in = true;
+    }
+    // this stage's planes; the metadata planes are indexed by ring row
+    const uint8_t* kst = smem + R.kc(stg);
+    const uint8_t* vst = smem + R.vc(stg);
     const int tok0 = t0 + it * kTileTokens + blk;
     if constexpr (K_KIVIB) {
       const int bk = (t0 + it * kTileTokens) / c.k.group;
       if (bk != cur_blk && tok0 < t1) {   // warp-uniform
         cur_blk = bk;
-        const __half* bs = reinterpret_cast<const __half*>(st + TL.kbs);
-        const __half* bz = reinterpret_cast<const __half*>(st + TL.kbz);
+        const __half* bs = reinterpret_cast<const __half*>(smem + R.kbs(stg));
+        const __half* bz = reinterpret_cast<const __half*>(smem + R.kbz(stg));
         const int hq = 4 * hg + (g >> 1);
         const float* qr = sm_qraw[hq < G ? hq : 0];
         const bool live = hq < G;
@@ -478,7 +511,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       float acc[NACC][4];
 #pragma unroll
       for (int i = 0; i < NACC; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-      const uint8_t* kpl = st + TL.kc;
+      const uint8_t* kpl = kst;
       if constexpr (KB == 4) {
 #pragma unroll
         for (int p = 0; p < NB; ++p) {
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         if constexpr (K_Q40) {
           // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
           float d[NB], x[NB];
-          load_halves<NB>(st + TL.ks + rk[e] * (2 * NB), d);
+          load_halves<NB>(smem + R.ks(stg) + rk[e] * (2 * NB), d);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][2 * e] + acc[nb][2 * e + 1];
           v = fmaf(d[1], x[1], d[0] * x[0]);
@@ -529,8 +562,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
           float x[NB];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) x[nb] = acc[nb][2 * e] + acc[nb][2 * e + 1];
-          const uint8_t* srow = st + TL.ks + rk[e] * (2 * kng);
-          const uint8_t* zrow = st + TL.kz + rk[e] * (2 * kng);
+          const uint8_t* srow = smem + R.ks(stg) + rk[e] * (2 * kng);
+          const uint8_t* zrow = smem + R.kz(stg) + rk[e] * (2 * kng);
           if (kng == NB) {
             float sg[NB], zg[NB];
             load_halves<NB>(srow, sg);
@@ -594,8 +627,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       for (int i = 0; i < 4; ++i) vok[i] = !MASK || tok0 - blk + rr[i] < t1;
       __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);
       if constexpr (V_AFF) {
-        const __half* vs = reinterpret_cast<const __half*>(st + TL.vs);
-        const __half* vz = reinterpret_cast<const __half*>(st + TL.vz);
+        const __half* vs = reinterpret_cast<const __half*>(smem + R.vs(stg));
+        const __half* vz = reinterpret_cast<const __half*>(smem + R.vz(stg));
         if (vfold) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -629,7 +662,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       // bytes per token.
       constexpr int NWT = VTB / 4;
       constexpr int NW = NWT > 4 ? 4 : NWT;
-      const uint8_t* vpl = st + TL.vc;
+      const uint8_t* vpl = vst;
 #pragma unroll
       for (int w0 = 0; w0 < NWT; w0 += NW) {
         // keep the next chunk's loads behind this one's MMAs (register pressure)
@@ -670,7 +703,9 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         const int nx = it + NSTAGE;
         if (nx < ntiles) {
           fence_async_smem();
-          issue_tile_tma<D, KF, VF>(smem + stg * TL.bytes, TL, c, bh, t0 + nx * kTileTokens, &mbar[stg]);
+          mbar_expect_tx(&mbar[stg], (uint32_t)(R.tx_codes + R.tx_meta));
+          issue_codes<D, KF, VF>(smem, R, stg, c, bh, t0 + nx * kTileTokens, &mbar[stg]);
+          if (R.tx_meta > 0) issue_meta(smem, R, stg, 1, c, bh, t0 + nx * kTileTokens, &mbar[stg]);
           s_last_tile[stg] = nx;
         }
       }
@@ -684,6 +719,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       set_status(c.state, KVQ_DEV_TIMEOUT);
       for (int s = 0; s < NSTAGE; ++s)
         if (s_last_tile[s] >= 0) mbar_wait_bounded(&mbar[s], (s_last_tile[s] / NSTAGE) & 1);
+      if (NGRP > 1 && s_ninit > 0 && R.tx_meta > 0) mbar_wait_bounded(&mbar_meta, 0);
     }
     return;
   }
@@ -792,16 +828,14 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
 
 template <int D, int G, int KF, int VF, int NGRP>
 cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
-  const TileLayout L = tc_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   using S = TcStages<D, G, KF, VF, NGRP>;
   using Shape = typename S::Shape;
   auto kern = decode_tc_kernel<D, G, KF, VF, NGRP>;
-  const int smem = S::dyn_bytes(L.bytes);
+  const int smem = S::dyn_bytes(S::stage);
   static_assert(S::dyn_bytes(S::stage) + S::static_smem <= 227 * 1024, "shared memory per CTA");
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = once_per_device(configured, [&]() {
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                S::dyn_bytes(tc_layout<D, KF, VF>(S::kng_max, S::vng_max).bytes));
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (e != cudaSuccess) return e;
   // Launched as a programmatic dependent of the previous kernel in the

@@ -189,50 +189,106 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// One thread: copies tile rows [row0, row0 + 64) of every plane into stage `st`.
-template <int D, int KF, int VF>
-__device__ __forceinline__ void issue_tile_tma(uint8_t* st, const TileLayout& L, const CacheView& c, size_t bh,
-                                               int row0, uint64_t* m) {
+// Shared-memory ring of NSTAGE tile stages, in one of two layouts.
+// Plane-major (PM): the K codes of stage s at kc + s * KCT and the V codes at
+// vc + s * VCT (tiles of 64 rows, each a multiple of 1024 bytes, where the
+// 128-byte swizzle pattern repeats), then each per-token metadata plane as one
+// array of NSTAGE * 64 ring rows of this cache's row size, so that the
+// metadata of a split's first tiles (consecutive rows in global memory) lands
+// with one copy per plane: one-wave grids, whose CTAs request a whole split at
+// once and wait on every copy request the SM's copy engine serves in turn.
+// Stage-major (!PM): stage s is one block of STAGE bytes holding its tile's
+// planes at fixed offsets: multi-wave grids of short rings, where plane bases
+// that are compile-time constants save instructions in the loop.  In both,
+// every region is sized for the largest group counts the kernel accepts (key
+// scale groups of 32 channels, value groups of D / 8), and KIVI_BLOCK keys
+// add the (scale, zero) rows of each stage's block.
+template <int D, int KF, int VF, int NSTAGE, bool PM>
+struct TcRing {
+  static constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
+  static constexpr bool K_Q40 = (KF == F_Q40);
+  static constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
+  static constexpr bool K_KIVIB = (KF == F_KIVIB8 || KF == F_KIVIB4);
+  static constexpr int KCT = kTileTokens * D * FmtBits<KF>::v / 8;
+  static constexpr int VCT = kTileTokens * D * FmtBits<VF>::v / 8;
+  static_assert(KCT % 1024 == 0 && VCT % 1024 == 0, "code tiles keep the swizzle alignment");
+  static constexpr int KMR_MAX = (K_AFF || K_Q40) ? 2 * (D / 32) : 0;   // metadata bytes per row, at most
+  static constexpr int VMR_MAX = V_AFF ? 2 * 8 : 0;
+  // one stage's planes at their largest (stage-major offsets)
+  static constexpr int S_KS = KCT + VCT;
+  static constexpr int S_KZ = S_KS + kTileTokens * KMR_MAX;
+  static constexpr int S_VS = S_KZ + (K_AFF ? kTileTokens * KMR_MAX : 0);
+  static constexpr int S_VZ = S_VS + kTileTokens * VMR_MAX;
+  static constexpr int S_KBS = S_VZ + kTileTokens * VMR_MAX;
+  static constexpr int S_KBZ = S_KBS + (K_KIVIB ? D * 2 : 0);
+  static constexpr int STAGE = (S_KBZ + (K_KIVIB ? D * 2 : 0) + 1023) / 1024 * 1024;
+  // plane-major region bases
+  static constexpr int P_VC = NSTAGE * KCT;
+  static constexpr int P_KS = P_VC + NSTAGE * VCT;
+  static constexpr int P_KZ = P_KS + NSTAGE * kTileTokens * KMR_MAX;
+  static constexpr int P_VS = P_KZ + (K_AFF ? NSTAGE * kTileTokens * KMR_MAX : 0);
+  static constexpr int P_VZ = P_VS + NSTAGE * kTileTokens * VMR_MAX;
+  static constexpr int P_KBS = P_VZ + NSTAGE * kTileTokens * VMR_MAX;
+  static constexpr int P_KBZ = P_KBS + (K_KIVIB ? NSTAGE * D * 2 : 0);
+  static constexpr int bytes = PM ? P_KBZ + (K_KIVIB ? NSTAGE * D * 2 : 0) : NSTAGE * STAGE;
+  int kmr, vmr;     // this cache's metadata bytes per row of the key and value planes
+  int tx_codes;     // bytes one tile's code planes (and block rows) bring
+  int tx_meta;      // bytes one tile's metadata planes bring
+
+  __host__ __device__ __forceinline__ TcRing(int kng, int vng) {
+    kmr = (K_AFF || K_Q40) ? 2 * kng : 0;
+    vmr = V_AFF ? 2 * vng : 0;
+    tx_codes = KCT + VCT + (K_KIVIB ? 2 * D * 2 : 0);
+    tx_meta = kTileTokens * ((K_AFF ? 2 : 1) * kmr + 2 * vmr);
+  }
+  // byte offsets of stage s's planes; row r of a metadata plane follows at
+  // r times the plane's row size
+  __device__ __forceinline__ int kc(int s) const { return PM ? s * KCT : s * STAGE; }
+  __device__ __forceinline__ int vc(int s) const { return PM ? P_VC + s * VCT : s * STAGE + KCT; }
+  __device__ __forceinline__ int ks(int s) const { return PM ? P_KS + s * kTileTokens * kmr : s * STAGE + S_KS; }
+  __device__ __forceinline__ int kz(int s) const { return PM ? P_KZ + s * kTileTokens * kmr : s * STAGE + S_KZ; }
+  __device__ __forceinline__ int vs(int s) const { return PM ? P_VS + s * kTileTokens * vmr : s * STAGE + S_VS; }
+  __device__ __forceinline__ int vz(int s) const { return PM ? P_VZ + s * kTileTokens * vmr : s * STAGE + S_VZ; }
+  __device__ __forceinline__ int kbs(int s) const { return PM ? P_KBS + s * D * 2 : s * STAGE + S_KBS; }
+  __device__ __forceinline__ int kbz(int s) const { return PM ? P_KBZ + s * D * 2 : s * STAGE + S_KBZ; }
+};
+
+// One thread: the code planes (and KIVI_BLOCK block rows) of tile rows
+// [row0, row0 + 64) into stage s, completing on m (whose expected bytes the
+// caller has armed).
+template <int D, int KF, int VF, class Ring>
+__device__ __forceinline__ void issue_codes(uint8_t* smem, const Ring& R, int s, const CacheView& c, size_t bh,
+                                            int row0, uint64_t* m) {
   constexpr int KROW = D * FmtBits<KF>::v / 8;
   constexpr int VROW = D * FmtBits<VF>::v / 8;
-  constexpr bool K_AFF = (KF == F_AFF8 || KF == F_AFF4);
-  constexpr bool K_Q40 = (KF == F_Q40);
-  constexpr bool V_AFF = (VF == F_AFF8 || VF == F_AFF4);
   const size_t row = bh * c.cap_alloc + row0;
-  mbar_expect_tx(m, (uint32_t)L.tx);
-  tma_rows<KROW>(st + L.kc, &c.kmap, (int)row, m);
-  tma_rows<VROW>(st + L.vc, &c.vmap, (int)row, m);
-  if constexpr (K_AFF || K_Q40) {
-    const uint32_t mb = c.k.n_groups * 2;
-    bulk_copy(st + L.ks, reinterpret_cast<const uint8_t*>(c.k.tok_scale) + row * mb, kTileTokens * mb, m);
-    if constexpr (K_AFF)
-      bulk_copy(st + L.kz, reinterpret_cast<const uint8_t*>(c.k.tok_zero) + row * mb, kTileTokens * mb, m);
-  }
-  if constexpr (V_AFF) {
-    const uint32_t mb = c.v.n_groups * 2;
-    bulk_copy(st + L.vs, reinterpret_cast<const uint8_t*>(c.v.tok_scale) + row * mb, kTileTokens * mb, m);
-    bulk_copy(st + L.vz, reinterpret_cast<const uint8_t*>(c.v.tok_zero) + row * mb, kTileTokens * mb, m);
-  }
+  tma_rows<KROW>(smem + R.kc(s), &c.kmap, (int)row, m);
+  tma_rows<VROW>(smem + R.vc(s), &c.vmap, (int)row, m);
   if constexpr (KF == F_KIVIB8 || KF == F_KIVIB4) {
     // the per-channel scale and zero of the tile's block (a tile never spans two)
     const size_t mr = (bh * (c.cap_alloc / c.k.group) + row0 / c.k.group) * D;
-    bulk_copy(st + L.kbs, c.k.blk_scale + mr, D * 2, m);
-    bulk_copy(st + L.kbz, c.k.blk_zero + mr, D * 2, m);
+    bulk_copy(smem + R.kbs(s), c.k.blk_scale + mr, D * 2, m);
+    bulk_copy(smem + R.kbz(s), c.k.blk_zero + mr, D * 2, m);
   }
 }
 
-// Stage layout: the planes placed for the largest group counts the kernel
-// accepts (key scale groups of 32 channels, value groups of D / 8), so that
-// every offset and the stage size are compile-time constants, with every
-// stage a multiple of 1024 bytes (the 128-byte swizzle pattern repeats every
-// 1024 bytes and needs its destination aligned to it); tx is what one tile of
-// this cache actually copies.
-template <int D, int KF, int VF>
-__host__ __device__ __forceinline__ TileLayout tc_layout(int kng, int vng) {
-  TileLayout L = tile_layout<D, KF, VF>(D / 32, 8);
-  L.bytes = (L.bytes + 1023) / 1024 * 1024;
-  L.tx = tile_layout<D, KF, VF>(kng, vng).bytes;
-  return L;
+// One thread: the per-token metadata of nt consecutive tiles from row0 on
+// into stages s0 .. s0 + nt - 1, completing on m: one copy per plane (nt > 1
+// only in the plane-major layout, where those stages' rows are contiguous).
+template <class Ring>
+__device__ __forceinline__ void issue_meta(uint8_t* smem, const Ring& R, int s0, int nt, const CacheView& c,
+                                           size_t bh, int row0, uint64_t* m) {
+  const size_t row = bh * c.cap_alloc + row0;
+  const uint32_t rows = (uint32_t)(nt * kTileTokens);
+  if constexpr (Ring::K_AFF || Ring::K_Q40) {
+    bulk_copy(smem + R.ks(s0), reinterpret_cast<const uint8_t*>(c.k.tok_scale) + row * R.kmr, rows * R.kmr, m);
+    if constexpr (Ring::K_AFF)
+      bulk_copy(smem + R.kz(s0), reinterpret_cast<const uint8_t*>(c.k.tok_zero) + row * R.kmr, rows * R.kmr, m);
+  }
+  if constexpr (Ring::V_AFF) {
+    bulk_copy(smem + R.vs(s0), reinterpret_cast<const uint8_t*>(c.v.tok_scale) + row * R.vmr, rows * R.vmr, m);
+    bulk_copy(smem + R.vz(s0), reinterpret_cast<const uint8_t*>(c.v.tok_zero) + row * R.vmr, rows * R.vmr, m);
+  }
 }
 
 // 2^x with the hardware's approximate base-2 exponential (ex2.approx.ftz: a
