@@ -50,6 +50,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (profiling small footprints; not a bench line)")
+    p.add_argument("--separate-step", action="store_true",
+                   help="run each layer's append, eviction and decode as separate launches even where the "
+                        "library fuses them (kvq_append_decode), to compare the two")
     p.add_argument("--no-per-config", action="store_true",
                    help="skip the other workloads' summary that a one-GPU run of the default workload adds")
     a = p.parse_args(argv)
@@ -122,12 +125,25 @@ def stored_after(w, t_seen):
 
 # ------------------------------------------------------ decode workloads --
 
+def fused_step(kvq, w, cfg, sms):
+    """Whether kvq_append_decode runs this workload's decode step (append, eviction, attention) as
+    one launch per layer: LINEAR and RING caches on the tensor-core decode with head_dim 128 (16-bit
+    io), not KIVI_BLOCK keys, whose decode grid is one wave (the plan's `wide` >= 1).  Otherwise the
+    step runs as separate launches, and the bench groups every layer's append before every layer's
+    decode."""
+    if not (w.layout in ("linear", "ring") and w.k_format != "kivi_block" and w.io_dtype != "float32"
+            and w.head_dim == 128):
+        return False
+    return kvq.kvq_decode_plan_query(cfg, w.n_q_heads, sms)[2] >= 1
+
+
 class DecodeStep:
     """All layers of one workload: caches filled to the context, per-layer step
-    inputs and outputs resident in HBM, and two captured CUDA graphs (every
-    layer's append + eviction, then every layer's decode attention)."""
+    inputs and outputs resident in HBM, and captured CUDA graphs: one launch
+    per layer (kvq_append_decode) where the library fuses the step, else every
+    layer's append + eviction, then every layer's decode attention."""
 
-    def __init__(self, kvq, w, extra_rows, device):
+    def __init__(self, kvq, w, extra_rows, device, separate=False):
         self.kvq, self.w, self.device = kvq, w, device
         dt = synth.torch_dtype(w.io_dtype)
         if w.layout == "linear":
@@ -164,8 +180,22 @@ class DecodeStep:
             self.out.append(self.outbuf[layer * B * Hq * D: (layer + 1) * B * Hq * D].view(B, Hq, D))
         for c in self.caches:                      # workspaces allocated before capture
             c.workspace(Hq)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.fused = not separate and fused_step(kvq, w, self.caches[0].cfg, sms)
         self.launches_append = 0
         self.launches_decode = 0
+
+    def eager_step(self):
+        """One step through the public API; returns the library's launch count."""
+        if not self.fused:
+            return self.eager_append() + self.eager_decode()
+        n = 0
+        for layer, c in enumerate(self.caches):
+            c.launches = 0
+            c.append_decode(self.k1[layer], self.v1[layer], self.q[layer], out=self.out[layer])
+            n += c.launches
+        self.t_seen += 1
+        return n
 
     def eager_append(self):
         n = 0
@@ -188,6 +218,15 @@ class DecodeStep:
 
     def capture(self):
         # one eager pass first: every kernel is loaded before capture
+        if self.fused:
+            self.eager_step()
+            torch.cuda.synchronize()
+            self.g_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_step):
+                self.launches_decode = self.eager_step()
+            self.t_seen -= 1      # capture records the launches without running them
+            torch.cuda.synchronize()
+            return
         self.eager_append()
         self.eager_decode()
         torch.cuda.synchronize()
@@ -201,15 +240,33 @@ class DecodeStep:
         torch.cuda.synchronize()
 
     def replay(self):
-        self.g_append.replay()
-        self.g_decode.replay()
+        if self.fused:
+            self.g_step.replay()
+        else:
+            self.g_append.replay()
+            self.g_decode.replay()
+        self.t_seen += 1
+
+    def replay_timed(self, e0, e1, e2):
+        """One step with events before, between (appends | decodes) and after; a fused step records
+        its one graph between e0 and e2 (e1 right after e0)."""
+        e0.record()
+        if self.fused:
+            e1.record()
+            self.g_step.replay()
+        else:
+            self.g_append.replay()
+            e1.record()
+            self.g_decode.replay()
+        e2.record()
         self.t_seen += 1
 
     def stored(self):
         return stored_after(self.w, self.t_seen)
 
     def step_bytes(self):
-        """(append + eviction + attention bytes of the next step, attention bytes per layer)."""
+        """(append + eviction + attention bytes of the next step, bytes per launch of the step's
+        dominant kernel: the fused append + decode, else the decode attention)."""
         w = self.w
         T = stored_after(w, self.t_seen + 1)
         dec = decode_bytes(w, T)
@@ -219,7 +276,7 @@ class DecodeStep:
             ev = 2 * w.batch * w.n_kv_heads * w.window * (
                 side_token_bytes(w.k_format, w.k_bits, w.k_group, w.head_dim)
                 + side_token_bytes(w.v_format, w.v_bits, w.v_group, w.head_dim))
-        return w.layers * (dec + app + ev), dec
+        return w.layers * (dec + app + ev), dec + (app if self.fused else 0)
 
 
 # ----------------------------------------------------------------- clocks --
@@ -315,12 +372,7 @@ def timed_decode(ds, steps, warmup, world):
         total_bytes += b
         dec_bytes.append(d)
         flush.zero_()
-        ev[i][0].record()
-        ds.g_append.replay()
-        ev[i][1].record()
-        ds.g_decode.replay()
-        ev[i][2].record()
-        ds.t_seen += 1
+        ds.replay_timed(*ev[i])
     torch.cuda.synchronize()
     barrier(world)
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
@@ -335,8 +387,7 @@ def e2e_decode(ds, steps, world):
     host_out = torch.empty(ds.outbuf.shape, dtype=ds.outbuf.dtype, pin_memory=True)
     for _ in range(2):
         ds.stage.copy_(host_in, non_blocking=True)
-        ds.eager_append()
-        ds.eager_decode()
+        ds.eager_step()
         host_out.copy_(ds.outbuf, non_blocking=True)
         torch.cuda.synchronize()
     total = 0
@@ -346,8 +397,7 @@ def e2e_decode(ds, steps, world):
     for _ in range(steps):
         total += ds.step_bytes()[0]
         ds.stage.copy_(host_in, non_blocking=True)
-        ds.eager_append()
-        ds.eager_decode()
+        ds.eager_step()
         host_out.copy_(ds.outbuf, non_blocking=True)
         torch.cuda.synchronize()
     t1 = time.perf_counter()
@@ -495,7 +545,7 @@ def run_reference(a, rank, world):
     print(json.dumps(line))
 
 
-DECODE_SOURCES = ("kvq_internal.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh")
+DECODE_SOURCES = ("kvq_internal.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh", "quantize_row.cuh")
 
 
 def decode_source_sha(kvq_dir):
@@ -533,7 +583,7 @@ def decode_traffic(w, kvq_dir):
 def bench_decode(a, kvq, w, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
     extra = 2 * (a.steps + a.warmup) + 64
-    ds = DecodeStep(kvq, w, extra, device)
+    ds = DecodeStep(kvq, w, extra, device, separate=a.separate_step)
     ds.capture()
     clocks = ClockSampler()
     clocks.start()
@@ -555,7 +605,9 @@ def bench_decode(a, kvq, w, rank, world):
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
                    "k_format": f"{w.k_format}{w.k_bits}" + (f"g{w.k_group}" if w.k_group else ""),
                    "v_format": f"{w.v_format}{w.v_bits}" + (f"g{w.v_group}" if w.v_group else ""),
-                   "layout": w.layout, "step": "per layer: append 1 token, evict, decode attention",
+                   "layout": w.layout,
+                   "step": ("per layer: append 1 token, evict, decode attention"
+                            + (" (one fused launch per layer)" if ds.fused else " (separate launches)")),
                    "l2": "flushed (256 MiB write) between timed steps, outside the events",
                    "parallelism": f"replicas x{world}"},
         "decode_steps_per_s": world * a.steps / t_max,
@@ -600,9 +652,10 @@ def snapkv_episode_bytes(w, batch, n_kv_heads):
 class SnapKVEpisode:
     """SnapKV prefill eviction and the decode that follows, on the device: the
     prompt's K/V in an fp16 cache, observation-window scoring + top-k, keep-set
-    gather into the cache, then `decode_steps` single-token appends and decode
-    attentions.  The episode (everything after the prompt fill) is one CUDA
-    graph; each replay starts from a freshly filled cache."""
+    gather into the cache, then `decode_steps` decode steps (each one launch:
+    the single-token append and the attention over the cache including it).
+    The episode (everything after the prompt fill) is one CUDA graph; each
+    replay starts from a freshly filled cache."""
 
     def __init__(self, kvq, w, device):
         self.kvq, self.w = kvq, w
@@ -643,8 +696,8 @@ class SnapKVEpisode:
         c.launches = 0
         c.evict_keepset(self.idx)
         for t in range(w.decode_steps):
-            c.append(self.k1[t], self.v1[t])
-            c.decode_attn(self.q[t], out=self.out[t])
+            # one launch: the token is coded into the fp16 cache and attended over
+            c.append_decode(self.k1[t], self.v1[t], self.q[t], out=self.out[t])
         return n + c.launches
 
     def capture(self):

@@ -8,7 +8,7 @@
 // mean-centering for Q4_0": subtract the per-(kv head, channel) bias, then
 // code symmetric blocks (32 channels, one fp16 scale: the Q4_0 layout, which
 // the page does not spell out).
-#include "kvq_internal.cuh"
+#include "quantize_row.cuh"
 
 namespace kvq {
 
@@ -143,121 +143,6 @@ __global__ void __launch_bounds__(256) recompute_kivi_kernel(CacheView c, const 
   if (blockIdx.x == 0 && tid == 0) c.state->k_calibrated = 1;
 }
 
-// ---------------------------------------------------------------------------
-// Row quantiser: one warp codes one token row of D = 32 * E channels; lane l
-// holds channels [l*E, l*E + E).
-
-template <int E>
-__device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[E]) {
-  if constexpr (E == 1) {
-    dst[0] = b[0];
-  } else if constexpr (E == 2) {
-    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(b[0] | (b[1] << 8));
-  } else {
-#pragma unroll
-    for (int i = 0; i < E; i += 4) {
-      *reinterpret_cast<uint32_t*>(dst + i) = (uint32_t)b[i] | ((uint32_t)b[i + 1] << 8) |
-                                              ((uint32_t)b[i + 2] << 16) | ((uint32_t)b[i + 3] << 24);
-    }
-  }
-}
-
-// Writes the lane's E codes u (0..levels) in the side's storage encoding.
-template <int E>
-__device__ __forceinline__ void store_codes(uint8_t* row, int lane, int bits, const int (&u)[E]) {
-  if (bits == 8) {
-    uint8_t b[E];
-#pragma unroll
-    for (int i = 0; i < E; ++i) b[i] = (uint8_t)(u[i] ^ 0x80);   // signed level q = u - 128
-    store_bytes<E>(row + lane * E, b);
-  } else {  // 4-bit: channel 2j in the low nibble of byte j
-    if constexpr (E == 1) {
-      const int nb = __shfl_down_sync(0xffffffffu, u[0], 1);
-      if ((lane & 1) == 0) row[lane >> 1] = (uint8_t)(u[0] | (nb << 4));
-    } else {
-      uint8_t b[E / 2];
-#pragma unroll
-      for (int i = 0; i < E / 2; ++i) b[i] = (uint8_t)(u[2 * i] | (u[2 * i + 1] << 4));
-      store_bytes<E / 2>(row + lane * (E / 2), b);
-    }
-  }
-}
-
-// Max / min over the `width` lanes (a power of two) of the lane's group.
-__device__ __forceinline__ float group_max(float x, int width) {
-  for (int o = 1; o < width; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ float group_min(float x, int width) {
-  for (int o = 1; o < width; o <<= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-
-// Codes lane `lane`'s E channels x (already loaded as fp32) of one row.
-template <int E>
-__device__ __forceinline__ void quantize_row(const SideView& s, const float* __restrict__ bias, float (&x)[E],
-                                             size_t bh, int cap_alloc, int slot, int lane) {
-  uint8_t* row = s.codes + ((size_t)bh * cap_alloc + slot) * s.row_bytes;
-  const size_t meta_row = ((size_t)bh * cap_alloc + slot) * s.n_groups;
-
-  if (s.fmt == KVQ_FMT_FP16) {
-    __half* dst = reinterpret_cast<__half*>(row) + lane * E;
-#pragma unroll
-    for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(x[i]);
-    return;
-  }
-
-  const float levels = (s.bits == 8) ? 255.0f : 15.0f;
-  int u[E];
-
-  if (s.fmt == KVQ_FMT_KIVI_CHAN) {
-    const float* sc = s.ch_scale32 + bh * (32 * E) + lane * E;
-    const float* zr = s.ch_zero32 + bh * (32 * E) + lane * E;
-#pragma unroll
-    for (int i = 0; i < E; ++i) u[i] = affine_code(x[i], sc[i], zr[i], levels);
-    store_codes<E>(row, lane, s.bits, u);
-    return;
-  }
-
-  if (s.fmt == KVQ_FMT_AFFINE_TOKEN) {
-    const int width = s.group / E;           // lanes per group
-    float mn = x[0], mx = x[0];
-#pragma unroll
-    for (int i = 1; i < E; ++i) {
-      mn = fminf(mn, x[i]);
-      mx = fmaxf(mx, x[i]);
-    }
-    mn = group_min(mn, width);
-    mx = group_max(mx, width);
-    const float sc = affine_scale(mn, mx, levels);
-#pragma unroll
-    for (int i = 0; i < E; ++i) u[i] = affine_code(x[i], sc, mn, levels);
-    store_codes<E>(row, lane, s.bits, u);
-    if (lane % width == 0) {
-      const int g = lane / width;
-      s.tok_scale[meta_row + g] = __float2half_rn(sc);
-      s.tok_zero[meta_row + g] = __float2half_rn(mn);
-    }
-    return;
-  }
-
-  // KVQ_FMT_Q4_0: optional centering, then symmetric 32-channel blocks.
-  if (bias != nullptr) {
-#pragma unroll
-    for (int i = 0; i < E; ++i) x[i] = __fsub_rn(x[i], bias[lane * E + i]);
-  }
-  const int width = 32 / E;
-  float a = fabsf(x[0]);
-#pragma unroll
-  for (int i = 1; i < E; ++i) a = fmaxf(a, fabsf(x[i]));
-  a = group_max(a, width);
-  const float d = __fdiv_rn(a, 7.0f);
-#pragma unroll
-  for (int i = 0; i < E; ++i) u[i] = q40_code(x[i], d);
-  store_codes<E>(row, lane, 4, u);
-  if (lane % width == 0) s.tok_scale[meta_row + lane / width] = __float2half_rn(d);
-}
-
 // One warp per (b, kv head, token) row of the append; 8 warps per CTA.  The
 // input rows are requested before the counters are read (they do not depend
 // on them).  With more than one CTA the last to arrive advances the counters,
@@ -274,6 +159,10 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kAppendWarps + warp;
+  // launched as a programmatic dependent: the inputs and counters may come
+  // from the previous kernel; the next launch may start its prologue now
+  grid_dependency_wait();
+  grid_launch_dependents();
   float xk[E], xv[E];
   if (row < rows) {
     // token row % n of (b, kv head) row / n sits at row (row / n) * hstride + row % n of the input
@@ -498,14 +387,24 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
   }
   const long long rows = (long long)c.B * c.Hkv * n;
   const unsigned grid = (unsigned)((rows + kAppendWarps - 1) / kAppendWarps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(32 * kAppendWarps);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   switch (c.D) {
-    case 32: append_kernel<T, 1><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
-    case 64: append_kernel<T, 2><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
-    case 128: append_kernel<T, 4><<<grid, 32 * kAppendWarps, 0, st>>>(c, kk, vv, n, rows, hstride); break;
+    case 32: e = cudaLaunchKernelEx(&cfg, append_kernel<T, 1>, c, kk, vv, n, rows, hstride); break;
+    case 64: e = cudaLaunchKernelEx(&cfg, append_kernel<T, 2>, c, kk, vv, n, rows, hstride); break;
+    case 128: e = cudaLaunchKernelEx(&cfg, append_kernel<T, 4>, c, kk, vv, n, rows, hstride); break;
     default: return cudaErrorInvalidValue;
   }
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_append(const CacheView& c, const void* k, const void* v, int n, long long hstride, int in_dtype,

@@ -166,6 +166,15 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
   return old;
 }
 
+// The counter update of a fused append + decode step: every CTA of the grid
+// reads the counters first, then the last merge of the grid writes these.
+struct StepUpdate {
+  bool on = false;    // a fused step
+  bool ok = false;    // the token was stored (a LINEAR cache was not full)
+  long long pos = 0;  // counters after the step
+  int stored = 0;
+};
+
 // Threads per output float4 in the cross-split merge: the largest of 8, 4, 2
 // that fits the CTA with a whole number of warps, else 1.
 __host__ __device__ constexpr int merge_lanes(int items, int threads) {
@@ -181,18 +190,43 @@ __host__ __device__ constexpr int merge_lanes(int items, int threads) {
 // Accumulator layout: ACCPAD == 0: acc[warp][h][d]; ACCPAD > 0 (tensor-core
 // kernel): rows of D + ACCPAD floats, channel d at (d % (D/8)) * 8 + d / (D/8).
 // HG > 1: warp w holds only heads 4 j .. 4 j + 3, j = (w / 4) % HG, and the
-// other heads' entries of that warp are not read.
-template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps, int HG = 1>
+// other heads' entries of that warp are not read.  EXTRA = 1: one more state
+// per head after the warps' (row NWARP of sm_m / sm_l), whose accumulator row
+// ex_acc (laid out like a warp's, the same for every head) enters only when
+// its weight is not zero.
+// One (b, kv head) of a fused step is done: the last of the grid's B * Hkv
+// to get here (after every CTA of the grid has read the counters) writes the
+// new counters.
+__device__ __forceinline__ void step_arrive(const CacheView& c, const StepUpdate& step) {
+  const unsigned units = (unsigned)c.B * (unsigned)c.Hkv;
+  if (atom_add_acq_rel_gpu(&c.state->step_arrive, 1u) == units - 1) {
+    if (step.ok) {
+      c.state->pos = step.pos;
+      c.state->stored = step.stored;
+    } else {
+      set_status(c.state, KVQ_DEV_OVERFLOW);
+    }
+    c.state->step_arrive = 0u;
+  }
+}
+
+// STEP (a fused step): every CTA of the (b, kv head) arrives, with rows or
+// without (splits >= nse write nothing), the last arrival merges when there
+// are several live splits, and the last such arrival of the grid advances
+// the cache counters (or reports an overflow).
+template <int D, int G, int ACCPAD, int NWARP = kDecodeWarps, int HG = 1, int EXTRA = 0, bool STEP = false>
 __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs& a, int b, int kvh, int split, int nse,
-                                            float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc) {
+                                            float (*sm_m)[G], float (*sm_l)[G], const float* sm_acc,
+                                            const float* ex_acc = nullptr, StepUpdate step = StepUpdate{}) {
   constexpr int PROW = D + kPartialPad;
   constexpr int AROW = D + ACCPAD;
   constexpr int NTHR = 32 * NWARP;
-  static_assert(NWARP <= 32, "one lane per warp in the per-head reduction");
+  constexpr int NW = NWARP + EXTRA;
+  static_assert(NW <= 32 && EXTRA <= 1, "one lane per state in the per-head reduction");
   __shared__ float sm_w[kMaxSplits][G];
   __shared__ float sm_lsum[kMaxSplits][G];
   __shared__ float sm_inv[G];
-  __shared__ float sm_we[NWARP][G];   // weight of warp w's state in head h's CTA merge
+  __shared__ float sm_we[NW][G];      // weight of state w in head h's CTA merge
   __shared__ float sm_hm[G];          // CTA max and sum of each head
   __shared__ float sm_hl[G];
   __shared__ int s_last;
@@ -204,7 +238,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   {
     const int lane = threadIdx.x & 31;
     for (int h = threadIdx.x >> 5; h < G; h += NWARP) {
-      const bool mine = lane < NWARP && (HG == 1 || ((lane >> 2) % HG) == (h >> 2));
+      const bool mine = lane < NW && (lane >= NWARP || HG == 1 || ((lane >> 2) % HG) == (h >> 2));
       const float mw = mine ? sm_m[lane][h] : neg_inf();
       float M = mw;
 #pragma unroll
@@ -213,7 +247,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
       float L = mine ? sm_l[lane][h] * e : 0.0f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane < NWARP) sm_we[lane][h] = e;
+      if (lane < NW) sm_we[lane][h] = e;
       if (lane == 0) {
         sm_hm[h] = M;
         sm_hl[h] = L;
@@ -235,7 +269,13 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
       if (HG > 1 && ((w >> 2) % HG) != (h >> 2)) continue;
       A = fmaf(sm_acc[w * G * AROW + pos], sm_we[w][h], A);
     }
-    if (nse == 1) {
+    if constexpr (EXTRA) {
+      const float e = sm_we[NWARP][h];
+      A = e != 0.0f ? fmaf(ex_acc[p], e, A) : A;
+    }
+    if (STEP && split >= nse) {
+      // a fused step's CTA without rows: nothing to write
+    } else if (nse == 1) {
       const size_t oo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + d;
       store_io(a.out, oo, a.io_dtype, L > 0.0f ? A / L : 0.0f);
     } else {
@@ -247,7 +287,7 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
       }
     }
   }
-  if (nse == 1) return;
+  if (!STEP && nse == 1) return;
 
   // The last split of this (b, kv head) to finish merges all partials.  The
   // barrier orders every thread's partial stores before thread 0's arrival,
@@ -256,11 +296,19 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
   // whole CTA after the second barrier.
   __syncthreads();
   if (threadIdx.x == 0) {
-    const bool last = atom_add_acq_rel_gpu(&c.split_sem[bh], 1u) == (unsigned)(nse - 1);
+    const unsigned arrivals = STEP ? gridDim.x : (unsigned)nse;
+    const bool last = atom_add_acq_rel_gpu(&c.split_sem[bh], 1u) == arrivals - 1;
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
+  if (STEP && nse == 1) {   // a fused step with one live split: its output is written
+    if (threadIdx.x == 0) {
+      c.split_sem[bh] = 0u;
+      step_arrive(c, step);
+    }
+    return;
+  }
   const float* P0 = a.partials + bh * a.nsplit * G * PROW;
   // Thread layout of the merge: SPL threads (adjacent lanes) per float4 of the
   // G x D output, each summing every SPL-th split.  The first PF partial
@@ -360,7 +408,10 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     store_io(a.out, oo + 2, a.io_dtype, A.z * inv);
     store_io(a.out, oo + 3, a.io_dtype, A.w * inv);
   }
-  if (threadIdx.x == 0) c.split_sem[bh] = 0u;
+  if (threadIdx.x == 0) {
+    c.split_sem[bh] = 0u;
+    if constexpr (STEP) step_arrive(c, step);
+  }
 }
 
 template <int KF> struct Stages { static constexpr int v = (KF == F_FP16) ? 3 : 4; };

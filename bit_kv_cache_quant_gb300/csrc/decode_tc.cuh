@@ -38,8 +38,53 @@
 #include <type_traits>
 
 #include "decode_tc_frag.cuh"
+#include "quantize_row.cuh"
 
 namespace kvq {
+
+// The fused append's new token, by one warp: codes the token of (b, kv head)
+// bh into cache slot `slot` with the append's rules, scores the dequantised
+// key against each head (fp32), and leaves the head's (score, 1, value row)
+// in m_row, l_row and newv (channel d of the value row at word
+// (d % VCH) * 8 + d / VCH, the per-warp accumulator layout).
+template <int D, int G, int VCH>
+__device__ __forceinline__ void append_new_token(const CacheView& c, const DecodeArgs& a, int b, int kvh, size_t bh,
+                                              int slot, int lane, float* newv, float* m_row, float* l_row) {
+  constexpr int E = D / 32;
+  float xk[E], xv[E], hk[E], hv[E], qv[G][E];
+  // every input first (the cache writes below would hold back later loads)
+  const size_t ro = bh * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    xk[e] = load_io(a.k_new, ro + e, a.in_dtype);
+    xv[e] = load_io(a.v_new, ro + e, a.in_dtype);
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const size_t qo = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[h][e] = load_io(a.q, qo + e, a.io_dtype);
+  }
+  quantize_row_dq<E, true>(c.k, c.k_bias ? c.k_bias + (size_t)kvh * D : nullptr, xk, bh, c.cap_alloc, slot, lane, hk);
+  quantize_row_dq<E, true>(c.v, nullptr, xv, bh, c.cap_alloc, slot, lane, hv);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int d = lane * E + e;
+    newv[(d % VCH) * 8 + d / VCH] = hv[e];
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float p = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) p = fmaf(qv[h][e], hk[e], p);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if (lane == 0) {
+      m_row[h] = p * a.qscale;
+      l_row[h] = 1.0f;
+    }
+  }
+}
 
 template <int ROWB, int NW>
 __device__ __forceinline__ void lds_row_words(uint32_t (&w)[NW], const uint8_t* plane, int r, int off) {
@@ -167,7 +212,8 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
   static constexpr int warps = Shape::warps;
   // per-warp (head, channel) accumulators, written over the stages after the loop
   static constexpr int acc_bytes = warps * G * (D + 8) * 4;
-  static constexpr int static_smem = 2 * kMaxSplits * G * 4 + 2 * warps * G * 4 + (D / 32) * 32 + 1024;
+  static constexpr int static_smem =
+      2 * kMaxSplits * G * 4 + 2 * (warps + 1) * G * 4 + (D + 8) * 4 + (D / 32) * 32 + 1024;
   static constexpr int budget = 227 * 1024 / Shape::ctas_per_sm - 2048 - static_smem;
   static constexpr int raw = (budget / stage) / NGRP * NGRP;
   static constexpr int cap = NGRP == 1 ? kTcStagesNarrow : 8;
@@ -178,7 +224,9 @@ template <int D, int G, int KF, int VF, int NGRP> struct TcStages {
   }
 };
 
-template <int D, int G, int KF, int VF, int NGRP>
+// APP: the fused append of kvq_append_decode (a.k_new set); its own
+// instantiation, so that the plain decode carries none of its code.
+template <int D, int G, int KF, int VF, int NGRP, bool APP>
 __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShape<NGRP, TcHeads<G>::hg>::ctas_per_sm)
     decode_tc_kernel(const __grid_constant__ CacheView c, DecodeArgs a) {
   constexpr int HG = TcHeads<G>::hg;
@@ -206,17 +254,22 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   // waves (whose later tiles would only crowd L2)
   constexpr int PF_TILES = NGRP == 1 ? 4 : NSTAGE;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per kv head");
+  static_assert(!(APP && K_KIVIB), "the fused append does not code KIVI_BLOCK keys");
   static_assert(NSTAGE % NGRP == 0, "each stage serves one tile group");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ float sm_m[NWARP][G];
-  __shared__ float sm_l[NWARP][G];
+  // per-warp (max, sum) of each head; with APP, slot NWARP: the new token
+  // (or nothing)
+  __shared__ float sm_m[NWARP + APP][G];
+  __shared__ float sm_l[NWARP + APP][G];
+  __shared__ float sm_newv[APP ? D + 8 : 1];   // the new token's dequantised value row (merge slot NWARP)
   __shared__ __align__(8) uint64_t mbar[NSTAGE];
   __shared__ __align__(8) uint64_t mbar_meta;   // metadata of the initial ring (one use)
   __shared__ int s_ninit;                       // tiles of the initial ring
   __shared__ unsigned s_done[NSTAGE];     // warps done with a stage, over all its tiles (TW per tile)
   __shared__ int s_last_tile[NSTAGE];     // last tile copied into a stage, -1 if none
   __shared__ int s_T;
+  __shared__ long long s_pos;             // fused append: absolute position of the new token
   __shared__ volatile int s_fail;
   __shared__ float sm_qsum[NB][8];        // sum of q of each head over each 32-channel key block
   // KIVI_BLOCK keys: the query in fp32 (the fragments are folded with each
@@ -269,15 +322,30 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         }
       }
     }
-    // the query rows of this kv head (the producer may still write them, so
-    // they are only requested into L2)
+    // the query rows of this kv head, and a fused append's new key and value
+    // rows (the producer may still write them, so they are only requested
+    // into L2)
     {
       const int es = a.io_dtype == KVQ_DTYPE_F32 ? 4 : 2;
       const uint8_t* q0 = reinterpret_cast<const uint8_t*>(a.q) + ((size_t)b * a.Hq + (size_t)kvh * G) * D * es;
       for (int off = 0; off < G * D * es; off += 128) prefetch_l2(q0 + off);
+      if constexpr (APP) {
+        const int ei = a.in_dtype == KVQ_DTYPE_F32 ? 4 : 2;
+        for (int off = 0; off < D * ei; off += 128) {
+          prefetch_l2(reinterpret_cast<const uint8_t*>(a.k_new) + bh * D * ei + off);
+          prefetch_l2(reinterpret_cast<const uint8_t*>(a.v_new) + bh * D * ei + off);
+        }
+      }
     }
     s_fail = 0;
     s_ninit = 0;
+    if constexpr (APP) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {   // merge slot NWARP stays empty unless this CTA appends
+        sm_m[NWARP][h] = neg_inf();
+        sm_l[NWARP][h] = 0.0f;
+      }
+    }
     mbar_init(&mbar_meta, 1);
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) {
@@ -311,6 +379,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     if (lane == 0) {
       T0 = c.state->stored;
       s_T = T0;
+      if constexpr (APP) s_pos = c.state->pos;
       if constexpr (K_KIVIB) s_tail = c.state->tail;
     }
     T0 = __shfl_sync(0xffffffffu, T0, 0);
@@ -321,11 +390,12 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       __syncwarp();   // lane 0's barrier initialisation is visible to the warp
       if (lane < nt0) {
         const int r0 = a0 + lane * kTileTokens;
+        const uint32_t stall = lane == 0 ? a.stall_tx : 0u;
         if constexpr (NGRP > 1) {
-          mbar_expect_tx(&mbar[lane], (uint32_t)R.tx_codes);
+          mbar_expect_tx(&mbar[lane], (uint32_t)R.tx_codes + stall);
           issue_codes<D, KF, VF>(smem, R, lane, c, bh, r0, &mbar[lane]);
         } else {
-          mbar_expect_tx(&mbar[lane], (uint32_t)(R.tx_codes + R.tx_meta));
+          mbar_expect_tx(&mbar[lane], (uint32_t)(R.tx_codes + R.tx_meta) + stall);
           issue_codes<D, KF, VF>(smem, R, lane, c, bh, r0, &mbar[lane]);
           if (R.tx_meta > 0) issue_meta(smem, R, lane, 1, c, bh, r0, &mbar[lane]);
         }
@@ -392,6 +462,32 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   const int T = s_T;
   int t0, t1, nse;
   split_rows(T, a.nsplit, split, t0, t1, nse);
+  // Fused append ("StreamingLLM + KIVI", "Implementation": per layer and
+  // step, append the token, evict, attend): the splits attend over the T rows
+  // stored before this step, and the last live split's CTA codes the new
+  // token into its slot and adds it to the merge as one more state.  A full
+  // ring overwrites the slot of the oldest window token, which the splits
+  // therefore leave out (excl).  The counters advance as kvq_append would,
+  // once every CTA has read them (merge_store's step arrival).
+  int excl = -1, slot = 0;
+  bool app_cta = false;
+  StepUpdate step{};
+  if constexpr (APP) {
+    const long long p = s_pos;
+    const bool ring = c.layout == KVQ_LAYOUT_RING;
+    step.on = true;
+    step.ok = ring || (long long)T + 1 <= c.cap;
+    step.pos = p + 1;
+    const long long w = (long long)c.sink + c.window;
+    step.stored = ring ? (int)(p + 1 < w ? p + 1 : w) : T + 1;
+    if (ring) {
+      slot = p < c.sink ? (int)p : c.sink + (int)((p - c.sink) % c.window);
+      if (T >= c.sink + c.window) excl = slot;
+    } else {
+      slot = T;
+    }
+    app_cta = step.ok && split == nse - 1;
+  }
   // KIVI_BLOCK: CTA a.nsplit attends over the fp32 tail and merges as one
   // more split (partial slot nse, after the bulk's); a cache with no closed
   // block has no bulk splits.
@@ -403,7 +499,9 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     if (T == 0) nse = TT > 0 ? 0 : 1;
     nse_all = nse + (TT > 0 ? 1 : 0);
   }
-  if (is_tail ? TT == 0 : split >= nse) return;   // no rows for this CTA (no copy was issued)
+  // no rows for this CTA (no copy was issued); in a fused step it still
+  // arrives at the merge, which counts every CTA of its (b, kv head)
+  if (!APP && (is_tail ? TT == 0 : split >= nse)) return;
   const int ntiles = is_tail ? 0 : (t1 - t0 + kTileTokens - 1) / kTileTokens;
 
   const int vgi = V_AFF ? (g * VCH) / c.v.group : 0;
@@ -444,6 +542,11 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   int cur_blk = -1;
   float zt = 0.0f;
 
+  // The fused append's token, coded while the first tiles are in flight.
+  if constexpr (APP) {
+    if (app_cta && warp == NWARP - 1)
+      append_new_token<D, G, VCH>(c, a, b, kvh, bh, slot, lane, sm_newv, sm_m[NWARP], sm_l[NWARP]);
+  }
   const int ninit = s_ninit;
   // the plane-major initial ring's metadata has landed (seen by this warp)
   bool meta_in = NGRP == 1 || R.tx_meta == 0;
@@ -503,7 +606,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       }
     }
     // Blocks wholly inside the split skip the row masks; the last block of
-    // the split (rows past its end) takes them.
+    // the split (rows past its end) and a block holding the excluded ring
+    // slot take them.
     auto block = [&](auto masked) {
       constexpr bool MASK = decltype(masked)::value;
       // ------------------------------------------------------ S^T = K Q^T
@@ -547,7 +651,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       float sc[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        vk[e] = !MASK || tok0 - blk + rk[e] < t1;
+        vk[e] = !MASK || (tok0 - blk + rk[e] < t1 && (!APP || tok0 - blk + rk[e] != excl));
         float v = 0.0f;
         if constexpr (K_Q40) {
           // codes entered as signed levels u - 8: the score is sum over blocks of d * sum(q (u - 8))
@@ -619,12 +723,13 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
         p[e] = fast_exp2(sc[e] - m_run);
         l_part += p[e];
       }
-      // Rows past the split's end were copied as whatever the buffer holds:
-      // their weight is 0, and their value scale / zero (or fp16 values) are
-      // zeroed so that no NaN reaches the MMA.
+      // Rows past the split's end were copied as whatever the buffer holds
+      // (the excluded slot, as whatever the fused append was writing): their
+      // weight is 0, and their value scale / zero (or fp16 values) are zeroed
+      // so that no NaN reaches the MMA.
       bool vok[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) vok[i] = !MASK || tok0 - blk + rr[i] < t1;
+      for (int i = 0; i < 4; ++i) vok[i] = !MASK || (tok0 - blk + rr[i] < t1 && (!APP || tok0 - blk + rr[i] != excl));
       __half2 sAB = u2h(0u), zAB = u2h(0u), sCD = u2h(0u), zCD = u2h(0u);
       if constexpr (V_AFF) {
         const __half* vs = reinterpret_cast<const __half*>(smem + R.vs(stg));
@@ -690,7 +795,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
           pvt_mma<VB, NW, MT, false>(oacc, pb, mo, A, B, C, E, sAB, zAB, sCD, zCD);
       }
     };
-    if (tok0 + 16 <= t1) block(std::false_type{});
+    if (tok0 + 16 <= t1 && (!APP || (unsigned)(excl - tok0) >= 16u)) block(std::false_type{});
     else if (tok0 < t1) block(std::true_type{});   // warp-uniform
     // Release the stage.  The tile group's last warp to finish it copies the
     // tile NSTAGE ahead into it (the warp barrier, the acquire-release count
@@ -711,17 +816,24 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       }
     }
   }
+  // The fused append's new token: the appending CTA's last warp codes it
+  // into its slot with the append's rules, then scores the dequantised key
+  // against each head (fp32) and leaves the head's (score, 1, value row)
+  // as merge slot NWARP.
   __syncthreads();
-  if (s_fail) {
-    // A stage never arrived: report it, wait (bounded) for the copies still
-    // in flight into this CTA's shared memory, and leave the outputs alone.
+  // A stage never arrived: report it and wait (bounded) for the copies still
+  // in flight into this CTA's shared memory.  The CTA still takes part in the
+  // split merge with empty states (the status word marks the outputs as
+  // invalid), so that the merge counter of its (b, kv head) returns to zero.
+  const bool failed = s_fail != 0;
+  if (failed) {
     if (threadIdx.x == 0) {
       set_status(c.state, KVQ_DEV_TIMEOUT);
       for (int s = 0; s < NSTAGE; ++s)
         if (s_last_tile[s] >= 0) mbar_wait_bounded(&mbar[s], (s_last_tile[s] / NSTAGE) & 1);
       if (NGRP > 1 && s_ninit > 0 && R.tx_meta > 0) mbar_wait_bounded(&mbar_meta, 0);
     }
-    return;
+    __syncthreads();
   }
 
   // Per-warp results to shared memory, over the stage ring (every copy has
@@ -807,12 +919,12 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     if (hd < G) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        sm_acc[warp][hd][(2 * mt) * 8 + g] = (oacc[mt][0] + oacc[mt][1]) + zacc;
-        sm_acc[warp][hd][(2 * mt + 1) * 8 + g] = (oacc[mt][2] + oacc[mt][3]) + zacc;
+        sm_acc[warp][hd][(2 * mt) * 8 + g] = failed ? 0.0f : (oacc[mt][0] + oacc[mt][1]) + zacc;
+        sm_acc[warp][hd][(2 * mt + 1) * 8 + g] = failed ? 0.0f : (oacc[mt][2] + oacc[mt][3]) + zacc;
       }
       if (g == 0) {
-        sm_m[warp][hd] = m_run;
-        sm_l[warp][hd] = l_part;
+        sm_m[warp][hd] = failed ? neg_inf() : m_run;
+        sm_l[warp][hd] = failed ? 0.0f : l_part;
       }
     }
   }
@@ -821,16 +933,18 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     DecodeArgs am = a;
     am.nsplit = a.nsplit + 1;   // partial slots per (b, kv head): the splits and the tail
     merge_store<D, G, 8, NWARP, HG>(c, am, b, kvh, is_tail ? nse : split, nse_all, sm_m, sm_l, &sm_acc[0][0][0]);
+  } else if constexpr (APP) {
+    merge_store<D, G, 8, NWARP, HG, 1, true>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0], sm_newv, step);
   } else {
     merge_store<D, G, 8, NWARP, HG>(c, a, b, kvh, split, nse, sm_m, sm_l, &sm_acc[0][0][0]);
   }
 }
 
-template <int D, int G, int KF, int VF, int NGRP>
+template <int D, int G, int KF, int VF, int NGRP, bool APP>
 cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
   using S = TcStages<D, G, KF, VF, NGRP>;
   using Shape = typename S::Shape;
-  auto kern = decode_tc_kernel<D, G, KF, VF, NGRP>;
+  auto kern = decode_tc_kernel<D, G, KF, VF, NGRP, APP>;
   const int smem = S::dyn_bytes(S::stage);
   static_assert(S::dyn_bytes(S::stage) + S::static_smem <= 227 * 1024, "shared memory per CTA");
   static std::atomic<unsigned long long> configured{0};
@@ -858,16 +972,38 @@ cudaError_t launch_decode_tc_shape(const CacheView& c, const DecodeArgs& a, cuda
   return e;
 }
 
+template <int D, int G, int KF, int VF, bool APP>
+cudaError_t launch_decode_tc_app(const CacheView& c, const DecodeArgs& at, cudaStream_t st) {
+  if constexpr (G <= 4) {
+    if (at.wide == 2) return launch_decode_tc_shape<D, G, KF, VF, 4, APP>(c, at, st);
+  }
+  if (at.wide == 2) return cudaErrorInvalidValue;   // the plan gives sixteen-warp CTAs up to four heads only
+  return at.wide ? launch_decode_tc_shape<D, G, KF, VF, 2, APP>(c, at, st)
+                 : launch_decode_tc_shape<D, G, KF, VF, 1, APP>(c, at, st);
+}
+
+// The fused append is instantiated for head_dim 128, every format but
+// KIVI_BLOCK keys and the one-wave shapes (wide 1 and 2): there the step's
+// separate append launch would cost as much as the decode's own chain, while
+// in a grid of several waves the token's coding delays its CTA's pipeline by
+// more than a separate launch costs (measured).  Other caches and plans report
+// cudaErrorNotSupported (nothing launched) and kvq_append_decode runs the
+// separate steps.
 template <int D, int G, int KF, int VF>
 cudaError_t launch_decode_tc_dg(const CacheView& c, const DecodeArgs& a, cudaStream_t st) {
   DecodeArgs at = a;
   at.nsplit = a.nsplit_tc;
   if (at.nsplit < 1 || at.nsplit > kMaxSplits) return cudaErrorInvalidValue;
-  if constexpr (G <= 4) {
-    if (a.wide == 2) return launch_decode_tc_shape<D, G, KF, VF, 4>(c, at, st);
+  if (a.k_new) {
+    if constexpr (D == 128 && !(KF == F_KIVIB8 || KF == F_KIVIB4)) {
+      if constexpr (G <= 4) {
+        if (at.wide == 2) return launch_decode_tc_shape<D, G, KF, VF, 4, true>(c, at, st);
+      }
+      if (at.wide == 1) return launch_decode_tc_shape<D, G, KF, VF, 2, true>(c, at, st);
+    }
+    return cudaErrorNotSupported;
   }
-  if (a.wide == 2) return cudaErrorInvalidValue;   // the plan gives sixteen-warp CTAs up to four heads only
-  return a.wide ? launch_decode_tc_shape<D, G, KF, VF, 2>(c, at, st) : launch_decode_tc_shape<D, G, KF, VF, 1>(c, at, st);
+  return launch_decode_tc_app<D, G, KF, VF, false>(c, at, st);
 }
 
 template <int D, int KF, int VF>
@@ -898,6 +1034,7 @@ cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaSt
     if (c.D == 128) return launch_decode_tc_d<128, KF, VF>(c, G, a, st);
     return launch_decode_tc_d<64, KF, VF>(c, G, a, st);
   }
+  if (a.k_new) return cudaErrorNotSupported;   // the fused append runs on the tensor-core kernel only
   return launch_decode_cc<KF, VF>(c, G, a, st);
   }
 }

@@ -142,13 +142,13 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Waits for phase `parity` of the mbarrier, giving up after ~200 ms (a stage
-// normally completes in microseconds); false means the wait ran out.
+// Waits for phase `parity` of the mbarrier, giving up after kWaitNs (~200 ms;
+// a stage normally completes in microseconds); false means the wait ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity) {
   if (mbar_try_wait(m, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(m, parity)) {
-    if (global_ns() - t0 > 200000000ull) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
   }
   return true;
 }
@@ -301,13 +301,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Programmatic dependent launch: wait until the grids this launch depends on
-// have completed (a no-op for a launch without the attribute), and allow the
-// next dependent launch to start its prologue.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-}
 
 // A hint: bring the line at p into L2 (and its page translation into the TLBs).
 __device__ __forceinline__ void prefetch_l2(const void* p) {

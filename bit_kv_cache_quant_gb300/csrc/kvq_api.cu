@@ -508,9 +508,16 @@ kvq_status kvq_decode_plan_query(const kvq_config* cfg, int32_t n_q_heads, int32
   return KVQ_OK;
 }
 
-kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
-                           float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  begin_call();
+}  // extern "C"
+
+namespace {
+
+// kvq_test_stall_decode_tiles: bytes every decode CTA's first tile barrier expects in excess.
+std::atomic<unsigned> g_stall_tx{0};
+
+// Argument checks shared by kvq_decode_attn and kvq_append_decode.
+kvq_status check_decode_args(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
+                             void* workspace, size_t ws_bytes) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "null cache");
   if (!q || !out) return fail(KVQ_ERR_INVALID_ARG, "null q or out");
   if (!valid_dtype(io_dtype)) return fail(KVQ_ERR_INVALID_ARG, "unknown io dtype %d", io_dtype);
@@ -524,6 +531,17 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   if (need && (!workspace || ws_bytes < need))
     return fail(KVQ_ERR_CAPACITY, "decode workspace needs %zu bytes, got %zu", need, ws_bytes);
   if (need && ((uintptr_t)workspace & 15)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  return KVQ_OK;
+}
+
+// One decode launch; k_new != null asks the tensor-core kernel to code the
+// new token first (cudaErrorNotSupported, with nothing launched, where that
+// kernel does not serve the cache and io dtype).
+cudaError_t launch_decode_any(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
+                              float softmax_scale, void* workspace, const void* k_new, const void* v_new,
+                              int32_t in_dtype, cudaStream_t stream) {
+  const int G = n_q_heads / c->cfg.n_kv_heads;
+  const size_t need = kvq_decode_workspace_bytes(c, n_q_heads);
   if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / sqrtf((float)c->cfg.head_dim);
   kvq::DecodeArgs a;
   a.q = q;
@@ -536,28 +554,92 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   a.nsplit_tc = plan.nsplit_tc;
   a.wide = plan.wide;
   a.partials = need ? static_cast<float*>(workspace) : nullptr;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.in_dtype = in_dtype;
+  a.stall_tx = g_stall_tx.load(std::memory_order_relaxed);
   const int kf = fmt_code(c->cfg.k_format, c->cfg.k_bits);
   const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);
-  cudaError_t e;
   using namespace kvq;
+  if (kf == F_KIVIB8 && vf == F_AFF8) return k_new ? cudaErrorNotSupported : launch_decode<F_KIVIB8, F_AFF8>(c->view, G, a, stream);
+  if (kf == F_KIVIB4 && vf == F_AFF4) return k_new ? cudaErrorNotSupported : launch_decode<F_KIVIB4, F_AFF4>(c->view, G, a, stream);
+  if (kf == F_FP16 && vf == F_FP16) return launch_decode<F_FP16, F_FP16>(c->view, G, a, stream);
+  if (kf == F_KIVI8 && vf == F_AFF8) return launch_decode<F_KIVI8, F_AFF8>(c->view, G, a, stream);
+  if (kf == F_KIVI4 && vf == F_AFF4) return launch_decode<F_KIVI4, F_AFF4>(c->view, G, a, stream);
+  if (kf == F_AFF8 && vf == F_AFF8) return launch_decode<F_AFF8, F_AFF8>(c->view, G, a, stream);
+  if (kf == F_AFF4 && vf == F_AFF4) return launch_decode<F_AFF4, F_AFF4>(c->view, G, a, stream);
+  if (kf == F_Q40 && vf == F_AFF8) return launch_decode<F_Q40, F_AFF8>(c->view, G, a, stream);
+  if (kf == F_Q40 && vf == F_AFF4) return launch_decode<F_Q40, F_AFF4>(c->view, G, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+// Whether the (K format, V format) pair and, for KIVI_BLOCK keys, the
+// head count have a decode kernel.
+kvq_status check_decode_pair(kvq_cache c, int G, int32_t io_dtype) {
+  using namespace kvq;
+  const int kf = fmt_code(c->cfg.k_format, c->cfg.k_bits);
+  const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);
   if (kf == F_KIVIB8 || kf == F_KIVIB4) {
     if (G > 4 && (io_dtype == KVQ_DTYPE_F32 || c->cfg.head_dim == 32 || !c->view.has_maps))
       return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode on the fp32 CUDA-core path takes up to 4 query heads per kv head");
-    if (kf == F_KIVIB8 && vf == F_AFF8) e = launch_decode<F_KIVIB8, F_AFF8>(c->view, G, a, stream);
-    else if (kf == F_KIVIB4 && vf == F_AFF4) e = launch_decode<F_KIVIB4, F_AFF4>(c->view, G, a, stream);
-    else return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode is built for 8-bit keys with 8-bit values and 4 with 4");
-    return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attn");
+    if (!((kf == F_KIVIB8 && vf == F_AFF8) || (kf == F_KIVIB4 && vf == F_AFF4)))
+      return fail(KVQ_ERR_UNSUPPORTED, "KIVI_BLOCK decode is built for 8-bit keys with 8-bit values and 4 with 4");
+    return KVQ_OK;
   }
-  if (kf == F_FP16 && vf == F_FP16) e = launch_decode<F_FP16, F_FP16>(c->view, G, a, stream);
-  else if (kf == F_KIVI8 && vf == F_AFF8) e = launch_decode<F_KIVI8, F_AFF8>(c->view, G, a, stream);
-  else if (kf == F_KIVI4 && vf == F_AFF4) e = launch_decode<F_KIVI4, F_AFF4>(c->view, G, a, stream);
-  else if (kf == F_AFF8 && vf == F_AFF8) e = launch_decode<F_AFF8, F_AFF8>(c->view, G, a, stream);
-  else if (kf == F_AFF4 && vf == F_AFF4) e = launch_decode<F_AFF4, F_AFF4>(c->view, G, a, stream);
-  else if (kf == F_Q40 && vf == F_AFF8) e = launch_decode<F_Q40, F_AFF8>(c->view, G, a, stream);
-  else if (kf == F_Q40 && vf == F_AFF4) e = launch_decode<F_Q40, F_AFF4>(c->view, G, a, stream);
-  else return fail(KVQ_ERR_UNSUPPORTED, "decode for this (K format, V format) pair is not built");
+  const bool built = (kf == F_FP16 && vf == F_FP16) || (kf == F_KIVI8 && vf == F_AFF8) ||
+                     (kf == F_KIVI4 && vf == F_AFF4) || (kf == F_AFF8 && vf == F_AFF8) ||
+                     (kf == F_AFF4 && vf == F_AFF4) || (kf == F_Q40 && vf == F_AFF8) || (kf == F_Q40 && vf == F_AFF4);
+  if (!built) return fail(KVQ_ERR_UNSUPPORTED, "decode for this (K format, V format) pair is not built");
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
+                           float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  begin_call();
+  kvq_status st = check_decode_args(c, q, out, n_q_heads, io_dtype, workspace, ws_bytes);
+  if (st != KVQ_OK) return st;
+  st = check_decode_pair(c, n_q_heads / c->cfg.n_kv_heads, io_dtype);
+  if (st != KVQ_OK) return st;
+  const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, nullptr, nullptr,
+                                          0, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attn");
 }
+
+kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t in_dtype, const void* q, void* out,
+                             int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream) {
+  begin_call();
+  kvq_status st = check_decode_args(c, q, out, n_q_heads, io_dtype, workspace, ws_bytes);
+  if (st != KVQ_OK) return st;
+  st = check_decode_pair(c, n_q_heads / c->cfg.n_kv_heads, io_dtype);
+  if (st != KVQ_OK) return st;
+  if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "null k or v");
+  if (!valid_dtype(in_dtype)) return fail(KVQ_ERR_INVALID_ARG, "unknown input dtype %d", in_dtype);
+  // one launch: the tensor-core kernel codes the token and attends
+  if (c->cfg.layout != KVQ_LAYOUT_COMPACT) {
+    const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, k, v,
+                                            in_dtype, stream);
+    if (e == cudaSuccess) return KVQ_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "kvq_append_decode");
+  }
+  // otherwise the three steps in turn: append, StreamingLLM eviction of a
+  // compact cache, decode
+  st = append_rows(c, k, v, 1, 1, in_dtype, 0, stream, "kvq_append_decode");
+  if (st != KVQ_OK) return st;
+  if (c->cfg.layout == KVQ_LAYOUT_COMPACT) {
+    const cudaError_t e = kvq::launch_evict_middle(c->view, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_append_decode");
+  }
+  const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, nullptr, nullptr,
+                                          0, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_append_decode");
+}
+
+void kvq_test_stall_decode_tiles(int32_t on) { g_stall_tx.store(on ? 16u : 0u, std::memory_order_relaxed); }
 
 size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int32_t head_dim, int32_t obs_window) {
   (void)head_dim;
@@ -643,7 +725,11 @@ kvq_status kvq_stats_read(kvq_cache c, kvq_stats* out) {
 kvq_status kvq_clear_status(kvq_cache c, cudaStream_t stream) {
   begin_call();
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "null cache");
+  // the status word, and the decode merge's per-(b, kv head) arrival counters
+  // (which a launch that stopped early could have left short of their reset)
   cudaError_t e = cudaMemsetAsync(&c->view.state->status, 0, sizeof(int), stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(c->view.split_sem, 0, (size_t)c->cfg.batch * c->cfg.n_kv_heads * sizeof(unsigned), stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_clear_status");
 }
 

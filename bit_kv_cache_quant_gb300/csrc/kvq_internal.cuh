@@ -25,7 +25,8 @@ struct DevState {
   unsigned evict_arrive;    // CTA arrival counter of the eviction in flight
   int k_calibrated;         // per-channel K scales frozen
   int tail;                 // KIVI_BLOCK: rows in the full-precision tail
-  int pad[56];
+  unsigned step_arrive;     // CTA arrival counter of the fused append + decode in flight
+  int pad[55];
 };
 static_assert(sizeof(DevState) == 256, "DevState must be 256 bytes");
 
@@ -74,6 +75,14 @@ struct CacheView {
   int B, Hkv, D, cap, cap_alloc, layout, sink, window;
   int has_maps;
 };
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed (a no-op for a launch without the attribute), and allow the
+// next dependent launch to start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 __device__ __forceinline__ void set_status(DevState* st, int code) {
   atomicCAS(&st->status, 0, code);
@@ -175,6 +184,16 @@ struct DecodeArgs {
   int wide;          // tensor-core kernel: 1 = two tile groups of warps per CTA (the grid fits
                      // in one wave at the CTAs per SM of that shape) instead of one; 2 = four
                      // tile groups, one CTA per SM
+  // Fused append (tensor-core kernel): the new token's key and value rows
+  // [B][Hkv][D] of in_dtype, coded into the cache by this launch before it
+  // attends over the cache including that token; null for a plain decode.
+  const void* k_new;
+  const void* v_new;
+  int in_dtype;
+  // Test hook (0 in use): bytes the first tile's barrier of every CTA expects
+  // beyond what its copies bring, so that the wait for that tile runs out
+  // and the launch reports KVQ_DEV_TIMEOUT.
+  unsigned stall_tx;
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
 // an (D, G) outside the instantiated set.
@@ -188,6 +207,7 @@ cudaError_t launch_snapkv_pool(const float* in, float* out, int BH, int S, int k
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
                         cudaStream_t st);
 
+constexpr unsigned long long kWaitNs = 200000000ull;   // default limit of a bounded device wait (200 ms)
 constexpr int kSnapChunk = 256;   // keys per CTA of the SnapKV scoring kernels
 constexpr int kTmaRows = 64;      // rows per TMA box of a code plane (one decode tile)
 constexpr int kMaxSplits = 128;   // decode splits per (b, kv head)

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define KVQ_ABI_VERSION 1
+#define KVQ_ABI_VERSION 2
 
 typedef enum kvq_status {
   KVQ_OK = 0,
@@ -286,6 +286,34 @@ kvq_status kvq_decode_plan_query(const kvq_config* cfg, int32_t n_q_heads, int32
 kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                            float softmax_scale, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* One decode step of one layer in one call ([SLK] "Implementation": per layer
+   and step, append the token, evict, then attend): the effect of kvq_append of
+   one token (k, v: device [B, Hkv, 1, D] of in_dtype, no flags), then
+   kvq_evict(KVQ_EVICT_MIDDLE) for COMPACT and RING caches, then
+   kvq_decode_attn (arguments, workspace and errors as that call), so the
+   attention sees the new token.  LINEAR and RING caches served by the
+   tensor-core decode with head_dim 128 (16-bit io, not KIVI_BLOCK keys) whose
+   decode grid is a single wave (kvq_decode_plan_query's *wide >= 1) do it in
+   one launch: the CTA holding the last stored rows codes the token into its
+   slot (bit-identical to kvq_append) and adds it to the attention from the
+   dequantised row, a full ring leaves the slot it overwrites out of the
+   attention, and the counters advance as kvq_append would.  Every other cache
+   runs the three steps as separate launches (in a grid of several waves the
+   coding would hold back its CTA for longer than a separate launch costs).
+   Device overflow of a LINEAR cache sets KVQ_DEV_OVERFLOW and attends over the
+   rows already stored. */
+kvq_status kvq_append_decode(kvq_cache cache, const void* k, const void* v, int32_t in_dtype, const void* q,
+                             void* out, int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/* Test hook for the failure path of the tensor-core decode: while on (0 off,
+   the default; process-wide, read at each launch), every CTA of the following
+   decode launches arms its first tile's barrier for 16 bytes more than the
+   copies bring, so that its bounded wait runs out (after 200 ms), the launch
+   sets KVQ_DEV_TIMEOUT and returns with the cache untouched; the GPU stays
+   usable.  Nothing faults or traps. */
+void kvq_test_stall_decode_tiles(int32_t on);
+
 /* kvq_decode_attn for callers that cannot allocate device memory.  The pages
    have no counterpart of this call; it exists for this library's users.
    Some callers may not call cudaMalloc at all: code running inside an allocator
@@ -343,7 +371,9 @@ kvq_status snapkv_topk(const float* scores, int32_t batch, int32_t n_kv_heads, i
 /* Synchronises the device, copies `cache`'s counters to the host and fills `*out`. */
 kvq_status kvq_stats_read(kvq_cache cache, kvq_stats* out);
 
-/* Clears the device status word (stream-ordered). */
+/* Clears the device status word and the decode merge's per-(b, kv head)
+   arrival counters (stream-ordered).  After a KVQ_DEV_TIMEOUT the cache is
+   usable again once this has run: the stored rows and counters are intact. */
 kvq_status kvq_clear_status(kvq_cache cache, cudaStream_t stream);
 
 /* Number of kernels the last call on this thread enqueued (for launch accounting). */

@@ -28,7 +28,7 @@ def test_exports_every_declared_function(kvq):
     raw = ctypes.CDLL(kvq.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.lib.kvq_abi_version() == 1
+    assert kvq.lib.kvq_abi_version() == 2
 
 
 def test_header_functions_are_extern_c():

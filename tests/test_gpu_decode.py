@@ -158,3 +158,30 @@ def test_decode_launch_shapes(kvq, pair, name, B, H, T, cap):
     cache, oc = _build(kvq, pair, B, H, 128, T, torch.bfloat16, seed=T + B, cap=cap, bias=pair[0] == "q4_0")
     for G in (3, 8):
         _check(kvq, cache, oc, G, torch.bfloat16, seed=G + 11, what=f"{name} G={G}")
+
+
+def test_tile_wait_timeout_reports_and_recovers(kvq):
+    # A tile that never completes (the test hook arms each CTA's first tile
+    # barrier for more bytes than arrive): its bounded wait runs out, the
+    # launch reports KVQ_DEV_TIMEOUT, the CTAs that stopped still arrive on
+    # their split's merge counter (which the last arrival resets), and after
+    # kvq_clear_status the same cache decodes exactly as before.
+    pair = ("affine_token", 4, 64, "affine_token", 4, 64)
+    cache, _ = _build(kvq, pair, 2, 8, 128, 4096, torch.bfloat16, seed=31)
+    q = _rand((2, 24, 128), 32, torch.bfloat16).cuda()
+    ref = cache.decode_attn(q).clone()
+    torch.cuda.synchronize()
+    assert cache.stats().device_status == 0
+    kvq.kvq_test_stall_decode_tiles(True)
+    try:
+        cache.decode_attn(q)
+        torch.cuda.synchronize()
+    finally:
+        kvq.kvq_test_stall_decode_tiles(False)
+    assert cache.stats().device_status == kvq.DEV_TIMEOUT
+    lay = cache.layout
+    sem = cache.buf[lay.split_sem: lay.split_sem + 4 * 16].view(torch.int32)
+    assert torch.all(sem == 0), "a merge counter was left short of its reset"
+    kvq.kvq_clear_status(cache.handle)
+    assert cache.stats().device_status == 0
+    assert torch.equal(cache.decode_attn(q), ref)
