@@ -190,9 +190,12 @@ class DecodeStep:
         if not self.fused:
             return self.eager_append() + self.eager_decode()
         n = 0
+        # a layer's step follows another layer's (or, for layer 0, the previous step's last layer's):
+        # with more than one layer, the kernel before each call never writes that call's cache
+        early = len(self.caches) > 1
         for layer, c in enumerate(self.caches):
             c.launches = 0
-            c.append_decode(self.k1[layer], self.v1[layer], self.q[layer], out=self.out[layer])
+            c.append_decode(self.k1[layer], self.v1[layer], self.q[layer], out=self.out[layer], early_read=early)
             n += c.launches
         self.t_seen += 1
         return n

@@ -43,6 +43,7 @@ EVICT_MIDDLE = 0
 EVICT_KEEPSET = 1
 APPEND_CALIBRATE_K = 1
 APPEND_RECOMPUTE_K = 2
+STEP_EARLY_READ = 1
 DEV_OK, DEV_OVERFLOW, DEV_BAD_KEEPSET, DEV_TIMEOUT = 0, 1, 2, 3
 
 
@@ -90,7 +91,7 @@ _proto("kvq_decode_plan_query", c_int32, POINTER(kvq_config), c_int32, c_int32, 
 _proto("kvq_decode_attn", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p, c_size_t,
        c_void_p)
 _proto("kvq_append_decode", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_int32,
-       c_float, c_void_p, c_size_t, c_void_p)
+       c_float, c_void_p, c_size_t, c_int32, c_void_p)
 _proto("kvq_test_stall_decode_tiles", None, c_int32)
 _proto("snapkv_workspace_bytes", c_size_t, c_int32, c_int32, c_int32, c_int32, c_int32)
 _proto("snapkv_pool", c_int32, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p)
@@ -197,10 +198,10 @@ def kvq_decode_attn(cache, q: torch.Tensor, out: torch.Tensor, n_q_heads: int, i
 
 def kvq_append_decode(cache, k: torch.Tensor, v: torch.Tensor, in_dtype: int, q: torch.Tensor, out: torch.Tensor,
                       n_q_heads: int, io_dtype: int, softmax_scale: float = 0.0,
-                      workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+                      workspace: Optional[torch.Tensor] = None, flags: int = 0, stream=None) -> None:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.kvq_append_decode(cache, _dev_ptr(k), _dev_ptr(v), in_dtype, _dev_ptr(q), _dev_ptr(out), n_q_heads,
-                                 io_dtype, softmax_scale, _dev_ptr(workspace), ws_bytes, _stream(stream)))
+                                 io_dtype, softmax_scale, _dev_ptr(workspace), ws_bytes, flags, _stream(stream)))
 
 
 def kvq_test_stall_decode_tiles(on: bool) -> None:
@@ -343,9 +344,10 @@ class KVCache:
         return out
 
     def append_decode(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out: Optional[torch.Tensor] = None,
-                      softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+                      softmax_scale: float = 0.0, early_read: bool = False, stream=None) -> torch.Tensor:
         """One decode step: append the token k, v [B, Hkv, 1, D], evict (streaming layouts) and attend
-        with q [B, Hq, D] over the cache including that token."""
+        with q [B, Hq, D] over the cache including that token.  early_read: the kernel just before
+        this call on the stream writes neither this cache nor its counters (KVQ_STEP_EARLY_READ)."""
         self._check_rows(k, v)
         if k.shape[2] != 1:
             raise ValueError("append_decode takes one token per (batch row, kv head)")
@@ -359,7 +361,7 @@ class KVCache:
             raise ValueError("out must have q's shape and dtype")
         hq = q.shape[1]
         kvq_append_decode(self.handle, k, v, DTYPES[k.dtype], q, out, hq, DTYPES[q.dtype], softmax_scale,
-                          self.workspace(hq), stream)
+                          self.workspace(hq), STEP_EARLY_READ if early_read else 0, stream)
         self.launches += kvq_last_launch_count()
         return out
 

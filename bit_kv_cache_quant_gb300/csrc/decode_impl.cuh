@@ -763,12 +763,15 @@ cudaError_t launch_decode_dg(const CacheView& c, const DecodeArgs& a, cudaStream
   const TileLayout L = tile_layout<D, KF, VF>(c.k.n_groups, c.v.n_groups);
   const int smem = NSTAGE * L.bytes;
   if (a.nsplit > kMaxSplits) return cudaErrorInvalidValue;
-  static int configured_for = -1;   // dynamic shared memory above 48 KB needs an opt-in
-  if (configured_for < smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes);
+  // dynamic shared memory above 48 KB needs an opt-in, per device (the
+  // attribute is set for the largest stage this kernel accepts)
+  static std::atomic<unsigned long long> configured{0};
+  {
+    const cudaError_t e = once_per_device(configured, []() {
+      return cudaFuncSetAttribute(decode_kernel<D, G, KF, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes);
+    });
     if (e != cudaSuccess) return e;
-    configured_for = NSTAGE * tile_layout<D, KF, VF>(D / 16, D / 16).bytes;
   }
   // KIVI_BLOCK keys: one more CTA per (b, kv head) for the full-precision tail
   const dim3 grid(a.nsplit + ((KF == F_KIVIB8 || KF == F_KIVIB4) ? 1 : 0), c.Hkv, c.B);

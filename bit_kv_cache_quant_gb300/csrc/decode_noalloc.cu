@@ -13,8 +13,11 @@
 //
 // The array's name is only a host-side stand-in in host code, not a device
 // address, so the real address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached here.  That
-// look-up happens inside the first call on each device; make that first call
+// cudaGetSymbolAddress (with that device current) and cached here, together
+// with the unique id of the CUDA context it belongs to.  That look-up happens
+// inside the first call on each device, and again in the first call after
+// the device's context was replaced (cudaDeviceReset ends the context, and
+// the array then lives at an address of the new one); make those calls
 // before any stream capture.
 //
 // Every call on a device shares the one array and leaves its last contents
@@ -27,6 +30,8 @@
 
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "kvq_internal.cuh"
 
 namespace {
@@ -38,8 +43,34 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // id of the context the address belongs to
 
-// Device address of g_decode_scratch on the current device (looked up once).
+// Unique id of the calling thread's current CUDA context (never reused within
+// the process), or 0 when there is none yet or the driver cannot tell.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_decode_scratch on the current device: looked up once
+// per device and context (again when the context id changed or is unknown).
 kvq_status scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -47,12 +78,14 @@ kvq_status scratch_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return kvq::report_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_noalloc: device index beyond 63");
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch_addr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);   // makes the device's context current if needed
     if (e != cudaSuccess || p == nullptr)
       return kvq::report_error(KVQ_ERR_CUDA, "kvq_decode_attn_noalloc: cudaGetSymbolAddress of the scratch failed");
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();
   }
   *out = g_scratch_addr[dev];
   return KVQ_OK;

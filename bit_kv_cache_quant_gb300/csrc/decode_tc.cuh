@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(&c.vmap) : "memory");
-    if constexpr (!K_KIVIB) {
+    if (!K_KIVIB && !a.early) {   // (an early launch requests the rows themselves)
       const int Th = min(max(*reinterpret_cast<volatile const int*>(&c.state->stored), 0), c.cap_alloc);
       int h0, h1, hn;
       split_rows(Th, a.nsplit, split, h0, h1, hn);
@@ -356,25 +356,12 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_async_smem();   // the initialised barriers are visible to the copy engine
   }
-  grid_dependency_wait();
-  // Every CTA of this grid is resident: the next launch may start its own
-  // prologue (and L2 requests) while this one runs.
-  grid_launch_dependents();
-  // Warp roles: 16-row block of each tile, head group, tile group.
-  const int blk = (warp & 3) * 16;
-  const int hg = (warp >> 2) % HG;
-  const int grp = (warp >> 2) / HG;
-  const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
   // Warp 0 reads the stored length and requests the whole initial ring of
   // tiles: lane s the code planes of stage s, lane NSTAGE the metadata of
   // all of them (one copy per plane; every copy request costs the issuing
   // SM's copy engine time, so a ring of many small copies arrives late),
   // while the other warps build their query fragments.
-  // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
-  // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
-  // columns and q enters exactly.  Thread (g, t) builds column g at the key
-  // channels of its fragment slots.
-  if (warp == 0) {
+  auto issue_ring = [&]() {
     int T0 = 0;
     if (lane == 0) {
       T0 = c.state->stored;
@@ -406,7 +393,27 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
       }
       if (lane == 0) s_ninit = nt0;
     }
-  }
+  };
+  // With a.early the caller guarantees that the kernel before this launch
+  // writes neither this cache nor its counters, so the counters and the
+  // stored rows are read before the dependency wait: the whole initial ring
+  // then lands while that kernel finishes.  Only the query (and a fused
+  // append's new token) wait for it.
+  if (a.early && warp == 0) issue_ring();
+  grid_dependency_wait();
+  // Every CTA of this grid is resident: the next launch may start its own
+  // prologue (and L2 requests) while this one runs.
+  grid_launch_dependents();
+  if (!a.early && warp == 0) issue_ring();
+  // Warp roles: 16-row block of each tile, head group, tile group.
+  const int blk = (warp & 3) * 16;
+  const int hg = (warp >> 2) % HG;
+  const int grp = (warp >> 2) / HG;
+  const int hd = 4 * hg + t;   // the query head whose scores and outputs this thread holds
+  // Column 2j + e of the warp's Q^T holds head 4 hg + j: e = 0 its fp16(q),
+  // e = 1 the residual q - fp16(q), so that head's score is the sum of the two
+  // columns and q enters exactly.  Thread (g, t) builds column g at the key
+  // channels of its fragment slots.
   uint32_t qf[KS][2];
   {
     const int hq = 4 * hg + (g >> 1);

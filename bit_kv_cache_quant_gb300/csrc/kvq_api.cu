@@ -210,7 +210,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
@@ -539,7 +539,7 @@ kvq_status check_decode_args(kvq_cache c, const void* q, void* out, int32_t n_q_
 // kernel does not serve the cache and io dtype).
 cudaError_t launch_decode_any(kvq_cache c, const void* q, void* out, int32_t n_q_heads, int32_t io_dtype,
                               float softmax_scale, void* workspace, const void* k_new, const void* v_new,
-                              int32_t in_dtype, cudaStream_t stream) {
+                              int32_t in_dtype, bool early, cudaStream_t stream) {
   const int G = n_q_heads / c->cfg.n_kv_heads;
   const size_t need = kvq_decode_workspace_bytes(c, n_q_heads);
   if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / sqrtf((float)c->cfg.head_dim);
@@ -558,6 +558,7 @@ cudaError_t launch_decode_any(kvq_cache c, const void* q, void* out, int32_t n_q
   a.v_new = v_new;
   a.in_dtype = in_dtype;
   a.stall_tx = g_stall_tx.load(std::memory_order_relaxed);
+  a.early = early ? 1 : 0;
   const int kf = fmt_code(c->cfg.k_format, c->cfg.k_bits);
   const int vf = fmt_code(c->cfg.v_format, c->cfg.v_bits);
   using namespace kvq;
@@ -605,13 +606,13 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   st = check_decode_pair(c, n_q_heads / c->cfg.n_kv_heads, io_dtype);
   if (st != KVQ_OK) return st;
   const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, nullptr, nullptr,
-                                          0, stream);
+                                          0, false, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attn");
 }
 
 kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t in_dtype, const void* q, void* out,
                              int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
-                             size_t ws_bytes, cudaStream_t stream) {
+                             size_t ws_bytes, int32_t flags, cudaStream_t stream) {
   begin_call();
   kvq_status st = check_decode_args(c, q, out, n_q_heads, io_dtype, workspace, ws_bytes);
   if (st != KVQ_OK) return st;
@@ -619,10 +620,12 @@ kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t 
   if (st != KVQ_OK) return st;
   if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "null k or v");
   if (!valid_dtype(in_dtype)) return fail(KVQ_ERR_INVALID_ARG, "unknown input dtype %d", in_dtype);
+  if (flags & ~KVQ_STEP_EARLY_READ) return fail(KVQ_ERR_INVALID_ARG, "unknown step flags 0x%x", flags);
+  const bool early = (flags & KVQ_STEP_EARLY_READ) != 0;
   // one launch: the tensor-core kernel codes the token and attends
   if (c->cfg.layout != KVQ_LAYOUT_COMPACT) {
     const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, k, v,
-                                            in_dtype, stream);
+                                            in_dtype, early, stream);
     if (e == cudaSuccess) return KVQ_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "kvq_append_decode");
   }
@@ -635,7 +638,7 @@ kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t 
     if (e != cudaSuccess) return cuda_fail(e, "kvq_append_decode");
   }
   const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, nullptr, nullptr,
-                                          0, stream);
+                                          0, false, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_append_decode");
 }
 

@@ -194,6 +194,10 @@ struct DecodeArgs {
   // beyond what its copies bring, so that the wait for that tile runs out
   // and the launch reports KVQ_DEV_TIMEOUT.
   unsigned stall_tx;
+  // The kernel just before this launch on the stream writes neither this
+  // cache nor its counters (kvq_append_decode's KVQ_STEP_EARLY_READ): the
+  // launch reads them before its dependency wait.
+  int early;
 };
 // Defined once per (K format, V format) pair; returns cudaErrorNotSupported for
 // an (D, G) outside the instantiated set.

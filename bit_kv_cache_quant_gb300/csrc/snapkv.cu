@@ -682,13 +682,12 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
     return e;
   }
   const int smem = S <= kTopkSmemKeys ? S * (int)sizeof(float) : 0;
-  static int configured = 0;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kTopkSmemKeys * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    configured = 1;
-  }
+  static std::atomic<unsigned long long> configured{0};   // the opt-in is per device
+  const cudaError_t e = once_per_device(configured, []() {
+    return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kTopkSmemKeys * (int)sizeof(float));
+  });
+  if (e != cudaSuccess) return e;
   topk_kernel<<<B * Hkv, 1024, smem, st>>>(scores, S, budget, n_sink, idx);
   note_launch();
   return cudaGetLastError();

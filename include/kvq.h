@@ -119,10 +119,15 @@ typedef enum kvq_evict_mode {
                                       again and the new ones with the new scale / zero.
                                       O(stored * D) per call; excludes CALIBRATE_K. */
 
+/* kvq_append_decode flags */
+#define KVQ_STEP_EARLY_READ 1      /* the kernel just before the call writes neither this
+                                      cache nor its counters (see kvq_append_decode) */
+
 /* Device status codes (kvq_stats.device_status). */
 #define KVQ_DEV_OK 0
 #define KVQ_DEV_OVERFLOW 1         /* an append would pass the capacity; nothing was written */
 #define KVQ_DEV_BAD_KEEPSET 2      /* keep-set not strictly ascending or beyond stored rows */
+#define KVQ_STEP_EARLY_READ 1      /* kvq_append_decode flag (see there)                     */
 #define KVQ_DEV_TIMEOUT 3          /* a bounded wait inside a kernel ran out; outputs of that call
                                       are unspecified */
 
@@ -301,10 +306,15 @@ kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_
    runs the three steps as separate launches (in a grid of several waves the
    coding would hold back its CTA for longer than a separate launch costs).
    Device overflow of a LINEAR cache sets KVQ_DEV_OVERFLOW and attends over the
-   rows already stored. */
+   rows already stored.  flags: 0 or KVQ_STEP_EARLY_READ, the caller's promise
+   that the kernel just before this call on the stream writes neither this
+   cache nor its counters (another layer's step, the projection that produced
+   q, k and v): the one-launch step then reads the counters and requests the
+   stored rows before that kernel has finished, and waits for it only for q,
+   k and v.  Breaking the promise gives wrong results (not a fault). */
 kvq_status kvq_append_decode(kvq_cache cache, const void* k, const void* v, int32_t in_dtype, const void* q,
                              void* out, int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
-                             size_t ws_bytes, cudaStream_t stream);
+                             size_t ws_bytes, int32_t flags, cudaStream_t stream);
 
 /* Test hook for the failure path of the tensor-core decode: while on (0 off,
    the default; process-wide, read at each launch), every CTA of the following
@@ -325,8 +335,9 @@ void kvq_test_stall_decode_tiles(int32_t on);
    library holds until the process exits.  A cache whose
    kvq_decode_workspace_bytes exceeds that returns KVQ_ERR_CAPACITY and enqueues
    nothing.  The first call on each device looks up the array's device address
-   (cudaGetSymbolAddress, that device current); make that first call before any
-   stream capture.  All calls on a device share the array and leave their last
+   (cudaGetSymbolAddress, that device current), and so does the first call
+   after that device's context was replaced (cudaDeviceReset); make those calls
+   before any stream capture.  All calls on a device share the array and leave their last
    contents in it (nothing in it needs to start at zero): calls that overlap on
    the GPU race and give wrong results, so serialise them.  Allocates nothing. */
 kvq_status kvq_decode_attn_noalloc(kvq_cache cache, const void* q, void* out, int32_t n_q_heads,

@@ -156,3 +156,37 @@ def test_full_linear_cache_reports_overflow(kvq):
     assert torch.equal(a.buf[lay.k_codes:], before[lay.k_codes:]), "an overflowing step wrote the cache"
     kh, vh = oc.dequant()
     assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), "overflow: the stored rows only")
+
+
+@pytest.mark.parametrize("pair", [PAIRS[4], PAIRS[5], PAIRS[2]], ids=["aff4", "q40v8", "kivi4"])
+def test_layers_in_turn_with_early_read(kvq, pair):
+    # Two layers' caches stepped in turn with KVQ_STEP_EARLY_READ (the kernel
+    # before each call is the other layer's step, which never writes this
+    # cache): the counters and stored rows are read before the dependency
+    # wait, and every step must still match the oracle.
+    B, H, D, G, T0, steps = 1, 8, 128, 3, 1500, 5
+    g = torch.Generator().manual_seed(23)
+    layers = []
+    for li in range(2):
+        bias = _rand((H, D), g, torch.float32, 1.5) if pair[0] == "q4_0" else None
+        off = bias[None, :, None, :] if bias is not None else _rand((1, H, 1, D), g, torch.float32, 2.0)
+        a, _, oc = _pair_caches(kvq, pair, B, H, D, 2048, "linear", 0, 0, bias)
+        k0 = _rand((B, H, T0, D), g, torch.bfloat16, 1.0, off)
+        v0 = _rand((B, H, T0, D), g, torch.bfloat16)
+        calib = pair[0] == "kivi_chan"
+        a.append(k0.cuda(), v0.cuda(), calibrate_k=calib)
+        if calib:
+            oc.calibrate_k(host(k0))
+        oc.append(host(k0), host(v0))
+        layers.append((a, oc, off))
+    for t in range(steps):
+        for a, oc, off in layers:
+            k1 = _rand((B, H, 1, D), g, torch.bfloat16, 1.0, off)
+            v1 = _rand((B, H, 1, D), g, torch.bfloat16)
+            q = _rand((B, H * G, D), g, torch.bfloat16)
+            out = a.append_decode(k1.cuda(), v1.cuda(), q.cuda(), early_read=True)
+            oc.append(host(k1), host(v1))
+            kh, vh = oc.dequant()
+            assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), f"early-read step {t}")
+    for a, oc, _ in layers:
+        assert_cache_equal(a, oc, "early-read cache")
