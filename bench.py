@@ -513,16 +513,63 @@ def oracle_sample(w):
     return SnapKVOracleSample(w) if w.prompt_len else OracleSample(w)
 
 
-def cpu_baseline(w, seconds):
-    s = oracle_sample(w)
+def _oracle_run(name, seconds):
+    """Builds one oracle sample of workload `name` and steps it for about `seconds`:
+    (bytes, steps, wall time, description)."""
+    s = oracle_sample(synth.get_workload(name))
     s.step()
     nbytes, n, t0 = 0, 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         nbytes += s.step()
         n += 1
-    dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} steps of {s.describe()}; {dt:.1f} s single-threaded numpy"}
+    return nbytes, n, time.perf_counter() - t0, s.describe()
+
+
+def _oracle_worker(args):
+    return _oracle_run(*args)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(w, seconds, all_cores=True, nproc=None):
+    """The oracle on the host: one thread, then (all_cores) one spawned process per core (nproc of
+    them if given), each stepping its own copy of the same one-slice sample (the slices of a step are
+    independent), the rate summed over the processes."""
+    nbytes, n, dt, desc = _oracle_run(w.name, seconds)
+    nproc = nproc or os.cpu_count() or 1
+    line = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} steps of {desc}; {dt:.1f} s single-threaded numpy",
+            "nproc": nproc, "cpu_model": cpu_model()}
+    if all_cores and nproc > 1:
+        import multiprocessing as mp
+
+        # spawned, not forked: this process already holds a CUDA context
+        with mp.get_context("spawn").Pool(nproc) as pool:
+            res = pool.map(_oracle_worker, [(w.name, seconds)] * nproc)
+        total, steps, wall = sum(r[0] for r in res), sum(r[1] for r in res), max(r[2] for r in res)
+        line["all_cores"] = {"value": total / wall / 1e9, "unit": "GB/s", "cores": nproc,
+                             "sample": f"{nproc} processes x one copy each of the same sample, {steps} steps "
+                                       f"in {wall:.1f} s (one thread per process)"}
+    return line
 
 
 def run_reference(a, rank, world):

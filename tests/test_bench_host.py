@@ -157,3 +157,14 @@ def test_reference_arm_line(name, capsys):
     assert cb["value"] == d["value"] and cb["unit"] == "GB/s" and cb["kind"] == "oracle" and cb["cores"] == 1
     assert cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_one_thread_and_all_cores():
+    # the oracle timed on one thread and in spawned processes, one per core (two here, to keep the
+    # test short), with the core count and the CPU model stated
+    w = synth.get_workload("tinygpt")
+    cb = bench.cpu_baseline(w, 0.3, nproc=2)
+    assert cb["cores"] == 1 and cb["kind"] == "oracle" and cb["value"] > 0 and cb["unit"] == "GB/s"
+    assert cb["nproc"] == 2 and isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    ac = cb["all_cores"]
+    assert ac["cores"] == 2 and ac["value"] > 0 and ac["unit"] == "GB/s" and "2 processes" in ac["sample"]

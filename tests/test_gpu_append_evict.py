@@ -120,23 +120,28 @@ def test_uncalibrated_kivi_append_rejected(kvq):
         cache.append(k, k)
 
 
-@pytest.mark.parametrize("layout,n_steps", [("compact", 1), ("compact", 259), ("compact", 261), ("compact", 300),
-                                            ("ring", 261), ("ring", 700)])
+@pytest.mark.parametrize("layout,n_steps", [("compact", 1), ("compact", 195), ("compact", 197), ("compact", 236),
+                                            ("ring", 197), ("ring", 636)])
 def test_streaming_decode_matches_oracle(kvq, layout, n_steps):
-    # KIVI int8, sink 4 + window 256, one append + one evict per step
-    sink, window, D, B, H = 4, 256, 32, 1, 2
+    # KIVI int8, sink 4 + window 256: the per-channel K scales calibrated over
+    # a 64-token fill (so later keys code to interior levels, not only to the
+    # clamps), then one append + one evict per step; 64 + n_steps tokens in all
+    # cover the cache before, at and past sink + window = 260
+    sink, window, D, B, H, n0 = 4, 256, 32, 1, 2, 64
     cap = sink + window + (1 if layout == "compact" else 0)
     cache = kvq.KVCache(B, H, D, cap, "kivi_chan", 8, 0, "affine_token", 8, 32, layout=layout, sink=sink,
                         window=window)
     oc = OracleCache(oracle_spec(cache))
-    fill = _inputs((B, H, 1, D), 7, torch.float32)
+    fill = _inputs((B, H, n0, D), 7, torch.float32)
     cache.append(fill.cuda(), fill.cuda(), calibrate_k=True)
     cache.evict_middle()
     oc.calibrate_k(host(fill))
     oc.append(host(fill), host(fill))
     oc.evict_middle()
     g = torch.Generator().manual_seed(8)
-    ks = torch.randn(n_steps, B, H, 1, D, generator=g)
+    # later keys from the fill's distribution (its channel offsets), so most codes are interior
+    off = fill.float().mean(dim=2, keepdim=True)
+    ks = torch.randn(n_steps, B, H, 1, D, generator=g) + off
     vs = torch.randn(n_steps, B, H, 1, D, generator=g)
     ksd, vsd = ks.cuda(), vs.cuda()
     for t in range(n_steps):
@@ -144,8 +149,60 @@ def test_streaming_decode_matches_oracle(kvq, layout, n_steps):
         cache.evict_middle()
         oc.append(ks[t].numpy(), vs[t].numpy())
         oc.evict_middle()
-    assert_cache_equal(cache, oc, f"{layout} after {n_steps + 1} tokens")
-    assert oc.stored == min(n_steps + 1, sink + window)
+    assert_cache_equal(cache, oc, f"{layout} after {n0 + n_steps} tokens")
+    assert oc.stored == min(n0 + n_steps, sink + window)
+    u = oc.k.codes(oc.stored).astype(np.int64)
+    assert ((u > 0) & (u < 255)).mean() > 0.9, "most key codes should be interior levels"
+
+
+def test_ring_forty_thousand_steps(kvq):
+    # The long streaming run of the ring workload on a reduced instance (B 1,
+    # 2 kv heads, sink 4 + window 256): a 260-token calibrated fill, then
+    # 40 000 single-token appends (graph replays of 1 000 each).  The final
+    # cache equals the oracle's, whose state after any number of steps is a
+    # function of the surviving tokens and their positions (the ring appends
+    # of one call and of many give the same cache): 260 rows, positions 0..3
+    # and the last 256.
+    sink, window, D, B, H, n0, N = 4, 256, 128, 1, 2, 260, 40000
+    chunk = 1000
+    cache = kvq.KVCache(B, H, D, sink + window, "kivi_chan", 4, 0, "affine_token", 4, 32, layout="ring", sink=sink,
+                        window=window)
+    oc = OracleCache(oracle_spec(cache))
+    fill_k = _inputs((B, H, n0, D), 41, torch.bfloat16)
+    fill_v = _inputs((B, H, n0, D), 42, torch.bfloat16, 0.0)
+    cache.append(fill_k.cuda(), fill_v.cuda(), calibrate_k=True)
+    oc.calibrate_k(host(fill_k))
+    oc.append(host(fill_k), host(fill_v))
+    g = torch.Generator().manual_seed(43)
+    off = fill_k.float().mean(dim=2, keepdim=True)
+    ks = (torch.randn(B, H, N, D, generator=g) + off).to(torch.bfloat16)
+    vs = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16)
+    ksd, vsd = ks.cuda(), vs.cuda()
+    stage_k = torch.empty(chunk, B, H, 1, D, dtype=torch.bfloat16, device="cuda")
+    stage_v = torch.empty_like(stage_k)
+    cache.append(stage_k[0].zero_(), stage_v[0].zero_())   # loads the kernel before capture
+    cache.reset()
+    cache.append(fill_k.cuda(), fill_v.cuda(), calibrate_k=True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(chunk):
+            cache.append(stage_k[i], stage_v[i])
+            cache.evict_middle()
+    for c0 in range(0, N, chunk):
+        stage_k.copy_(ksd[:, :, c0:c0 + chunk].permute(2, 0, 1, 3).unsqueeze(3))
+        stage_v.copy_(vsd[:, :, c0:c0 + chunk].permute(2, 0, 1, 3).unsqueeze(3))
+        graph.replay()
+    torch.cuda.synchronize()
+    st = cache.stats()
+    assert (st.pos, st.stored, st.device_status) == (n0 + N, sink + window, 0)
+    oc.append(host(ks), host(vs))
+    assert_cache_equal(cache, oc, "ring after 40 000 steps")
+    q = torch.randn(B, 3 * H, D, generator=g).to(torch.bfloat16)
+    kh, vh = oc.dequant()
+    from oracle import attention as oatt
+    from kvq_helpers import assert_attention_close
+    assert_attention_close(cache.decode_attn(q.cuda()), oatt.decode_attention(host(q), kh, vh), "after 40 000 steps")
 
 
 def test_ring_bulk_append_longer_than_window(kvq):

@@ -148,8 +148,22 @@ def test_snapkv_prefill_then_decode_full(kvq):
         ref = osk.obs_window_scores(kn[0, h], w.obs_window)
         rest = np.sort(ref[w.n_sink:])[::-1]
         gap = rest[w.budget - w.n_sink - 1] - rest[w.budget - w.n_sink]
-        if gap > 1e-5 * ref.max():
+        eps = 1e-5 * ref.max()
+        if gap > eps:
             np.testing.assert_array_equal(ig[0, h], osk.select_indices(ref, w.budget, w.n_sink))
+        else:
+            # an ill-conditioned cutoff: the device set must still be a valid
+            # top-k under the oracle's scores within eps (sinks kept, sorted,
+            # budget rows, no unselected row clearly above a selected one)
+            sel = ig[0, h]
+            assert len(sel) == w.budget and np.all(np.diff(sel) > 0)
+            assert np.array_equal(sel[:w.n_sink], np.arange(w.n_sink))
+            kth = rest[w.budget - w.n_sink - 1]
+            mask = np.zeros(S, bool)
+            mask[sel] = True
+            others = np.flatnonzero(~mask)
+            assert ref[sel[w.n_sink:]].min() >= kth - eps
+            assert others.size == 0 or ref[others].max() <= kth + eps
     outs = []
     for step in range(w.decode_steps):
         q, k1, v1 = synth.decode_token_inputs(w, 0, step, S + step, device="cuda")
