@@ -888,7 +888,7 @@ def bench_snapkv(a, kvq, w, rank, world):
             "decode_steps_per_s": world * w.decode_steps * a.steps / t,
             "gpu_launches": ep.launches * a.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None, "kernel": "snapkv_select (stats + scores + top-k)",
+                         "traffic": None, "kernel": "snapkv_select (one-pass scoring + top-k)",
                          "bytes_per_launch": sel_b, "avg_launch_us": t_sel * 1e6,
                          "peak_kind": f"{peak_kind} copy bandwidth"},
             "clocks": clk}

@@ -650,7 +650,9 @@ size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int3
   if (batch < 1 || n_kv_heads < 1 || S < 1) return 0;
   const size_t BH = (size_t)batch * n_kv_heads;
   const size_t nchunk = (S + kvq::kSnapChunk - 1) / kvq::kSnapChunk;
-  return align_up(BH * nchunk * 64 * sizeof(float2), 256) + align_up(BH * (size_t)S * sizeof(float), 256);
+  // row statistics, scores (when the caller passes none), arrival counts and a failure flag
+  return align_up(BH * nchunk * 64 * sizeof(float2), 256) + align_up(BH * (size_t)S * sizeof(float), 256) +
+         align_up((BH + 1) * sizeof(unsigned), 256);
 }
 
 kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int32_t n_kv_heads, int32_t S,
@@ -673,12 +675,14 @@ kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int3
   const size_t BH = (size_t)batch * n_kv_heads;
   const int nchunk = (S + kvq::kSnapChunk - 1) / kvq::kSnapChunk;
   float2* stats = static_cast<float2*>(workspace);
+  const size_t off_scores = align_up(BH * nchunk * 64 * sizeof(float2), 256);
+  const size_t off_arrive = off_scores + align_up(BH * (size_t)S * sizeof(float), 256);
   float* scores = scores_out;
-  if (!scores) scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                 align_up(BH * nchunk * 64 * sizeof(float2), 256));
+  if (!scores) scores = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off_scores);
+  unsigned* arrive = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + off_arrive);
   const int w = obs_window < S ? obs_window : S;
   cudaError_t e = kvq::launch_snapkv(k, head_stride, batch, n_kv_heads, S, head_dim, w, budget, n_sink, scores,
-                                     idx_out, stats, nchunk, stream);
+                                     idx_out, stats, nchunk, arrive, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "snapkv_select");
 }
 
@@ -702,7 +706,7 @@ kvq_status snapkv_topk(const float* scores, int32_t batch, int32_t n_kv_heads, i
   if (batch < 1 || n_kv_heads < 1 || S < 1) return fail(KVQ_ERR_INVALID_ARG, "batch, n_kv_heads, S must be >= 1");
   if (budget < 1 || n_sink < 0) return fail(KVQ_ERR_INVALID_ARG, "budget >= 1 and n_sink >= 0 required");
   if (n_sink > budget) return fail(KVQ_ERR_INVALID_ARG, "n_sink must not exceed budget");
-  cudaError_t e = kvq::launch_topk(scores, batch, n_kv_heads, S, budget, n_sink, idx_out, stream);
+  cudaError_t e = kvq::launch_topk(scores, batch, n_kv_heads, S, budget, n_sink, idx_out, nullptr, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "snapkv_topk");
 }
 

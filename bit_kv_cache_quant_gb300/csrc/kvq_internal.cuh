@@ -204,12 +204,15 @@ struct DecodeArgs {
 template <int KF, int VF>
 cudaError_t launch_decode(const CacheView& c, int G, const DecodeArgs& a, cudaStream_t st);
 
+// arrive: B * Hkv arrival counts then one failure flag (device, zeroed by the launcher).
 cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, int S, int D, int w, int budget,
-                          int n_sink, float* scores, int* idx, float2* stats, int nchunk, cudaStream_t st);
+                          int n_sink, float* scores, int* idx, float2* stats, int nchunk, unsigned* arrive,
+                          cudaStream_t st);
 // Max-pool smoothing of [BH][S] scores, odd kernel_size <= 63, in != out.
 cudaError_t launch_snapkv_pool(const float* in, float* out, int BH, int S, int kernel_size, cudaStream_t st);
+// fail (device, nullable): a scoring launch's failure flag; when set the indices are all -1.
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
-                        cudaStream_t st);
+                        const int* fail, cudaStream_t st);
 
 constexpr unsigned long long kWaitNs = 200000000ull;   // default limit of a bounded device wait (200 ms)
 constexpr int kSnapChunk = 256;   // keys per CTA of the SnapKV scoring kernels

@@ -7,13 +7,17 @@
 // rest are chosen and the union is returned in ascending order.
 //
 // Scoring is a [w x D] x [D x S] contraction per head, run on the tensor
-// cores (fp16 inputs, fp32 accumulation, mma.sync m16n8k16) in two passes
-// over the keys: pass 1 gives each CTA's per-row (max, sum of exp) over its
-// kSnapChunk keys, pass 2 merges those row statistics and turns every logit
-// into its probability, summing over the w rows.  Each warp keeps the next
-// 8 keys' fragments in flight while it multiplies the current ones.  The
-// second read of K is served by L2 for the prompt sizes the page discusses
-// (16K keys x 8 heads x 256 B).
+// cores (fp16 inputs, fp32 accumulation, mma.sync m16n8k16).  Each CTA takes
+// kSnapChunk keys: it computes their logits once, keeps them in shared
+// memory and publishes its per-row (max, sum of exp); once every chunk of
+// its head has published (a per-head arrival count, bounded wait, in a
+// cooperative launch whose CTAs are all resident), it merges the row
+// statistics and turns its logits into probabilities summed over the w rows.
+// K is read once.  Where the grid cannot be resident at once, two launches do
+// the same: pass 1 the statistics, pass 2 the logits again (K from L2 for the
+// prompt sizes the page discusses) and the scores; both give the same bits.
+// Each warp keeps the next 8 keys' fragments in flight while it multiplies
+// the current ones.
 //
 // Selection is a radix select on the fp32 score bit patterns (4 passes of 8
 // bits, the scores held in shared memory) that finds the (budget - n_sink)-th
@@ -36,7 +40,28 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 
 __device__ __forceinline__ uint2 ld_quad(const __half* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
 
+// A hint: request this CTA's keys [key0, key0 + kSnapChunk) (clipped to S)
+// into L2 with one bulk copy per 32 KB, so that the warps' loads, a tile of 8
+// keys ahead each, are served from L2 while HBM streams at full rate.  The
+// rows are contiguous (head_stride >= S) and 16-byte aligned when D * 2 is.
+template <int D>
+__device__ __forceinline__ void prefetch_chunk_l2(const __half* kh, int key0, int S) {
+  if (threadIdx.x != 0 || key0 >= S) return;
+  const uint8_t* p = reinterpret_cast<const uint8_t*>(kh + (size_t)key0 * D);
+  if (reinterpret_cast<uintptr_t>(p) & 15) return;
+  const uint32_t bytes = (uint32_t)(min(kSnapChunk, S - key0) * D * 2);
+  for (uint32_t off = 0; off < bytes; off += 32768)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p + off), "r"(min(32768u, bytes - off))
+                 : "memory");
+}
+
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ unsigned long long clock_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Channel order shared by the observation rows (A) and the keys (B): k-step
 // ks, mma k index 2t + j (j < 2) is channel 16 ks + 4t + j and 2t + 8 + j is
@@ -158,7 +183,7 @@ __device__ __forceinline__ void merge_row_stats(const float2* __restrict__ stats
   if (r < R && r < w) {
 #pragma unroll 8
     for (int cch = part; cch < nchunk; cch += TPR) {
-      const float2 st = stats[cch * 64 + r];
+      const float2 st = __ldcg(&stats[cch * 64 + r]);
       if (st.x != ninf()) {
         const float mn = fmaxf(M, st.x);
         Z = Z * exp2f(M - mn) + st.y * exp2f(st.x - mn);
@@ -227,6 +252,7 @@ __global__ void __launch_bounds__(128) snapkv_stats_kernel(const __half* __restr
   const size_t bh = (size_t)blockIdx.z * Hkv + blockIdx.y;
   const int chunk = blockIdx.x;
   const __half* kh = k + bh * head_stride * D;
+  prefetch_chunk_l2<D>(kh, chunk * kSnapChunk, S);
 
   uint32_t A[MT][D / 16][4];
   load_obs_perm<D, MT>(A, kh, S, w, g, t);
@@ -312,6 +338,105 @@ __global__ void __launch_bounds__(128) snapkv_scores_kernel(const __half* __rest
   }
 }
 
+// One pass (cooperative launch): the logits of this CTA's keys once, kept in
+// shared memory (each thread its own fragments: [warp][tile][mt][4][lane]),
+// the chunk's row statistics published, a per-head arrival count waited for
+// (bounded: after ~200 ms *fail is set and the scores are not valid), then
+// the scores exactly as pass 2 computes them from the same logits.
+template <int D, int MT>
+__global__ void __launch_bounds__(128) snapkv_fused_kernel(const __half* __restrict__ k, long long head_stride,
+                                                           int Hkv, int S, int w, float cscale, float2* stats,
+                                                           int nchunk, float* __restrict__ scores,
+                                                           unsigned* arrive, int* fail) {
+  constexpr int kPerWarp = kSnapChunk / 4;
+  constexpr int NT = kPerWarp / 8;   // tiles of 8 keys per warp
+  extern __shared__ float sm_logit[];
+  __shared__ float sm_m[4][MT * 16];
+  __shared__ float sm_z[4][MT * 16];
+  __shared__ float row_m[64];
+  __shared__ float row_iz[64];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const size_t bh = (size_t)blockIdx.z * Hkv + blockIdx.y;
+  const int chunk = blockIdx.x;
+  const __half* kh = k + bh * head_stride * D;
+  prefetch_chunk_l2<D>(kh, chunk * kSnapChunk, S);
+  float* mylog = sm_logit + (size_t)warp * NT * MT * 4 * 32 + lane;
+
+  uint32_t A[MT][D / 16][4];
+  load_obs_perm<D, MT>(A, kh, S, w, g, t);
+  float rm[MT][2], rz[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) rm[mt][0] = rm[mt][1] = ninf(), rz[mt][0] = rz[mt][1] = 0.0f;
+  const int wbase = chunk * kSnapChunk + warp * kPerWarp;
+  const int ntile = max(0, min(NT, (S - wbase + 7) / 8));
+  uint32_t Bn[D / 16][2];
+  if (ntile > 0) load_keys<D>(Bn, kh, wbase, S, g, t);
+  for (int tile = 0; tile < ntile; ++tile) {
+    const int key0 = wbase + tile * 8;
+    uint32_t Bc[D / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) Bc[ks][0] = Bn[ks][0], Bc[ks][1] = Bn[ks][1];
+    if (tile + 1 < ntile) load_keys<D>(Bn, kh, key0 + 8, S, g, t);
+    float cacc[MT][4];
+    tile_logits<D, MT>(cacc, A, Bc);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mylog[((tile * MT + mt) * 4 + i) * 32] = cacc[mt][i];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (key0 + 2 * t + e < S) {
+            const float v = cacc[mt][2 * hf + e] * cscale;
+            const float mn = fmaxf(rm[mt][hf], v);
+            rz[mt][hf] = rz[mt][hf] * exp2f(rm[mt][hf] - mn) + exp2f(v - mn);
+            rm[mt][hf] = mn;
+          }
+        }
+      }
+    }
+  }
+  snap_row_stats<MT>(rm, rz, sm_m, sm_z, stats + (bh * nchunk + chunk) * 64, g, t, warp);
+  __syncthreads();   // this CTA's statistics are written
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&arrive[bh], 1u);
+    const unsigned long long t0 = clock_ns();
+    unsigned n;
+    do {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(n) : "l"(&arrive[bh]) : "memory");
+      if (n >= (unsigned)nchunk) break;
+      if (clock_ns() - t0 > kWaitNs) {
+        atomicExch(fail, 1);
+        break;
+      }
+    } while (true);
+  }
+  __syncthreads();
+  merge_row_stats<MT>(stats + bh * nchunk * 64, nchunk, w, row_m, row_iz);   // ends with __syncthreads
+  float Mr[MT][2], Ir[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      Mr[mt][hf] = row_m[mt * 16 + g + 8 * hf];
+      Ir[mt][hf] = row_iz[mt * 16 + g + 8 * hf];
+    }
+  }
+  const float inv_w = 1.0f / (float)w;
+  for (int tile = 0; tile < ntile; ++tile) {
+    float cacc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cacc[mt][i] = mylog[((tile * MT + mt) * 4 + i) * 32];
+    }
+    snap_score_tile<MT>(cacc, Mr, Ir, cscale, inv_w, scores + bh * S, wbase + tile * 8, S, g, t);
+  }
+}
+
 // ----------------------------------------------------------------- top-k --
 
 // Monotone map from fp32 to uint32 order; -0.0 ranks with +0.0.
@@ -392,8 +517,10 @@ __device__ __forceinline__ int block_excl_count_n(int v, int* total, int* warp_s
   return r;
 }
 
+// fail (nullable): set by a scoring launch whose wait ran out; the indices
+// are then all -1.
 __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int S, int budget, int n_sink,
-                                                    int* __restrict__ idx_out) {
+                                                    int* __restrict__ idx_out, const int* fail) {
   extern __shared__ float sm_sc[];
   __shared__ unsigned hist[256];
   __shared__ unsigned s_bin, s_need;
@@ -402,6 +529,10 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
   const float* sc = scores + bh * S;
   const int n_keep = min(budget, S);
   int* out = idx_out + bh * n_keep;
+  if (fail && *fail) {
+    for (int j = threadIdx.x; j < n_keep; j += blockDim.x) out[j] = -1;
+    return;
+  }
   if (budget >= S) {
     for (int j = threadIdx.x; j < S; j += blockDim.x) out[j] = j;
     return;
@@ -495,7 +626,8 @@ constexpr int kTopkClusterMaxChunk = 8192;   // positions per CTA (32 KB of shar
 
 __global__ void __launch_bounds__(kTopkClusterThreads) topk_cluster_kernel(const float* __restrict__ scores, int S,
                                                                            int budget, int n_sink,
-                                                                           int* __restrict__ idx_out) {
+                                                                           int* __restrict__ idx_out,
+                                                                           const int* fail) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ float sm_sc[];
@@ -508,6 +640,11 @@ __global__ void __launch_bounds__(kTopkClusterThreads) topk_cluster_kernel(const
   const size_t bh = blockIdx.y;
   const float* sc = scores + bh * S;
   int* out = idx_out + bh * budget;   // budget < S (the host takes the other case)
+  if (fail && *fail) {   // every CTA of the cluster reads the same flag: none reaches a cluster barrier
+    if (rank == 0)
+      for (int j = threadIdx.x; j < budget; j += blockDim.x) out[j] = -1;
+    return;
+  }
   const int chunk = (S + kTopkCluster - 1) / kTopkCluster;
   const int c0 = min(S, rank * chunk), c1 = min(S, c0 + chunk);
   for (int i = threadIdx.x; i < c1 - c0; i += blockDim.x) sm_sc[i] = __ldg(sc + c0 + i);
@@ -637,12 +774,56 @@ cudaError_t launch_snapkv_pool(const float* in, float* out, int BH, int S, int k
 
 // ---------------------------------------------------------------- launch --
 
+// Whether a cooperative grid of `ctas` fused scoring CTAs is resident at once
+// on the current device (remembered per device and shape).
+template <int D, int MT>
+static bool fused_grid_fits(long long ctas, int smem) {
+  static std::atomic<int> per_dev[64];   // CTAs resident at once + 1, 0 unknown
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int known = per_dev[dev].load(std::memory_order_relaxed);
+  if (!known) {
+    int sms = 0, per_sm = 0, coop = 0;
+    bool ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+              cudaFuncSetAttribute(snapkv_fused_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                  cudaSuccess &&
+              cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, snapkv_fused_kernel<D, MT>, 128, smem) ==
+                  cudaSuccess;
+    (void)cudaGetLastError();
+    known = (ok ? per_sm * sms : 0) + 1;
+    per_dev[dev].store(known, std::memory_order_relaxed);
+  }
+  return ctas <= known - 1;
+}
+
 template <int D, int MT>
 static cudaError_t launch_snapkv_dm(const void* k, long long hs, int B, int Hkv, int S, int w,
-                                    float* scores, float2* stats, int nchunk, cudaStream_t st) {
+                                    float* scores, float2* stats, int nchunk, unsigned* arrive, int* fail,
+                                    cudaStream_t st) {
   const float cscale = 1.4426950408889634f / sqrtf((float)D);
   const dim3 grid(nchunk, Hkv, B);
   const __half* kk = static_cast<const __half*>(k);
+  const int smem = 4 * (kSnapChunk / 4 / 8) * MT * 4 * 32 * (int)sizeof(float);
+  // the arrival counts and the failure flag (read by the top-k) start at zero
+  cudaError_t e = cudaMemsetAsync(arrive, 0, ((size_t)B * Hkv + 1) * sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  if (fused_grid_fits<D, MT>((long long)nchunk * Hkv * B, smem)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, snapkv_fused_kernel<D, MT>, kk, hs, Hkv, S, w, cscale, stats, nchunk, scores, arrive,
+                           fail);
+    note_launch();
+    return e;
+  }
   snapkv_stats_kernel<D, MT><<<grid, 128, 0, st>>>(kk, hs, Hkv, S, w, cscale, stats, nchunk);
   note_launch();
   snapkv_scores_kernel<D, MT><<<grid, 128, 0, st>>>(kk, hs, Hkv, S, w, cscale, stats, nchunk, scores);
@@ -652,18 +833,19 @@ static cudaError_t launch_snapkv_dm(const void* k, long long hs, int B, int Hkv,
 
 template <int D>
 static cudaError_t launch_snapkv_d(const void* k, long long hs, int B, int Hkv, int S, int w,
-                                   float* scores, float2* stats, int nchunk, cudaStream_t st) {
+                                   float* scores, float2* stats, int nchunk, unsigned* arrive, int* fail,
+                                   cudaStream_t st) {
   switch ((w + 15) / 16) {
-    case 1: return launch_snapkv_dm<D, 1>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);
-    case 2: return launch_snapkv_dm<D, 2>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);
-    case 3: return launch_snapkv_dm<D, 3>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);
-    case 4: return launch_snapkv_dm<D, 4>(k, hs, B, Hkv, S, w, scores, stats, nchunk, st);
+    case 1: return launch_snapkv_dm<D, 1>(k, hs, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st);
+    case 2: return launch_snapkv_dm<D, 2>(k, hs, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st);
+    case 3: return launch_snapkv_dm<D, 3>(k, hs, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st);
+    case 4: return launch_snapkv_dm<D, 4>(k, hs, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, int n_sink, int* idx,
-                        cudaStream_t st) {
+                        const int* fail, cudaStream_t st) {
   if (budget < S && S >= 4096 && (S + kTopkCluster - 1) / kTopkCluster <= kTopkClusterMaxChunk) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kTopkCluster, B * Hkv);
@@ -677,7 +859,7 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, S, budget, n_sink, idx);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, S, budget, n_sink, idx, fail);
     note_launch();
     return e;
   }
@@ -688,22 +870,25 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
                                 kTopkSmemKeys * (int)sizeof(float));
   });
   if (e != cudaSuccess) return e;
-  topk_kernel<<<B * Hkv, 1024, smem, st>>>(scores, S, budget, n_sink, idx);
+  topk_kernel<<<B * Hkv, 1024, smem, st>>>(scores, S, budget, n_sink, idx, fail);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, int S, int D, int w, int budget,
-                          int n_sink, float* scores, int* idx, float2* stats, int nchunk, cudaStream_t st) {
+                          int n_sink, float* scores, int* idx, float2* stats, int nchunk, unsigned* arrive,
+                          cudaStream_t st) {
+  // the failure flag sits after the B * Hkv arrival counts
+  int* fail = reinterpret_cast<int*>(arrive + (size_t)B * Hkv);
   cudaError_t e;
   switch (D) {
-    case 32: e = launch_snapkv_d<32>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, st); break;
-    case 64: e = launch_snapkv_d<64>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, st); break;
-    case 128: e = launch_snapkv_d<128>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, st); break;
+    case 32: e = launch_snapkv_d<32>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st); break;
+    case 64: e = launch_snapkv_d<64>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st); break;
+    case 128: e = launch_snapkv_d<128>(k, head_stride, B, Hkv, S, w, scores, stats, nchunk, arrive, fail, st); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch_topk(scores, B, Hkv, S, budget, n_sink, idx, st);
+  return launch_topk(scores, B, Hkv, S, budget, n_sink, idx, fail, st);
 }
 
 }  // namespace kvq

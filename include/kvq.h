@@ -359,7 +359,11 @@ size_t snapkv_workspace_bytes(int32_t batch, int32_t n_kv_heads, int32_t S, int3
    first), ascending.  scores_out: device fp32 [B, Hkv, S] or NULL; idx_out: device
    int32 [B, Hkv, min(budget, S)].  n_sink > budget -> INVALID_ARG.
    obs_window in 1..64, head_dim in {32, 64, 128}, S >= 1; k 8-byte aligned
-   (INVALID_ARG otherwise). */
+   (INVALID_ARG otherwise).  When every scoring CTA fits on the device at once
+   the scores come from one cooperative launch whose CTAs of a head wait for
+   one another (bounded, ~200 ms); should that wait ever run out, every index
+   of that call is -1.  Calls that overlap on the GPU must not share a
+   workspace. */
 kvq_status snapkv_select(const void* k, int64_t head_stride, int32_t batch, int32_t n_kv_heads, int32_t S,
                          int32_t head_dim, int32_t obs_window, int32_t budget, int32_t n_sink,
                          float* scores_out, int32_t* idx_out, void* workspace, size_t ws_bytes,

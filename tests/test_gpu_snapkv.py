@@ -247,3 +247,17 @@ def test_chunked_prefill_reenforces_budget(kvq):
         assert st.stored == oc.stored == min(stored, budget)
         assert st.pos == pos
         assert_cache_equal(cache, oc, f"chunk {i}")
+
+
+def test_one_pass_and_two_pass_scores_are_the_same_bits(kvq):
+    # 8 heads of a 16K prompt fit on the device at once: the scores come from
+    # the one-pass cooperative launch.  The same keys as batch row 0 of an
+    # 8-row batch (4096 scoring CTAs, more than the device holds at once) take
+    # the two-pass path.  Both compute every logit and statistic in the same
+    # order, so row 0's scores and indices must agree bit for bit.
+    k = _keys(1, 8, 16384, 128, 51)
+    kd = k.cuda()
+    s1, i1 = kvq.snapkv(kd, 32, 512, 4)
+    kb = torch.cat([kd] + [_keys(1, 8, 16384, 128, 52 + j).cuda() for j in range(7)], dim=0)
+    s8, i8 = kvq.snapkv(kb, 32, 512, 4)
+    assert torch.equal(s1[0], s8[0]) and torch.equal(i1[0], i8[0])
