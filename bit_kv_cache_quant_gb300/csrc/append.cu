@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(256) recompute_kivi_kernel(CacheView c, const 
 // on them).  With more than one CTA the last to arrive advances the counters,
 // once every CTA has read them; a one-CTA append advances them directly.
 constexpr int kAppendWarps = 8;
+constexpr int kAppendCtasPerSm = 8;
 
 template <typename T, int E>
 __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, const T* __restrict__ k,
@@ -158,18 +159,22 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
   __shared__ int s_ok;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kAppendWarps + warp;
+  const long long stride = (long long)gridDim.x * kAppendWarps;   // rows per sweep of the grid
+  long long row = (long long)blockIdx.x * kAppendWarps + warp;
+  // token row % n of (b, kv head) row / n sits at row (row / n) * hstride + row % n of the input;
+  // rows < B * Hkv * cap_alloc < 2^31 (the layout refuses larger caches), so 32-bit division suffices
+  auto load = [&](long long r, float (&xk)[E], float (&xv)[E]) {
+    const unsigned q = (unsigned)r / (unsigned)n, i = (unsigned)r % (unsigned)n;
+    const long long src = (long long)q * hstride + i;
+    load_row_slice<T, E>(k + src * c.D + lane * E, xk);
+    load_row_slice<T, E>(v + src * c.D + lane * E, xv);
+  };
   // launched as a programmatic dependent: the inputs and counters may come
   // from the previous kernel; the next launch may start its prologue now
   grid_dependency_wait();
   grid_launch_dependents();
   float xk[E], xv[E];
-  if (row < rows) {
-    // token row % n of (b, kv head) row / n sits at row (row / n) * hstride + row % n of the input
-    const long long src = (row / n) * hstride + row % n;
-    load_row_slice<T, E>(k + src * c.D + lane * E, xk);
-    load_row_slice<T, E>(v + src * c.D + lane * E, xv);
-  }
+  if (row < rows) load(row, xk, xv);
   if (threadIdx.x == 0) {
     s_pos = c.state->pos;
     s_stored = c.state->stored;
@@ -178,10 +183,16 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
     if (!ok && blockIdx.x == 0) set_status(c.state, KVQ_DEV_OVERFLOW);
   }
   __syncthreads();
-  if (s_ok && row < rows) {
-    const int i = (int)(row % n);
-    const long long bh = row / n;
-    const int kvh = (int)(bh % c.Hkv);
+  // a warp codes rows row, row + stride, ...: the grid is capped at a few
+  // CTAs per SM (one arrival each on the append counter), and each warp
+  // requests its next row before coding the current one
+  for (; s_ok && row < rows; row += stride) {
+    float nk[E], nv[E];
+    const bool more = row + stride < rows;
+    if (more) load(row + stride, nk, nv);
+    const int i = (int)((unsigned)row % (unsigned)n);
+    const long long bh = (unsigned)row / (unsigned)n;
+    const int kvh = (int)((unsigned)bh % (unsigned)c.Hkv);
     const long long p = s_pos + i;
     bool write = true;
     int slot;
@@ -200,6 +211,13 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
       const float* bias = c.k_bias ? c.k_bias + (size_t)kvh * c.D : nullptr;
       quantize_row<E>(c.k, bias, xk, bh, c.cap_alloc, slot, lane);
       quantize_row<E>(c.v, nullptr, xv, bh, c.cap_alloc, slot, lane);
+    }
+    if (more) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        xk[e] = nk[e];
+        xv[e] = nv[e];
+      }
     }
   }
   __syncthreads();
@@ -386,7 +404,10 @@ static cudaError_t launch_append_t(const CacheView& c, const void* k, const void
     return cudaGetLastError();
   }
   const long long rows = (long long)c.B * c.Hkv * n;
-  const unsigned grid = (unsigned)((rows + kAppendWarps - 1) / kAppendWarps);
+  // at most kAppendCtasPerSm CTAs per SM; their warps sweep the rows
+  const long long need = (rows + kAppendWarps - 1) / kAppendWarps;
+  const long long cap = (long long)kAppendCtasPerSm * (c.sms > 0 ? c.sms : 132);
+  const unsigned grid = (unsigned)(need < cap ? need : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(32 * kAppendWarps);

@@ -391,6 +391,7 @@ kvq_status kvq_cache_init(const kvq_config* cfg, void* dev_mem, size_t bytes, cu
   v.layout = cfg->layout;
   v.sink = cfg->sink;
   v.window = cfg->window;
+  v.sms = sms;
   {
     const size_t rows = (size_t)cfg->batch * cfg->n_kv_heads * lay.cap_alloc;
     v.has_maps = cfg->head_dim >= 64 && encode_rows_map(&v.kmap, b + lay.k_codes, rows, lay.k_row_bytes) &&

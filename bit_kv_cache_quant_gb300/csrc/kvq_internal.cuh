@@ -74,6 +74,7 @@ struct CacheView {
   float* tail_v;
   int B, Hkv, D, cap, cap_alloc, layout, sink, window;
   int has_maps;
+  int sms;               // SMs of the device the cache was bound on
 };
 
 // Programmatic dependent launch: wait until the grids this launch depends on
@@ -133,11 +134,36 @@ __device__ __forceinline__ int affine_code(float x, float scale, float zero, flo
   return (int)u;
 }
 
+// affine_code from inv = 1 / scale (rounded once per group): q = (x - zero) * inv
+// is within 2^-23 of (x - zero) / scale relative to it, so wherever the
+// clamped code depends on the quotient (|quotient| <= 256) q is within 2^-14 of
+// it and rint(q) == rint(quotient) unless q lies within 2^-12 of a
+// half-integer; only there (rarely) does the exact division decide.  Larger
+// quotients clamp to the same code either way; NaN and infinities take the
+// same path as in affine_code.  Bit-identical to affine_code.
+__device__ __forceinline__ int affine_code_inv(float x, float scale, float inv, float zero, float levels) {
+  const float d = __fsub_rn(x, zero);
+  float t = __fmul_rn(d, inv);
+  if (fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f)) < 0x1p-12f) t = __fdiv_rn(d, scale);
+  const float u = fminf(fmaxf(rintf(t), 0.0f), levels);
+  return (int)u;
+}
+
 // Symmetric Q4_0 nibble: d == 0 stores level 0 (nibble 8).
 __device__ __forceinline__ int q40_code(float x, float d) {
   if (d == 0.0f) return 8;
   float t = __fdiv_rn(x, d);
   float q = fminf(fmaxf(rintf(t), -8.0f), 7.0f);
+  return (int)q + 8;
+}
+
+// q40_code from inv = 1 / d, by the argument of affine_code_inv (quotients
+// that matter are within [-9, 8]).  Bit-identical to q40_code.
+__device__ __forceinline__ int q40_code_inv(float x, float d, float inv) {
+  if (d == 0.0f) return 8;
+  float t = __fmul_rn(x, inv);
+  if (fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f)) < 0x1p-12f) t = __fdiv_rn(x, d);
+  const float q = fminf(fmaxf(rintf(t), -8.0f), 7.0f);
   return (int)q + 8;
 }
 

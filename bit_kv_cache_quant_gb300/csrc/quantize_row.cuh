@@ -110,8 +110,9 @@ __device__ __forceinline__ void quantize_row_dq(const SideView& s, const float* 
     mn = group_min(mn, width);
     mx = group_max(mx, width);
     const float sc = affine_scale(mn, mx, levels);
+    const float inv = __frcp_rn(sc);
 #pragma unroll
-    for (int i = 0; i < E; ++i) u[i] = affine_code(x[i], sc, mn, levels);
+    for (int i = 0; i < E; ++i) u[i] = affine_code_inv(x[i], sc, inv, mn, levels);
     store_codes<E>(row, lane, s.bits, u);
     const __half s16 = __float2half_rn(sc), z16 = __float2half_rn(mn);
     if (lane % width == 0) {
@@ -137,8 +138,9 @@ __device__ __forceinline__ void quantize_row_dq(const SideView& s, const float* 
   for (int i = 1; i < E; ++i) a = fmaxf(a, fabsf(x[i]));
   a = group_max(a, width);
   const float d = __fdiv_rn(a, 7.0f);
+  const float dinv = __frcp_rn(d);   // inf when d == 0 (q40_code_inv does not use it then)
 #pragma unroll
-  for (int i = 0; i < E; ++i) u[i] = q40_code(x[i], d);
+  for (int i = 0; i < E; ++i) u[i] = q40_code_inv(x[i], d, dinv);
   store_codes<E>(row, lane, 4, u);
   const __half d16 = __float2half_rn(d);
   if (lane % width == 0) s.tok_scale[meta_row + lane / width] = d16;
