@@ -50,6 +50,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (profiling small footprints; not a bench line)")
+    p.add_argument("--floor", action="store_true",
+                   help="measure the per-launch floor of a chain of dependent launches that only read the "
+                        "default workload's per-layer decode bytes (probe/floor_probe.cu) and print it")
     p.add_argument("--separate-step", action="store_true",
                    help="run each layer's append, eviction and decode as separate launches even where the "
                         "library fuses them (kvq_append_decode), to compare the two")
@@ -596,17 +599,23 @@ def run_reference(a, rank, world):
 
 
 DECODE_SOURCES = ("kvq_internal.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh", "quantize_row.cuh")
+SNAPKV_SOURCES = ("kvq_internal.cuh", "snapkv.cu")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
-def decode_source_sha(kvq_dir):
-    """sha256 over the decode kernels' sources: a committed ncu figure holds only for these bytes."""
+def sources_sha(kvq_dir, names):
+    """sha256 over kernel sources (in order): a committed ncu figure holds only for these bytes."""
     import hashlib
 
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         with open(os.path.join(kvq_dir, "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def decode_source_sha(kvq_dir):
+    return sources_sha(kvq_dir, DECODE_SOURCES)
 
 
 def decode_kernel_name(w):
@@ -615,17 +624,50 @@ def decode_kernel_name(w):
     return "decode_tc_kernel" if tc else "decode_kernel"
 
 
-def decode_traffic(w, kvq_dir):
-    """DRAM bytes per decode launch from the committed ncu summary, if it matches this kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if not os.path.exists(path):
+def profile_traffic(name, kvq_dir):
+    """DRAM bytes per launch of the dominant kernel of workload `name` from the committed ncu summary
+    (profiles/dram_traffic.json), if it was taken on the current sources of that kernel; else None."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
-    with open(path) as f:
+    with open(TRAFFIC_JSON) as f:
         d = json.load(f)
-    entry = d.get(w.name)
-    if not entry or entry.get("kernel_source_sha256") != decode_source_sha(kvq_dir):
+    entry = d.get(name)
+    if not entry:
+        return None
+    names = tuple(entry.get("sources", DECODE_SOURCES))
+    if entry.get("sources_sha256") != sources_sha(kvq_dir, names):
         return None
     return entry.get("dram_bytes_per_launch")
+
+
+def decode_traffic(w, kvq_dir):
+    return profile_traffic(w.name, kvq_dir)
+
+
+def run_floor(a):
+    """Builds and runs probe/floor_probe.cu for the default workload's layer count and decode bytes
+    per layer; prints its JSON lines and one summary line."""
+    import importlib.util
+
+    pkg = os.path.join(ROOT, "bit_kv_cache_quant_gb300")
+    src = os.path.join(pkg, "probe", "floor_probe.cu")
+    exe = os.path.join(pkg, "_build", "floor_probe")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
+        spec = importlib.util.spec_from_file_location("kvq_build", os.path.join(pkg, "build.py"))
+        build = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(build)
+        subprocess.run([build._nvcc(), *build.ARCH, "-O3", "-std=c++17", src, "-o", exe], check=True)
+    w = synth.get_workload(DEFAULT_WORKLOAD)
+    nbytes = decode_bytes(w, w.context)
+    out = subprocess.run([exe, str(w.layers), str(nbytes)], capture_output=True, text=True, check=True).stdout
+    rows = [json.loads(x) for x in out.splitlines() if x.startswith("{")]
+    for r in rows:
+        print(json.dumps(r))
+    best = {m: min((r for r in rows if r["mode"] == m), key=lambda r: r["us_per_launch"])
+            for m in {r["mode"] for r in rows}}
+    print(json.dumps({"floor": w.name, "layers": w.layers, "bytes_per_launch": nbytes,
+                      "best_us_per_launch": {str(m): best[m]["us_per_launch"] for m in sorted(best)}}))
 
 
 # -------------------------------------------------------------------- main --
@@ -888,7 +930,8 @@ def bench_snapkv(a, kvq, w, rank, world):
             "decode_steps_per_s": world * w.decode_steps * a.steps / t,
             "gpu_launches": ep.launches * a.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None, "kernel": "snapkv_select (one-pass scoring + top-k)",
+                         "traffic": profile_traffic(w.name, os.path.dirname(kvq.__file__)),
+                         "kernel": "snapkv_select (one-pass scoring + top-k)",
                          "bytes_per_launch": sel_b, "avg_launch_us": t_sel * 1e6,
                          "peak_kind": f"{peak_kind} copy bandwidth"},
             "clocks": clk}
@@ -950,7 +993,8 @@ def per_config(a, kvq):
             out[w.name] = {"value": ln["value"], "unit": ln["unit"], "ms_per_step": ln["ms_per_step"],
                            "steps": sub.steps, "decode_steps_per_s": ln.get("decode_steps_per_s"),
                            "roofline_kernel": r.get("kernel"), "kernel_us": r.get("avg_launch_us"),
-                           "frac": r["frac"], "clocks": ln.get("clocks")}
+                           "bytes_per_launch": r.get("bytes_per_launch"), "frac": r["frac"],
+                           "traffic": r.get("traffic"), "clocks": ln.get("clocks")}
             for key in ("snapkv_select_us", "convert", "recompute_k_append"):
                 if key in ln:
                     out[w.name][key] = ln[key]
@@ -963,6 +1007,9 @@ def per_config(a, kvq):
 
 def main(argv=None):
     a = parse_args(argv)
+    if a.floor:
+        run_floor(a)
+        return
     rank, world, local = dist_env()
     if a.impl == "reference":
         run_reference(a, rank, world)

@@ -29,7 +29,12 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
 
 // Eight nibbles of w (channel i in bits 4i..4i+3) as exact fp16 pairs:
 // h[0] = (c0, c4), h[1] = (c1, c5), h[2] = (c2, c6), h[3] = (c3, c7).
-// 0x6400 | n is 1024 + n; 0x6400 | (n << 4) is 1024 + 16 n.  OFF = 8 gives the
+// This is the exponent-bias ("magic number") integer-to-fp16 conversion of
+// weight-only quantised GEMM kernels (Kim et al., "Who Says Elephants Can't
+// Run", 2022): an fp16 with exponent field 25 (bits 0x6400) has a mantissa
+// step of exactly 1 over [1024, 2048), so ORing a small integer n into the
+// mantissa gives the fp16 1024 + n, and 0x6400 | (n << 4) gives 1024 + 16 n;
+// one subtraction (or fma by 1/16) leaves n exactly.  OFF = 8 gives the
 // signed levels n - 8 (Q4_0) instead.
 template <int OFF = 0>
 __device__ __forceinline__ void nibbles_to_h2(uint32_t w, __half2 (&h)[4]) {
@@ -70,7 +75,8 @@ __device__ __forceinline__ void load_halves(const uint8_t* p, float (&f)[N]) {
   }
 }
 
-// Four unsigned bytes of x as exact fp16 pairs: lo = (b0, b1), hi = (b2, b3).
+// Four unsigned bytes of x as exact fp16 pairs: lo = (b0, b1), hi = (b2, b3),
+// by the same exponent-bias conversion (byte b in the mantissa of 1024).
 __device__ __forceinline__ void bytes_to_h2(uint32_t x, __half2& lo, __half2& hi) {
   const __half2 k1024 = u2h(0x64006400u);
   lo = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x5140u)), k1024);
