@@ -598,7 +598,8 @@ def run_reference(a, rank, world):
     print(json.dumps(line))
 
 
-DECODE_SOURCES = ("kvq_internal.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh", "quantize_row.cuh")
+DECODE_SOURCES = ("kvq_internal.cuh", "async_copy.cuh", "decode_impl.cuh", "decode_tc_frag.cuh", "decode_tc.cuh",
+                  "quantize_row.cuh")
 SNAPKV_SOURCES = ("kvq_internal.cuh", "snapkv.cu")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
 

@@ -8,6 +8,7 @@
 // (bounded in time) before reading the stage.
 #pragma once
 
+#include "async_copy.cuh"
 #include "decode_impl.cuh"
 
 namespace kvq {
@@ -120,53 +121,7 @@ __device__ __forceinline__ int swz_off(int r, int off) {
   }
 }
 
-// --------------------------------------------------------- mbarrier / TMA --
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(m)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(smem_u32(m)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Waits for phase `parity` of the mbarrier, giving up after kWaitNs (~200 ms;
-// a stage normally completes in microseconds); false means the wait ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity) {
-  if (mbar_try_wait(m, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(m, parity)) {
-    if (global_ns() - t0 > kWaitNs) return false;
-  }
-  return true;
-}
-
-// Shared-memory add with acquire-release semantics at CTA scope; returns the old value.
-__device__ __forceinline__ unsigned atom_add_acq_rel_cta(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// ------------------------------------------------------------------- TMA --
 
 // 64 rows of a code plane starting at row y (TMA tensor copy, swizzled).
 template <int ROWB>
@@ -184,15 +139,6 @@ __device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, int 
         "l"(map), "r"(0), "r"(y), "r"(smem_u32(m))
         : "memory");
   }
-}
-
-// Contiguous bytes (16-byte aligned, a multiple of 16) into shared memory.
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(m))
-      : "memory");
 }
 
 // Shared-memory ring of NSTAGE tile stages, in one of two layouts.

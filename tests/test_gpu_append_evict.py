@@ -113,6 +113,78 @@ def test_overflow_sets_status_and_writes_nothing(kvq):
     assert cache.stats().device_status == 0
 
 
+@pytest.mark.parametrize("fmt", [FORMATS[2], FORMATS[4], FORMATS[6]], ids=["kivi4", "aff4", "q40-int8"])
+def test_bulk_append_many_chunks_per_cta(kvq, fmt):
+    """A prefill long enough that every CTA of the staged bulk append cycles its
+    shared-memory stages several times, with a ragged last chunk per (b, kv head)."""
+    kf, kb, kg, vf, vb, vg = fmt
+    B, H, D, n = 4, 8, 128, 4096 + 17
+    bias = None
+    if kf == "q4_0":
+        bias = (torch.randn(H, D, generator=torch.Generator().manual_seed(41)) * 1.5).float()
+    cache = kvq.KVCache(B, H, D, n + 8, kf, kb, kg, vf, vb, vg, k_bias=None if bias is None else bias.cuda())
+    oc = OracleCache(oracle_spec(cache, None if bias is None else bias.numpy()))
+    k = _inputs((B, H, n, D), 42, torch.bfloat16)
+    v = _inputs((B, H, n, D), 43, torch.bfloat16, 0.0)
+    calibrate = kf == "kivi_chan"
+    cache.append(k.cuda(), v.cuda(), calibrate_k=calibrate)
+    if calibrate:
+        oc.calibrate_k(host(k))
+    oc.append(host(k), host(v))
+    assert_cache_equal(cache, oc, "bulk append, many chunks per CTA")
+
+
+@pytest.mark.parametrize("fmt", [FORMATS[2], FORMATS[6]], ids=["kivi4", "q40-int8"])
+def test_misaligned_input_takes_the_per_row_kernel_with_the_same_bytes(kvq, fmt):
+    """Inputs that do not start on a 16-byte boundary cannot be staged by bulk copies or
+    read as 16-byte vectors; the append (and the KIVI calibration) read them element by
+    element instead, to the same bytes."""
+    kf, kb, kg, vf, vb, vg = fmt
+    B, H, D, n = 2, 4, 128, 300
+    k = _inputs((B, H, n, D), 44, torch.bfloat16).cuda()
+    v = _inputs((B, H, n, D), 45, torch.bfloat16, 0.0).cuda()
+    shifted = []
+    for x in (k, v):
+        flat = torch.empty(x.numel() + 4, dtype=x.dtype, device="cuda")
+        y = flat[4:].view(x.shape)
+        y.copy_(x)
+        assert y.data_ptr() % 16 == 8
+        shifted.append(y)
+    bias = None
+    if kf == "q4_0":
+        bias = (torch.randn(H, D, generator=torch.Generator().manual_seed(46)) * 1.5).float().cuda()
+    a = kvq.KVCache(B, H, D, n + 8, kf, kb, kg, vf, vb, vg, k_bias=bias)
+    b = kvq.KVCache(B, H, D, n + 8, kf, kb, kg, vf, vb, vg, k_bias=bias)
+    calibrate = kf == "kivi_chan"
+    a.append(k, v, calibrate_k=calibrate)
+    b.append(*shifted, calibrate_k=calibrate)
+    pa, pb = gpu_planes(a), gpu_planes(b)
+    assert pa["stored"] == pb["stored"] == n
+    for name in ("k_rows", "v_rows"):
+        np.testing.assert_array_equal(pa[name][:, :, :n], pb[name][:, :, :n])
+    for name in ("k_tok_scale", "v_tok_scale", "v_tok_zero"):
+        if name in pa:
+            np.testing.assert_array_equal(pa[name][:, :, :n].view(np.uint16), pb[name][:, :, :n].view(np.uint16))
+    for name in ("k_ch_scale32", "k_ch_zero32"):
+        if name in pa:
+            np.testing.assert_array_equal(pa[name], pb[name])
+
+
+def test_bulk_append_overflow_writes_nothing(kvq):
+    cache = kvq.KVCache(1, 2, 128, 40, "affine_token", 4, 64, "affine_token", 4, 64)
+    k = _inputs((1, 2, 8, 128), 47, torch.bfloat16)
+    cache.append(k.cuda(), k.cuda())
+    before = gpu_planes(cache)
+    big = _inputs((1, 2, 33, 128), 48, torch.bfloat16)    # a whole bulk chunk and more, past the capacity
+    cache.append(big.cuda(), big.cuda())
+    after = gpu_planes(cache)
+    assert after["status"] == kvq.DEV_OVERFLOW
+    assert after["stored"] == 8 and after["pos"] == 8
+    np.testing.assert_array_equal(before["k_rows"], after["k_rows"])
+    np.testing.assert_array_equal(before["v_rows"], after["v_rows"])
+    kvq.kvq_clear_status(cache.handle)
+
+
 def test_uncalibrated_kivi_append_rejected(kvq):
     cache = kvq.KVCache(1, 1, 32, 16, "kivi_chan", 8, 0, "affine_token", 8, 32)
     k = torch.randn(1, 1, 2, 32, device="cuda")
