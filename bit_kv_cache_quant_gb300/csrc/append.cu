@@ -452,65 +452,91 @@ __device__ __forceinline__ void code_side(const SideView& sv, float (&x)[kPart],
     const float* psc = kp.sc + part * kPart;
     const float* pinv = kp.inv + part * kPart;
     const float* pzr = kp.zr + part * kPart;
-    // codes packed per unit in register order: 8-bit one byte per code (signed
-    // level u - 128), 4-bit one nibble (channel 2i low)
-    uint32_t w[kPart * BITS / 32];
-#pragma unroll
-    for (int i = 0; i < kPart * BITS / 32; ++i) w[i] = 0u;
+    // Rounding: adding MAGIC = 1.5 * 2^23 + OFF to a value v in [-2^21, 2^21]
+    // rounds it to the nearest integer, ties to even, and leaves OFF + rint(v)
+    // in the low bits of the sum; OFF = 8 gives the Q4_0 nibble u + 8, OFF =
+    // -128 the int8 byte u ^ 0x80 (the signed level u - 128), OFF = 0 the
+    // 4-bit code.  The quotient is first clamped to the level range where it
+    // can leave it: per-channel KIVI scales come from a calibration that later
+    // tokens may exceed; a per-token group's own range bounds its quotients to
+    // [0, levels (1 + 2^-22)] and a Q4_0 block's to [-7 (1 + 2^-22), 7 (1 +
+    // 2^-22)], so there only NaN (from non-finite inputs) needs the lower
+    // clamp, which maps it to the level the exact rule gives it.  Rounding the
+    // clamped value equals clamping the rounded one: the bounds are integers.
+    constexpr float OFF = Q40 ? 8.0f : (BITS == 8 ? -128.0f : 0.0f);
+    constexpr float MAGIC = 0x1.8p23f + OFF;
+    auto clamp = [&](float t) { return CHAN ? fminf(fmaxf(t, LO), HI) : fmaxf(t, LO); };
+    uint8_t* o = out + part * (kPart * BITS / 8);
+    constexpr int UB = S::UE * BITS / 8;   // bytes per unit: 2, 4 or 8
 #pragma unroll
     for (int jj = 0; jj < S::NU; ++jj) {
       const int uu = (jj + rot) % S::NU;
       [[maybe_unused]] const bool second = G16 && uu * S::UE >= 16;
+      float y[S::UE], dd[S::UE];
+      float far = 0.0f;   // the unit's largest distance of a rounded quotient from its integer
 #pragma unroll
       for (int e = 0; e < S::UE; ++e) {
-        const int kk = jj * S::UE + e;
-        float d, inv, sc;
+        float inv;
         if constexpr (Q40) {
-          d = x[kk];
+          dd[e] = x[jj * S::UE + e];
           inv = i0;
-          sc = s0;
         } else if constexpr (CHAN) {
-          d = __fsub_rn(x[kk], pzr[uu * S::UE + e]);
+          dd[e] = __fsub_rn(x[jj * S::UE + e], pzr[uu * S::UE + e]);
           inv = pinv[uu * S::UE + e];
-          sc = psc[uu * S::UE + e];
         } else {
-          d = __fsub_rn(x[kk], second ? z1 : z0);
+          dd[e] = __fsub_rn(x[jj * S::UE + e], second ? z1 : z0);
           inv = second ? i1 : i0;
-          sc = second ? s1 : s0;
         }
-        // the clamped quotient rounded to an integer by adding 1.5 * 2^23
-        // (round-to-nearest-even, exact for |value| < 2^22; the code is then
-        // the low bits of the sum); rounding the clamped value equals
-        // clamping the rounded one because the bounds are integers
-        float tc = fminf(fmaxf(__fmul_rn(d, inv), LO), HI);
-        float y = __fadd_rn(tc, 0x1.8p23f);
-        if (fabsf(__fsub_rn(tc, __fsub_rn(y, 0x1.8p23f))) > 0.5f - 0x1p-13f) {
-          // within 2^-13 of a tie inside the range: the exact quotient decides
-          // (the reciprocal's quotient is within 2^-15 of it for |quotient| <= 256)
-          tc = fminf(fmaxf(__fdiv_rn(d, sc), LO), HI);
-          y = __fadd_rn(tc, 0x1.8p23f);
+        const float tc = clamp(__fmul_rn(dd[e], inv));
+        y[e] = __fadd_rn(tc, MAGIC);
+        far = fmaxf(far, fabsf(__fsub_rn(tc, __fsub_rn(y[e], MAGIC))));
+      }
+      if (far > 0.5f - 0x1p-13f) {
+        // a quotient within 2^-13 of a tie: there the exact quotient decides
+        // (the reciprocal's is within 2^-15 of it for |quotient| <= 256)
+#pragma unroll
+        for (int e = 0; e < S::UE; ++e) {
+          float sc, inv;
+          if constexpr (Q40) {
+            sc = s0;
+            inv = i0;
+          } else if constexpr (CHAN) {
+            sc = psc[uu * S::UE + e];
+            inv = pinv[uu * S::UE + e];
+          } else {
+            sc = second ? s1 : s0;
+            inv = second ? i1 : i0;
+          }
+          const float tc = clamp(__fmul_rn(dd[e], inv));
+          if (fabsf(__fsub_rn(tc, __fsub_rn(y[e], MAGIC))) > 0.5f - 0x1p-13f)
+            y[e] = __fadd_rn(clamp(__fdiv_rn(dd[e], sc)), MAGIC);
         }
-        const int code = __float_as_int(y) - 0x4B400000 + (Q40 ? 8 : 0);
-        if constexpr (BITS == 8) w[kk >> 2] |= (uint32_t)((code ^ 0x80) & 0xff) << (8 * (kk & 3));
-        else w[kk >> 3] |= (uint32_t)code << (4 * (kk & 7));
       }
-    }
-    if constexpr (Q40) {
-      if (s0 == 0.0f) {   // an all-zero block stores level 0 (nibble 8) throughout
+      if constexpr (Q40) {
+        if (s0 == 0.0f) {   // an all-zero block stores level 0 (nibble 8) throughout
 #pragma unroll
-        for (int i = 0; i < kPart * BITS / 32; ++i) w[i] = 0x88888888u;
+          for (int e = 0; e < S::UE; ++e) y[e] = MAGIC;
+        }
       }
-    }
-    // each unit's codes at the unit's own offset
-    constexpr int UB = S::UE * BITS / 8;   // bytes per unit: 2, 4 or 8
-    uint8_t* o = out + part * (kPart * BITS / 8);
+      // the low byte of each sum is the stored byte (8-bit) or nibble (4-bit)
+      uint32_t b[S::UE / 4];
 #pragma unroll
-    for (int jj = 0; jj < S::NU; ++jj) {
-      uint8_t* dst = o + ((jj + rot) % S::NU) * UB;
-      const int kk = jj * S::UE;   // first register slot of the unit
-      if constexpr (UB == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[kk >> 2], w[(kk >> 2) + 1]);
-      else if constexpr (UB == 4) *reinterpret_cast<uint32_t*>(dst) = BITS == 8 ? w[kk >> 2] : w[kk >> 3];
-      else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(w[kk >> 3] >> (4 * (kk & 7)));
+      for (int q = 0; q < S::UE / 4; ++q) {
+        const uint32_t lo = __byte_perm(__float_as_uint(y[4 * q]), __float_as_uint(y[4 * q + 1]), 0x0040);
+        const uint32_t hi = __byte_perm(__float_as_uint(y[4 * q + 2]), __float_as_uint(y[4 * q + 3]), 0x0040);
+        b[q] = __byte_perm(lo, hi, 0x5410);
+      }
+      uint8_t* dst = o + uu * UB;
+      if constexpr (BITS == 8) {
+        if constexpr (UB == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(b[0], b[1]);
+        else *reinterpret_cast<uint32_t*>(dst) = b[0];
+      } else {
+        // bytes c0..c3 (each < 16) -> nibble pairs c0 | c1 << 4 and c2 | c3 << 4 in bytes 0 and 2
+#pragma unroll
+        for (int q = 0; q < S::UE / 4; ++q) b[q] |= b[q] >> 4;
+        if constexpr (UB == 4) *reinterpret_cast<uint32_t*>(dst) = __byte_perm(b[0], b[1], 0x6420);
+        else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)__byte_perm(b[0], 0u, 0x0020);
+      }
     }
   }
 }
@@ -622,8 +648,7 @@ __global__ void __launch_bounds__(kBulkThreads) append_bulk_kernel(CacheView c, 
 #pragma unroll
         for (int e = 0; e < S::UE; ++e) x[jj * S::UE + e] = In<T>::ld(&t[e]);
       }
-      if (side == 0) code_side_any<T>(kind_k, c.k, x, rot, part, lane, orow, bias, s_kp);
-      else code_side_any<T>(kind_v, c.v, x, rot, part, lane, orow, bias, s_kp);
+      code_side_any<T>(side == 0 ? kind_k : kind_v, side == 0 ? c.k : c.v, x, rot, part, lane, orow, bias, s_kp);
     }
   }
   __syncthreads();
