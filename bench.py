@@ -187,21 +187,19 @@ class DecodeStep:
         self.fused = not separate and fused_step(kvq, w, self.caches[0].cfg, sms)
         self.launches_append = 0
         self.launches_decode = 0
+        self.layer_step = None
 
     def eager_step(self):
         """One step through the public API; returns the library's launch count."""
         if not self.fused:
             return self.eager_append() + self.eager_decode()
-        n = 0
-        # a layer's step follows another layer's (or, for layer 0, the previous step's last layer's):
-        # with more than one layer, the kernel before each call never writes that call's cache
-        early = len(self.caches) > 1
-        for layer, c in enumerate(self.caches):
-            c.launches = 0
-            c.append_decode(self.k1[layer], self.v1[layer], self.q[layer], out=self.out[layer], early_read=early)
-            n += c.launches
+        # one call for all layers; layer 0 follows the previous step's last layer (or the input
+        # copy), so with more than one layer the kernel before it never writes its cache
+        if self.layer_step is None:
+            self.layer_step = self.kvq.LayerStep(self.caches, self.k1, self.v1, self.q, self.out)
+        self.layer_step.run(early_read=len(self.caches) > 1)
         self.t_seen += 1
-        return n
+        return self.layer_step.launches
 
     def eager_append(self):
         n = 0
@@ -721,8 +719,9 @@ def bench_decode(a, kvq, w, rank, world):
         e_bytes, e_dt, h2d, d2h = e2e_decode(ds, max(3, min(a.steps, 200)), world)
         line["e2e"] = {"value": world * e_bytes / e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h,
-                       "how": "public Python API, eager calls per layer, pinned host inputs copied in and "
-                              "outputs read back every step (wall clock)"}
+                       "how": ("public Python API, " + ("one LayerStep call (kvq_append_decode_layers) per step"
+                                                          if ds.fused else "eager calls per layer")
+                               + ", pinned host inputs copied in and outputs read back every step (wall clock)")}
     return line
 
 

@@ -92,6 +92,9 @@ _proto("kvq_decode_attn", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int3
        c_void_p)
 _proto("kvq_append_decode", c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_int32,
        c_float, c_void_p, c_size_t, c_int32, c_void_p)
+_proto("kvq_append_decode_layers", c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p), c_int32,
+       POINTER(c_void_p), POINTER(c_void_p), c_int32, c_int32, c_float, POINTER(c_void_p), POINTER(c_size_t), c_int32,
+       c_void_p)
 _proto("kvq_test_stall_decode_tiles", None, c_int32)
 _proto("snapkv_workspace_bytes", c_size_t, c_int32, c_int32, c_int32, c_int32, c_int32)
 _proto("snapkv_pool", c_int32, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p)
@@ -202,6 +205,64 @@ def kvq_append_decode(cache, k: torch.Tensor, v: torch.Tensor, in_dtype: int, q:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.kvq_append_decode(cache, _dev_ptr(k), _dev_ptr(v), in_dtype, _dev_ptr(q), _dev_ptr(out), n_q_heads,
                                  io_dtype, softmax_scale, _dev_ptr(workspace), ws_bytes, flags, _stream(stream)))
+
+
+def kvq_append_decode_layers(caches: list, ks: list, vs: list, in_dtype: int, qs: list, outs: list, n_q_heads: int,
+                             io_dtype: int, softmax_scale: float = 0.0, workspaces: Optional[list] = None,
+                             flags: int = 0, stream=None) -> None:
+    n = len(caches)
+    arr = lambda xs: (c_void_p * n)(*xs)
+    ws = wsb = None
+    if workspaces is not None:
+        ws = arr([_dev_ptr(w) for w in workspaces])
+        wsb = (c_size_t * n)(*[0 if w is None else w.numel() * w.element_size() for w in workspaces])
+    _check(lib.kvq_append_decode_layers(n, arr([c.value for c in caches]), arr([_dev_ptr(t) for t in ks]),
+                                        arr([_dev_ptr(t) for t in vs]), in_dtype, arr([_dev_ptr(t) for t in qs]),
+                                        arr([_dev_ptr(t) for t in outs]), n_q_heads, io_dtype, softmax_scale, ws, wsb,
+                                        flags, _stream(stream)))
+
+
+class LayerStep:
+    """One decode step over a stack of layer caches as one call (kvq_append_decode_layers):
+    layer l appends ks[l], vs[l] [B, Hkv, 1, D] to caches[l], evicts, and attends with
+    qs[l] [B, Hq, D] into outs[l].  The per-layer pointer arrays are built once here, so the
+    tensors must stay alive and in place while the step is in use."""
+
+    def __init__(self, caches: list, ks: list, vs: list, qs: list, outs: list, softmax_scale: float = 0.0):
+        n = len(caches)
+        if not n or not all(len(x) == n for x in (ks, vs, qs, outs)):
+            raise ValueError("one k, v, q and out per cache")
+        for c, k, v, q, o in zip(caches, ks, vs, qs, outs):
+            c._check_rows(k, v)
+            if k.shape[2] != 1:
+                raise ValueError("a step takes one token per (batch row, kv head)")
+            if q.dim() != 3 or q.shape[0] != c.batch or q.shape[2] != c.head_dim or q.dtype not in DTYPES:
+                raise ValueError(f"q must be [{c.batch}, Hq, {c.head_dim}] fp32 / bf16 / fp16")
+            if o.shape != q.shape or o.dtype != q.dtype:
+                raise ValueError("out must have q's shape and dtype")
+        self.n = n
+        self.hq = qs[0].shape[1]
+        self.in_dtype, self.io_dtype = DTYPES[ks[0].dtype], DTYPES[qs[0].dtype]
+        self.softmax_scale = softmax_scale
+        ws = [c.workspace(self.hq) for c in caches]
+        arr = lambda xs: (c_void_p * n)(*xs)
+        self._args = (arr([c.handle.value for c in caches]), arr([_dev_ptr(t) for t in ks]),
+                      arr([_dev_ptr(t) for t in vs]), arr([_dev_ptr(t) for t in qs]),
+                      arr([_dev_ptr(t) for t in outs]), arr([_dev_ptr(w) for w in ws]),
+                      (c_size_t * n)(*[0 if w is None else w.numel() * w.element_size() for w in ws]))
+        self._keep = (list(caches), list(ks), list(vs), list(qs), list(outs), ws)
+        self._handles = tuple(c.handle for c in caches)   # the handle objects: reset() makes new ones
+        self.launches = 0
+
+    def run(self, early_read: bool = False, stream=None) -> None:
+        """early_read: the kernel just before this call on the stream writes none of the caches."""
+        if any(c.handle is not h for c, h in zip(self._keep[0], self._handles)):
+            raise ValueError("a cache of this step was reset or released; build a new LayerStep")
+        h, k, v, q, o, ws, wsb = self._args
+        _check(lib.kvq_append_decode_layers(self.n, h, k, v, self.in_dtype, q, o, self.hq, self.io_dtype,
+                                            self.softmax_scale, ws, wsb, STEP_EARLY_READ if early_read else 0,
+                                            _stream(stream)))
+        self.launches = kvq_last_launch_count()
 
 
 def kvq_test_stall_decode_tiles(on: bool) -> None:

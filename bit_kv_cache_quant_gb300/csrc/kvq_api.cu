@@ -611,10 +611,12 @@ kvq_status kvq_decode_attn(kvq_cache c, const void* q, void* out, int32_t n_q_he
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attn");
 }
 
-kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t in_dtype, const void* q, void* out,
+namespace {
+
+// One layer's step of kvq_append_decode (the counters of the call are the caller's).
+kvq_status append_decode_one(kvq_cache c, const void* k, const void* v, int32_t in_dtype, const void* q, void* out,
                              int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
                              size_t ws_bytes, int32_t flags, cudaStream_t stream) {
-  begin_call();
   kvq_status st = check_decode_args(c, q, out, n_q_heads, io_dtype, workspace, ws_bytes);
   if (st != KVQ_OK) return st;
   st = check_decode_pair(c, n_q_heads / c->cfg.n_kv_heads, io_dtype);
@@ -641,6 +643,45 @@ kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t 
   const cudaError_t e = launch_decode_any(c, q, out, n_q_heads, io_dtype, softmax_scale, workspace, nullptr, nullptr,
                                           0, false, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_append_decode");
+}
+
+}  // namespace
+
+kvq_status kvq_append_decode(kvq_cache c, const void* k, const void* v, int32_t in_dtype, const void* q, void* out,
+                             int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
+                             size_t ws_bytes, int32_t flags, cudaStream_t stream) {
+  begin_call();
+  return append_decode_one(c, k, v, in_dtype, q, out, n_q_heads, io_dtype, softmax_scale, workspace, ws_bytes, flags,
+                           stream);
+}
+
+kvq_status kvq_append_decode_layers(int32_t n_layers, const kvq_cache* caches, const void* const* k,
+                                    const void* const* v, int32_t in_dtype, const void* const* q, void* const* out,
+                                    int32_t n_q_heads, int32_t io_dtype, float softmax_scale,
+                                    void* const* workspace, const size_t* ws_bytes, int32_t flags,
+                                    cudaStream_t stream) {
+  begin_call();
+  if (n_layers < 1) return fail(KVQ_ERR_INVALID_ARG, "n_layers must be >= 1");
+  if (!caches || !k || !v || !q || !out) return fail(KVQ_ERR_INVALID_ARG, "null per-layer array");
+  if (flags & ~KVQ_STEP_EARLY_READ) return fail(KVQ_ERR_INVALID_ARG, "unknown step flags 0x%x", flags);
+  // layers after the first read their caches early (their predecessor on the
+  // stream is the previous layer's step, which writes only its own cache):
+  // that needs distinct caches
+  for (int32_t i = 0; i < n_layers; ++i)
+    for (int32_t j = 0; j < i; ++j)
+      if (caches[i] == caches[j]) return fail(KVQ_ERR_INVALID_ARG, "layers %d and %d share one cache", j, i);
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const kvq_status st =
+        append_decode_one(caches[l], k[l], v[l], in_dtype, q[l], out[l], n_q_heads, io_dtype, softmax_scale,
+                          workspace ? workspace[l] : nullptr, ws_bytes ? ws_bytes[l] : 0,
+                          l == 0 ? flags : (flags | KVQ_STEP_EARLY_READ), stream);
+    if (st != KVQ_OK) {
+      char msg[256];
+      snprintf(msg, sizeof(msg), "layer %d: %s", l, kvq_last_error());
+      return fail(st, "%s", msg);
+    }
+  }
+  return KVQ_OK;
 }
 
 void kvq_test_stall_decode_tiles(int32_t on) { g_stall_tx.store(on ? 16u : 0u, std::memory_order_relaxed); }

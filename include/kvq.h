@@ -127,7 +127,6 @@ typedef enum kvq_evict_mode {
 #define KVQ_DEV_OK 0
 #define KVQ_DEV_OVERFLOW 1         /* an append would pass the capacity; nothing was written */
 #define KVQ_DEV_BAD_KEEPSET 2      /* keep-set not strictly ascending or beyond stored rows */
-#define KVQ_STEP_EARLY_READ 1      /* kvq_append_decode flag (see there)                     */
 #define KVQ_DEV_TIMEOUT 3          /* a bounded wait inside a kernel ran out; outputs of that call
                                       are unspecified */
 
@@ -315,6 +314,26 @@ kvq_status kvq_decode_attn(kvq_cache cache, const void* q, void* out, int32_t n_
 kvq_status kvq_append_decode(kvq_cache cache, const void* k, const void* v, int32_t in_dtype, const void* q,
                              void* out, int32_t n_q_heads, int32_t io_dtype, float softmax_scale, void* workspace,
                              size_t ws_bytes, int32_t flags, cudaStream_t stream);
+
+/* One decode step of n_layers layers in one call: kvq_append_decode on caches[l]
+   with k[l], v[l], q[l], out[l] (and workspace[l] / ws_bytes[l] when the arrays
+   are given; NULL arrays mean no workspace for every layer), layer 0 first, all
+   on `stream`.  Every argument keeps kvq_append_decode's meaning and layout; the
+   arrays are host arrays of n_layers device pointers, read during the call only.
+   flags apply to layer 0; every later layer runs as if KVQ_STEP_EARLY_READ were
+   given, since the kernel just before it is the previous layer's step, which
+   writes only the previous layer's cache, so the caches must be distinct
+   (KVQ_ERR_INVALID_ARG otherwise, nothing enqueued).  Stops at the first layer
+   whose step fails and returns its status, with the layer named in
+   kvq_last_error(); the layers before it are enqueued.  This is the same step
+   as the StreamingLLM + KIVI page's per-layer loop in "Implementation"
+   (append, evict, attend, layer by layer), with one crossing of this boundary
+   per step instead of one per layer. */
+kvq_status kvq_append_decode_layers(int32_t n_layers, const kvq_cache* caches, const void* const* k,
+                                    const void* const* v, int32_t in_dtype, const void* const* q, void* const* out,
+                                    int32_t n_q_heads, int32_t io_dtype, float softmax_scale,
+                                    void* const* workspace, const size_t* ws_bytes, int32_t flags,
+                                    cudaStream_t stream);
 
 /* Test hook for the failure path of the tensor-core decode: while on (0 off,
    the default; process-wide, read at each launch), every CTA of the following

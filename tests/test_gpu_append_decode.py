@@ -190,3 +190,61 @@ def test_layers_in_turn_with_early_read(kvq, pair):
             assert_attention_close(out, oatt.decode_attention(host(q), kh, vh), f"early-read step {t}")
     for a, oc, _ in layers:
         assert_cache_equal(a, oc, "early-read cache")
+
+
+@pytest.mark.parametrize("pair", [PAIRS[4], PAIRS[6]], ids=["aff4", "q40v4"])
+def test_layer_step_one_call_matches_per_layer_calls(kvq, pair):
+    # kvq_append_decode_layers over four layers: the same outputs and cache
+    # bytes as four kvq_append_decode calls, and the oracle's attention.
+    B, H, D, G, T0, L, steps = 1, 8, 128, 3, 700, 4, 3
+    g = torch.Generator().manual_seed(31)
+    one, per, ocs, offs = [], [], [], []
+    for _ in range(L):
+        bias = _rand((H, D), g, torch.float32, 1.5) if pair[0] == "q4_0" else None
+        off = bias[None, :, None, :] if bias is not None else _rand((1, H, 1, D), g, torch.float32, 2.0)
+        a, b, oc = _pair_caches(kvq, pair, B, H, D, 1024, "linear", 0, 0, bias)
+        k0 = _rand((B, H, T0, D), g, torch.bfloat16, 1.0, off)
+        v0 = _rand((B, H, T0, D), g, torch.bfloat16)
+        for c in (a, b):
+            c.append(k0.cuda(), v0.cuda())
+        oc.append(host(k0), host(v0))
+        one.append(a), per.append(b), ocs.append(oc), offs.append(off)
+    ks = [torch.empty(B, H, 1, D, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vs = [torch.empty_like(k) for k in ks]
+    qs = [torch.empty(B, H * G, D, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    outs = [torch.empty_like(q) for q in qs]
+    step = kvq.LayerStep(one, ks, vs, qs, outs)
+    for t in range(steps):
+        inputs = []
+        for li in range(L):
+            k1 = _rand((B, H, 1, D), g, torch.bfloat16, 1.0, offs[li])
+            v1 = _rand((B, H, 1, D), g, torch.bfloat16)
+            q = _rand((B, H * G, D), g, torch.bfloat16)
+            ks[li].copy_(k1), vs[li].copy_(v1), qs[li].copy_(q)
+            inputs.append((k1, v1, q))
+        step.run()
+        assert step.launches == L
+        for li, (k1, v1, q) in enumerate(inputs):
+            ref_out = per[li].append_decode(k1.cuda(), v1.cuda(), q.cuda())
+            assert torch.equal(outs[li], ref_out), f"layer {li} step {t}: one call differs from per-layer calls"
+            ocs[li].append(host(k1), host(v1))
+            kh, vh = ocs[li].dequant()
+            assert_attention_close(outs[li], oatt.decode_attention(host(q), kh, vh), f"layer {li} step {t}")
+    for a, b, oc in zip(one, per, ocs):
+        assert_cache_equal(a, oc, "one-call cache")
+        assert_cache_equal(b, oc, "per-layer cache")
+
+
+def test_layer_step_rejects_a_shared_cache(kvq):
+    c = kvq.KVCache(1, 2, 64, 64, "affine_token", 4, 64, "affine_token", 4, 64)
+    k = torch.zeros(1, 2, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(kvq.KvqError, match="share one cache"):
+        kvq.kvq_append_decode_layers([c.handle, c.handle], [k, k], [k, k], kvq.DTYPES[k.dtype], [q, q], [out, out],
+                                     2, kvq.DTYPES[q.dtype])
+    assert c.stats().pos == 0
+    step = kvq.LayerStep([c], [k], [k], [q], [out])
+    c.reset()
+    with pytest.raises(ValueError, match="reset or released"):
+        step.run()
