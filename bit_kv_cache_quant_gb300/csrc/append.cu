@@ -316,7 +316,7 @@ template <typename T>
 struct BulkShape {
   static constexpr int UE = 16 / (int)sizeof(T);     // elements per 16-byte unit
   static constexpr int NU = kPart / UE;              // units per part
-  static constexpr int stages = sizeof(T) == 2 ? 3 : 2;
+  static constexpr int stages = 2;   // 64 KB per CTA for 16-bit inputs: three CTAs (24 warps) per SM
   static constexpr int stage_bytes = 2 * 8192 * (int)sizeof(T);   // K and V rows of one chunk
   static constexpr int smem = stages * stage_bytes;
 };
@@ -557,7 +557,7 @@ __device__ __forceinline__ void code_side_any(int kind, const SideView& sv, floa
 }
 
 template <typename T, int E>
-__global__ void __launch_bounds__(kBulkThreads) append_bulk_kernel(CacheView c, const T* __restrict__ k,
+__global__ void __launch_bounds__(kBulkThreads, 3) append_bulk_kernel(CacheView c, const T* __restrict__ k,
                                                                     const T* __restrict__ v, int n,
                                                                     long long hstride) {
   using S = BulkShape<T>;
