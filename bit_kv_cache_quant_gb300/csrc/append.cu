@@ -798,7 +798,7 @@ template <typename T, int E>
 static cudaError_t launch_bulk(const CacheView& c, const T* k, const T* v, int n, long long hstride, int sms,
                                cudaLaunchConfig_t cfg) {
   static std::atomic<unsigned long long> done{0};
-  static int per_sm[64];
+  static std::atomic<int> per_sm[64];   // resident CTAs per SM, per device (0 until looked up)
   constexpr int smem = BulkShape<T>::smem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -808,12 +808,13 @@ static cudaError_t launch_bulk(const CacheView& c, const T* k, const T* v, int n
     if (r != cudaSuccess) return r;
     int b = 0;
     r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, append_bulk_kernel<T, E>, kBulkThreads, smem);
-    if (r == cudaSuccess && dev >= 0 && dev < 64) per_sm[dev] = b > 0 ? b : 1;
+    if (r == cudaSuccess && dev >= 0 && dev < 64) per_sm[dev].store(b > 0 ? b : 1, std::memory_order_relaxed);
     return r;
   });
   if (e != cudaSuccess) return e;
   constexpr int rows = kBulkThreads / (E * 32 / kPart);   // tokens per chunk
-  const long long resident = (long long)(dev >= 0 && dev < 64 ? per_sm[dev] : 1) * sms;
+  const int b = dev >= 0 && dev < 64 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
+  const long long resident = (long long)(b > 0 ? b : 1) * sms;
   const long long units = (long long)c.B * c.Hkv * ((n + rows - 1) / rows);
   cfg.gridDim = dim3((unsigned)(units < resident ? units : resident));
   cfg.blockDim = dim3(kBulkThreads);
