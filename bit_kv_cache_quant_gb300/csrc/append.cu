@@ -291,10 +291,10 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
 // ---------------------------------------------------------------------------
 // Bulk append (kvq_convert, prefill-sized appends).  The input tokens of one
 // (b, kv head) are consecutive rows, so the work is cut into chunks of
-// kBulkRows(D) = 8192 / D tokens of one (b, kv head).  CTA x takes chunks
+// 256 / (D / 32) = 8192 / D tokens of one (b, kv head).  CTA x takes chunks
 // x, x + grid, ... (the grid is the resident CTA count); thread 0 copies each
 // chunk's K rows and V rows into one of the shared-memory stages with two bulk
-// copies on one mbarrier, a few chunks ahead of the chunk being coded.
+// copies on one mbarrier, one stage ahead of the chunk being coded.
 //
 // Thread t of the 256 codes channels [32 p, 32 p + 32) (its part p = t % (D /
 // 32)) of token row t / (D / 32) of the chunk, first of K, then of V, with the
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(CacheView c, 
 // groups, one 32-channel group, or half / a quarter of a 64 / 128-channel
 // group, whose range the 2 / 4 lanes of the group then combine with
 // shuffles; divisions and reciprocals are taken once per part.  Codes come
-// from one reciprocal per group (the rule of affine_code_inv): a part whose
-// quotients all stay 2^-12 away from a rounding tie keeps them, a part with
-// one near a tie (rare) codes its channels again with the exact division.
+// from one reciprocal per group (per channel for KIVI keys); a quotient
+// within 2^-13 of a rounding tie (rare) is taken again with the exact
+// division (code_side states the bound), so the bytes equal the exact rule's.
 // Parts are read from shared memory as 16-byte units, starting at unit
 // `rot` and wrapping, so that the threads of a shared-memory wavefront hit
 // distinct banks; each unit's codes are stored at the unit's own offset.
@@ -350,9 +350,11 @@ __device__ __forceinline__ int bulk_kind(const SideView& s) {
 // one staged row (x in register order: unit (jj + rot) % NU of the part in
 // slots [jj UE, jj UE + UE)), with the formats' fp32 rules, and stores the
 // codes (each unit's at its own offset) and the part's metadata.  Codes come
-// from one reciprocal per group (per channel for KIVI_CHAN) by the rule of
-// affine_code_inv: if any quotient of the part lies within 2^-12 of a
-// rounding tie (rare), the part is coded again with the exact division.
+// from one reciprocal per group (per channel for KIVI_CHAN): the product is
+// within 2^-15 of the exact quotient wherever the code depends on it, so a
+// quotient further than 2^-13 from a rounding tie rounds as the exact one
+// does; the few nearer a tie (a 16-byte unit is checked at once) are taken
+// again with the exact division.
 template <typename T, int KIND>
 __device__ __forceinline__ void code_side(const SideView& sv, float (&x)[kPart], int rot, int part, int lane,
                                           size_t orow, const float* __restrict__ bias, const KiviParams& kp) {
