@@ -291,3 +291,24 @@ def test_decode_plan_argument_checks(kvq):
         _plan(kvq, 8, sms=0, batch=1, n_kv_heads=4, capacity=100)
     with pytest.raises(kvq.KvqError):
         _plan(kvq, 8, batch=1, n_kv_heads=4, capacity=100, head_dim=96)
+
+
+def test_layer_step_argument_checks(kvq):
+    # checked on the host before any cache is touched: a layer count below 1,
+    # missing per-layer arrays, unknown flags, and two layers on one cache
+    lib = kvq.lib
+    INVALID_ARG = 1   # KVQ_ERR_INVALID_ARG
+    V = ctypes.c_void_p
+    arr = lambda *xs: (V * len(xs))(*xs)
+    one = arr(V(0x1000))
+    st = lib.kvq_append_decode_layers(0, one, one, one, 1, one, one, 3, 1, 0.0, None, None, 0, None)
+    assert st == INVALID_ARG and b"n_layers" in lib.kvq_last_error()
+    st = lib.kvq_append_decode_layers(1, None, one, one, 1, one, one, 3, 1, 0.0, None, None, 0, None)
+    assert st == INVALID_ARG and b"null per-layer array" in lib.kvq_last_error()
+    st = lib.kvq_append_decode_layers(1, one, one, one, 1, one, one, 3, 1, 0.0, None, None, 4, None)
+    assert st == INVALID_ARG and b"flags" in lib.kvq_last_error()
+    # the same handle twice (never dereferenced: the check runs first)
+    two = arr(V(0x1000), V(0x1000))
+    st = lib.kvq_append_decode_layers(2, two, two, two, 1, two, two, 3, 1, 0.0, None, None, 0, None)
+    assert st == INVALID_ARG and b"share one cache" in lib.kvq_last_error()
+    assert lib.kvq_last_launch_count() == 0
