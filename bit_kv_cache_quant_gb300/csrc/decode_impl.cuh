@@ -309,6 +309,15 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     }
     return;
   }
+  if (threadIdx.x == NTHR - 1) {
+    // every CTA of this (b, kv head) has arrived, so the counter can be reset
+    // and (fused step) every one of them has read the cache counters: the
+    // grid-wide arrival goes out now, its round trip overlapping the merge's
+    // loads, from the last thread (whose warp the float4 merge leaves idle
+    // whenever it needs fewer threads than the CTA has)
+    c.split_sem[bh] = 0u;
+    if constexpr (STEP) step_arrive(c, step);
+  }
   const float* P0 = a.partials + bh * a.nsplit * G * PROW;
   // Thread layout of the merge: SPL threads (adjacent lanes) per float4 of the
   // G x D output, each summing every SPL-th split.  The first PF partial
@@ -407,10 +416,6 @@ __device__ __forceinline__ void merge_store(const CacheView& c, const DecodeArgs
     store_io(a.out, oo + 1, a.io_dtype, A.y * inv);
     store_io(a.out, oo + 2, a.io_dtype, A.z * inv);
     store_io(a.out, oo + 3, a.io_dtype, A.w * inv);
-  }
-  if (threadIdx.x == 0) {
-    c.split_sem[bh] = 0u;
-    if constexpr (STEP) step_arrive(c, step);
   }
 }
 
