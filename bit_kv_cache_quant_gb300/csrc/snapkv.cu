@@ -360,6 +360,9 @@ __global__ void __launch_bounds__(128) snapkv_fused_kernel(const __half* __restr
   const size_t bh = (size_t)blockIdx.z * Hkv + blockIdx.y;
   const int chunk = blockIdx.x;
   const __half* kh = k + bh * head_stride * D;
+  // the top-k that follows is a programmatic dependent: it may be scheduled
+  // now (it waits for this grid to complete before reading anything)
+  grid_launch_dependents();
   prefetch_chunk_l2<D>(kh, chunk * kSnapChunk, S);
   float* mylog = sm_logit + (size_t)warp * NT * MT * 4 * 32 + lane;
 
@@ -521,6 +524,7 @@ __device__ __forceinline__ int block_excl_count_n(int v, int* total, int* warp_s
 // are then all -1.
 __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int S, int budget, int n_sink,
                                                     int* __restrict__ idx_out, const int* fail) {
+  grid_dependency_wait();   // launched as a programmatic dependent of the scoring
   extern __shared__ float sm_sc[];
   __shared__ unsigned hist[256];
   __shared__ unsigned s_bin, s_need;
@@ -628,6 +632,7 @@ __global__ void __launch_bounds__(kTopkClusterThreads) topk_cluster_kernel(const
                                                                            int budget, int n_sink,
                                                                            int* __restrict__ idx_out,
                                                                            const int* fail) {
+  grid_dependency_wait();   // launched as a programmatic dependent of the scoring
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ float sm_sc[];
@@ -852,13 +857,15 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
     cfg.blockDim = dim3(kTopkClusterThreads);
     cfg.dynamicSmemBytes = ((S + kTopkCluster - 1) / kTopkCluster) * sizeof(float);
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = kTopkCluster;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, S, budget, n_sink, idx, fail);
     note_launch();
     return e;
@@ -870,9 +877,19 @@ cudaError_t launch_topk(const float* scores, int B, int Hkv, int S, int budget, 
                                 kTopkSmemKeys * (int)sizeof(float));
   });
   if (e != cudaSuccess) return e;
-  topk_kernel<<<B * Hkv, 1024, smem, st>>>(scores, S, budget, n_sink, idx, fail);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * Hkv);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, topk_kernel, scores, S, budget, n_sink, idx, fail);
   note_launch();
-  return cudaGetLastError();
+  return e2;
 }
 
 cudaError_t launch_snapkv(const void* k, long long head_stride, int B, int Hkv, int S, int D, int w, int budget,
