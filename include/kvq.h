@@ -224,9 +224,9 @@ void kvq_cache_release(kvq_cache cache);
    channel over its R tokens, values per token) into bulk rows stored .. stored + R - 1,
    and the rest becomes the tail; the split into calls does not change the result.
    Device overflow of the bulk -> KVQ_DEV_OVERFLOW, nothing written; flags must be 0.
-   Speed only: appends of 32 or more tokens whose k and v start on 16-byte
-   boundaries are staged through shared memory by bulk copies; other appends
-   read the rows directly.  Both give the same bytes. */
+   Speed only: outside KIVI_BLOCK caches, appends of 32 or more tokens whose k
+   and v start on 16-byte boundaries are staged through shared memory by bulk
+   copies; other appends read the rows directly.  Both give the same bytes. */
 kvq_status kvq_append(kvq_cache cache, const void* k, const void* v, int32_t n_tokens, int32_t in_dtype,
                       int32_t flags, cudaStream_t stream);
 
