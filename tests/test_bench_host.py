@@ -168,3 +168,28 @@ def test_cpu_baseline_one_thread_and_all_cores():
     assert cb["nproc"] == 2 and isinstance(cb["cpu_model"], str) and cb["cpu_model"]
     ac = cb["all_cores"]
     assert ac["cores"] == 2 and ac["value"] > 0 and ac["unit"] == "GB/s" and "2 processes" in ac["sample"]
+
+
+def test_every_workload_has_a_traffic_entry_on_the_current_sources():
+    # the committed ncu DRAM figures hold for the kernel sources they were taken on:
+    # every bench workload has one, and each matches the files as they are now
+    kd = os.path.join(ROOT, "bit_kv_cache_quant_gb300")
+    for w in synth.WORKLOADS.values():
+        t = bench.profile_traffic(w.name, kd)
+        assert t is not None and t > 0, f"{w.name}: no DRAM traffic for the current sources"
+    assert bench.profile_traffic("no_such_workload", kd) is None
+
+
+def test_traffic_entry_goes_null_when_a_kernel_source_changes(tmp_path):
+    import shutil
+
+    kd = os.path.join(ROOT, "bit_kv_cache_quant_gb300")
+    copy = tmp_path / "pkg"
+    shutil.copytree(os.path.join(kd, "csrc"), copy / "csrc")
+    name = "llama3b_mlx_affine4_g64_ctx8k"
+    assert bench.profile_traffic(name, str(copy)) == bench.profile_traffic(name, kd)
+    with open(copy / "csrc" / "decode_tc.cuh", "a") as f:
+        f.write("\n// edited\n")
+    assert bench.profile_traffic(name, str(copy)) is None
+    # the SnapKV entry keys a different set of files
+    assert bench.profile_traffic("snapkv_s16k_budget512_fp16", str(copy)) is not None
