@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(TcShape<NGRP, TcHeads<G>::hg>::threads, TcShap
   // append's new token) wait for it.
   if (a.early && warp == 0) issue_ring();
   grid_dependency_wait();
-  // Every CTA of this grid is resident: the next launch may start its own
-  // prologue (and L2 requests) while this one runs.
+  // Once every CTA of this grid has passed this point (or exited), the next
+  // launch may start its own prologue (and L2 requests) while this one runs.
   grid_launch_dependents();
   if (!a.early && warp == 0) issue_ring();
   // Warp roles: 16-row block of each tile, head group, tile group.
